@@ -1,0 +1,182 @@
+"""CPU oracle (fp64, plain C) for the ternary linear layer and AdamW.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
+bench's CPU-baseline leg may import this package.  It shares no code with the
+CUDA library in ``bit_linear_gb300`` and never imports it; the two meet only in
+the seeded inputs of ``tern_synth``.
+
+The arithmetic lives in ``tern_oracle.c`` (each function cites the passage of
+the pages it follows); this module compiles it with gcc and marshals numpy
+arrays.  Every function returns fp64 results together with the sum of |term| of
+each output's dot product, the denominator of the comparison tolerance.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "tern_oracle.c")
+_LIB = os.path.join(_HERE, "libtern_oracle.so")
+
+SR4_THETA = 2      # train_gpu.cu: SR4_THETA
+SR4_Q_CLAMP = 7    # train_gpu.cu: SR4_Q_CLAMP
+
+
+def build(force: bool = False) -> str:
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-shared", "-fPIC", "-std=c11", "-fno-fast-math", "-ffp-contract=off",
+             "-o", tmp, _SRC, "-lm", "-lpthread"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+
+
+def _L():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        vp, i64, ci, dbl, flt = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double,
+                                 ctypes.c_float)
+        sig = {
+            "or_ternary": ([ci, ci], ci),
+            "or_clamp": ([ci, ci], ci),
+            "or_bf16_value": ([ctypes.c_uint16], dbl),
+            "or_bf16_round": ([dbl], ctypes.c_uint16),
+            "or_materialize": ([vp, vp, i64, i64, ci, ci, vp, vp, vp, vp, vp], None),
+            "or_fwd": ([vp, vp, vp, i64, i64, i64, ci, vp, vp, ci], None),
+            "or_dx": ([vp, vp, vp, i64, i64, i64, ci, vp, vp, ci], None),
+            "or_dw": ([vp, vp, vp, vp, i64, i64, i64, ci, vp, vp, vp, vp, ci], None),
+            "or_fwd_at": ([vp, vp, flt, i64, ci, vp, vp], None),
+            "or_dx_at": ([vp, vp, vp, i64, ci, vp, vp], None),
+            "or_gq_at": ([vp, vp, flt, i64, vp, vp], None),
+            "or_sgrad_at": ([vp, vp, vp, i64, i64, ci, vp, vp, ci], None),
+            "or_adamw": ([vp, vp, vp, vp, i64, ci, dbl, dbl, dbl, dbl, dbl, dbl, ci, vp, vp, vp], None),
+        }
+        for name, (args, res) in sig.items():
+            f = getattr(lib, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = lib
+    return _lib
+
+
+def _p(a):
+    if a is None:
+        return None
+    assert isinstance(a, np.ndarray) and a.flags["C_CONTIGUOUS"], "oracle needs C-contiguous numpy"
+    return a.ctypes.data
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def ternary(q: int, theta: int = SR4_THETA) -> int:
+    return _L().or_ternary(int(q), int(theta))
+
+
+def clamp(q: int, c: int = SR4_Q_CLAMP) -> int:
+    return _L().or_clamp(int(q), int(c))
+
+
+def bf16_value(bits: int) -> float:
+    return _L().or_bf16_value(int(bits))
+
+
+def bf16_round(x: float) -> int:
+    return int(_L().or_bf16_round(float(x)))
+
+
+def materialize(q, scale, theta=SR4_THETA, q_clamp=SR4_Q_CLAMP):
+    """Returns dict(qc, packed [K,N/16] u32, t, whi, wlo [K,N] bf16 bits)."""
+    q = _c(q, np.int8)
+    K, N = q.shape
+    scale = _c(scale, np.float32)
+    out = dict(qc=np.empty((K, N), np.int8),
+               packed=np.empty((K, N // 16), np.uint32) if N % 16 == 0 else None,
+               t=np.empty((K, N), np.uint16), whi=np.empty((K, N), np.uint16),
+               wlo=np.empty((K, N), np.uint16))
+    _L().or_materialize(_p(q), _p(scale), K, N, theta, q_clamp, _p(out["qc"]), _p(out["packed"]),
+                        _p(out["t"]), _p(out["whi"]), _p(out["wlo"]))
+    return out
+
+
+def fwd(X, q, scale, theta=SR4_THETA, nthreads=0):
+    """Y [M,N] fp64 and its abs sums."""
+    X, q, scale = _c(X, np.uint16), _c(q, np.int8), _c(scale, np.float32)
+    M, K = X.shape
+    N = q.shape[1]
+    Y, Ya = np.empty((M, N)), np.empty((M, N))
+    _L().or_fwd(_p(X), _p(q), _p(scale), M, K, N, theta, _p(Y), _p(Ya), nthreads)
+    return Y, Ya
+
+
+def dx(dY, q, scale, theta=SR4_THETA, nthreads=0):
+    dY, q, scale = _c(dY, np.uint16), _c(q, np.int8), _c(scale, np.float32)
+    M, N = dY.shape
+    K = q.shape[0]
+    out, oa = np.empty((M, K)), np.empty((M, K))
+    _L().or_dx(_p(dY), _p(q), _p(scale), M, K, N, theta, _p(out), _p(oa), nthreads)
+    return out, oa
+
+
+def dw(X, dY, q, scale, theta=SR4_THETA, nthreads=0):
+    """(gq, gq_abs) [K,N] and (sgrad, sgrad_abs) [N], fp64."""
+    X, dY, q, scale = _c(X, np.uint16), _c(dY, np.uint16), _c(q, np.int8), _c(scale, np.float32)
+    M, K = X.shape
+    N = dY.shape[1]
+    gq, gqa = np.empty((K, N)), np.empty((K, N))
+    sg, sga = np.empty(N), np.empty(N)
+    _L().or_dw(_p(X), _p(dY), _p(q), _p(scale), M, K, N, theta, _p(gq), _p(gqa), _p(sg), _p(sga),
+               nthreads)
+    return gq, gqa, sg, sga
+
+
+def fwd_at(xrow, qcol, s, theta=SR4_THETA):
+    xrow, qcol = _c(xrow, np.uint16), _c(qcol, np.int8)
+    o, oa = ctypes.c_double(), ctypes.c_double()
+    _L().or_fwd_at(_p(xrow), _p(qcol), float(s), len(xrow), theta, ctypes.byref(o), ctypes.byref(oa))
+    return o.value, oa.value
+
+
+def dx_at(dyrow, qrow, scale, theta=SR4_THETA):
+    dyrow, qrow, scale = _c(dyrow, np.uint16), _c(qrow, np.int8), _c(scale, np.float32)
+    o, oa = ctypes.c_double(), ctypes.c_double()
+    _L().or_dx_at(_p(dyrow), _p(qrow), _p(scale), len(dyrow), theta, ctypes.byref(o), ctypes.byref(oa))
+    return o.value, oa.value
+
+
+def gq_at(xcol, dycol, s):
+    xcol, dycol = _c(xcol, np.uint16), _c(dycol, np.uint16)
+    o, oa = ctypes.c_double(), ctypes.c_double()
+    _L().or_gq_at(_p(xcol), _p(dycol), float(s), len(xcol), ctypes.byref(o), ctypes.byref(oa))
+    return o.value, oa.value
+
+
+def sgrad_at(X, dycol, qcol, theta=SR4_THETA, nthreads=0):
+    X, dycol, qcol = _c(X, np.uint16), _c(dycol, np.uint16), _c(qcol, np.int8)
+    M, K = X.shape
+    o, oa = ctypes.c_double(), ctypes.c_double()
+    _L().or_sgrad_at(_p(X), _p(dycol), _p(qcol), M, K, theta, ctypes.byref(o), ctypes.byref(oa),
+                     nthreads)
+    return o.value, oa.value
+
+
+def adamw(w, g, m, v, t, lr, b1, b2, eps, wd, gmul=1.0, decoupled=True):
+    """One fp64 AdamW step; hyper-parameters are taken as fp32 then widened."""
+    w, g, m, v = (_c(a, np.float32) for a in (w, g, m, v))
+    n = w.size
+    wo, mo, vo = np.empty(n), np.empty(n), np.empty(n)
+    f32 = lambda x: float(np.float32(x))  # noqa: E731
+    _L().or_adamw(_p(w), _p(g), _p(m), _p(v), n, int(t), f32(lr), f32(b1), f32(b2), f32(eps), f32(wd),
+                  f32(gmul), 1 if decoupled else 0, _p(wo), _p(mo), _p(vo))
+    return wo, mo, vo
