@@ -1,0 +1,202 @@
+"""Python binding of libtern, the sm_103a ternary-weight linear layer library.
+
+Argument marshalling only: every step runs in the library's CUDA kernels (see
+``include/tern.h`` for the C ABI).  PyTorch supplies device memory and the
+current stream.  The functions carry the C names:
+
+    tern_materialize(q, scale, tiles, theta=2, q_clamp=7, q_clamped=None)
+    tern_linear_fwd(X, tiles, scale, Y)
+    tern_linear_bwd(X, dY, tiles, scale, dX, gq, sgrad, workspace)
+    adamw_step(w, g, m, v, t, lr, b1, b2, eps, wd, gmul=1.0, decoupled=True)
+
+Importing this package loads ``lib/libtern.so``; if it is missing the import
+fails (run ``bit_linear_gb300.build.build()`` or ``__graft_entry__.build()``).
+There is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "lib", "libtern.so")
+
+TERN_OK = 0
+TERN_ERR_ARG = -1
+TERN_ERR_ALIGN = -2
+TERN_ERR_CUDA = -3
+TERN_ERR_TIMEOUT = -4
+TERN_ERR_WORKSPACE = -5
+TERN_ERR_DEVICE = -6
+
+TERN_TILE_PACKED, TERN_TILE_T, TERN_TILE_WHI, TERN_TILE_WLO = 0, 1, 2, 3
+
+# the C ABI's exported symbols (tests check the library exports every one)
+ABI_SYMBOLS = ("tern_tiles_bytes", "tern_materialize", "tern_linear_fwd", "tern_linear_bwd_workspace",
+               "tern_linear_bwd", "adamw_step", "tern_strerror", "tern_device_status")
+
+
+class TernError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {strerror(status)} (status {status})")
+
+
+class _Tiles(ctypes.Structure):
+    _fields_ = [("packed", ctypes.c_void_p), ("t_bf16", ctypes.c_void_p),
+                ("whi_bf16", ctypes.c_void_p), ("wlo_bf16", ctypes.c_void_p)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libtern.so is not built ({LIB_PATH}); build it with bit_linear_gb300.build.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i64, ci, cf, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    tp = ctypes.POINTER(_Tiles)
+    sigs = {
+        "tern_tiles_bytes": ([i64, i64, ci], sz),
+        "tern_materialize": ([vp, vp, vp, i64, i64, ci, ci, tp, vp], ci),
+        "tern_linear_fwd": ([vp, tp, vp, vp, i64, i64, i64, vp], ci),
+        "tern_linear_bwd_workspace": ([i64, i64, i64], sz),
+        "tern_linear_bwd": ([vp, vp, tp, vp, vp, vp, vp, vp, sz, i64, i64, i64, vp], ci),
+        "adamw_step": ([vp, vp, vp, vp, i64, ci, cf, cf, cf, cf, cf, cf, ci, vp], ci),
+        "tern_strerror": ([ci], ctypes.c_char_p),
+        "tern_device_status": ([vp, ci], ci),
+    }
+    for name, (args, res) in sigs.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    return lib
+
+
+lib = _load()
+
+
+def strerror(status: int) -> str:
+    return lib.tern_strerror(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != TERN_OK:
+        raise TernError(status, where)
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t, dtype, shape=None, name="tensor"):
+    """Device pointer of a contiguous CUDA tensor of the given dtype (None -> NULL)."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+class Tiles:
+    """Caller-owned weight encodings of one K x N ternary matrix (see tern.h, tern_tiles).
+
+    packed int32 [K, N/16] (2-bit codes), t/whi/wlo bfloat16 [K, N].  Any member may be None.
+    """
+
+    def __init__(self, K, N, packed=None, t_bf16=None, whi_bf16=None, wlo_bf16=None):
+        self.K, self.N = int(K), int(N)
+        self.packed, self.t_bf16, self.whi_bf16, self.wlo_bf16 = packed, t_bf16, whi_bf16, wlo_bf16
+
+    @classmethod
+    def empty(cls, K, N, device="cuda", packed=True, t=True, hi_lo=True):
+        K, N = int(K), int(N)
+        mk = lambda shape, dt: torch.empty(shape, dtype=dt, device=device)  # noqa: E731
+        return cls(K, N,
+                   mk((K, N // 16), torch.int32) if packed else None,
+                   mk((K, N), torch.bfloat16) if t else None,
+                   mk((K, N), torch.bfloat16) if hi_lo else None,
+                   mk((K, N), torch.bfloat16) if hi_lo else None)
+
+    def _c(self) -> _Tiles:
+        K, N = self.K, self.N
+        return _Tiles(
+            _ptr(self.packed, torch.int32, (K, N // 16), "tiles.packed"),
+            _ptr(self.t_bf16, torch.bfloat16, (K, N), "tiles.t_bf16"),
+            _ptr(self.whi_bf16, torch.bfloat16, (K, N), "tiles.whi_bf16"),
+            _ptr(self.wlo_bf16, torch.bfloat16, (K, N), "tiles.wlo_bf16"))
+
+
+def tern_tiles_bytes(K, N, which) -> int:
+    return int(lib.tern_tiles_bytes(int(K), int(N), int(which)))
+
+
+def tern_materialize(q, scale, tiles: Tiles, theta=2, q_clamp=7, q_clamped=None, stream=None):
+    K, N = q.shape
+    if (tiles.K, tiles.N) != (K, N):
+        raise ValueError("tiles shape does not match q")
+    ct = tiles._c()
+    _check(lib.tern_materialize(_ptr(q, torch.int8, (K, N), "q"),
+                                _ptr(q_clamped, torch.int8, (K, N), "q_clamped"),
+                                _ptr(scale, torch.float32, (N,), "scale"),
+                                K, N, int(theta), int(q_clamp), ctypes.byref(ct), _stream(stream)),
+           "tern_materialize")
+
+
+def tern_linear_fwd(X, tiles: Tiles, scale, Y, stream=None):
+    M, K = X.shape
+    N = tiles.N
+    ct = tiles._c()
+    _check(lib.tern_linear_fwd(_ptr(X, torch.bfloat16, (M, K), "X"), ctypes.byref(ct),
+                               _ptr(scale, torch.float32, (N,), "scale"),
+                               _ptr(Y, torch.float32, (M, N), "Y"), M, K, N, _stream(stream)),
+           "tern_linear_fwd")
+
+
+def tern_linear_bwd_workspace(M, K, N) -> int:
+    return int(lib.tern_linear_bwd_workspace(int(M), int(K), int(N)))
+
+
+def tern_linear_bwd(X, dY, tiles: Tiles, scale, dX, gq, sgrad, workspace, stream=None):
+    M, K = X.shape
+    N = tiles.N
+    ct = tiles._c()
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    ws_ptr = None if workspace is None else _ptr(workspace, workspace.dtype, None, "workspace")
+    _check(lib.tern_linear_bwd(_ptr(X, torch.bfloat16, (M, K), "X"), _ptr(dY, torch.bfloat16, (M, N), "dY"),
+                               ctypes.byref(ct), _ptr(scale, torch.float32, (N,), "scale"),
+                               _ptr(dX, torch.float32, (M, K), "dX"), _ptr(gq, torch.float32, (K, N), "gq"),
+                               _ptr(sgrad, torch.float32, (N,), "sgrad"), ws_ptr, ws_bytes, M, K, N,
+                               _stream(stream)),
+           "tern_linear_bwd")
+
+
+def adamw_step(w, g, m, v, t, lr, b1, b2, eps, wd, gmul=1.0, decoupled=True, stream=None):
+    n = w.numel()
+    for name, x in (("g", g), ("m", m), ("v", v)):
+        if x.numel() != n:
+            raise ValueError(f"{name} has {x.numel()} elements, w has {n}")
+    _check(lib.adamw_step(_ptr(w, torch.float32, None, "w"), _ptr(g, torch.float32, None, "g"),
+                          _ptr(m, torch.float32, None, "m"), _ptr(v, torch.float32, None, "v"), n, int(t),
+                          float(lr), float(b1), float(b2), float(eps), float(wd), float(gmul),
+                          1 if decoupled else 0, _stream(stream)),
+           "adamw_step")
+
+
+def tern_device_status(stream=None, clear=True) -> int:
+    """Synchronise the stream; TERN_ERR_TIMEOUT if a kernel gave up on a bounded wait."""
+    return int(lib.tern_device_status(_stream(stream), 1 if clear else 0))
+
+
+def workspace_for(M, K, N, device="cuda") -> torch.Tensor:
+    nbytes = tern_linear_bwd_workspace(M, K, N)
+    return torch.empty(max(nbytes // 4, 4), dtype=torch.float32, device=device)

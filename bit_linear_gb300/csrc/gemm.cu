@@ -1,0 +1,554 @@
+// Tensor-core GEMMs of the ternary linear layer on sm_103a (tcgen05 + TMEM + TMA).
+//
+// Page "train_gpu.cu" (RWKV-x SR4 training driver): W_eff[r,c] = scale[c] *
+// ternary(q)[r,c] (header comment "Optimizer split"); the backward products
+// gq = grad*scale[c] and sgrad[c] = sum_r grad[r,c]*tern[r,c] (device glue
+// kernels tg_gq, tg_scale_grad) with grad = X^T * dY.  The pages run these as a
+// cuBLAS fp32 GEMM on a materialised W_eff followed by separate rows x cols
+// passes; here each is one persistent tensor-core kernel:
+//
+//   forward : Y[m][c]  = scale[c] * (X * T)[m][c]        scale in the epilogue
+//   dX      : dX[m][r] = (dY * W_hi^T + dY * W_lo^T)[m][r]  two MMAs per k-step
+//                        into one TMEM accumulator; W_hi/W_lo = bf16 split of
+//                        scale[c]*T, exact to 2^-17 relative
+//   dW      : G = X^T * dY kept in TMEM; the epilogue writes gq = G*scale[c] and
+//             reduces sum_r G*T per column from the 2-bit tiles (no stored G)
+//
+// GEMM convention inside a kernel: D[Mg][Ng] = sum_k A[m][k] * B[n][k], A and
+// B bf16 in shared memory, D fp32 in TMEM.  A/B are "K-major" (k contiguous in
+// global memory) or "MN-major" (m or n contiguous); both are read by TMA with
+// the 128-byte (or 64-byte) swizzle that the tcgen05 shared-memory descriptors
+// describe, so no operand is ever transposed in memory.
+//
+// Kernel shape (one CTA per SM, persistent over output tiles of 128 x BN):
+//   warp 0     TMA producer (one thread): STAGES-deep ring of operand stages
+//   warp 1     TMEM allocator + MMA issuer (one thread)
+//   warps 2-5  epilogue: TMEM -> registers -> global, one TMEM lane quarter each
+// Two TMEM accumulators (2 x BN columns) let the epilogue of tile i overlap the
+// main loop of tile i+1.
+//
+// Every mbarrier wait is bounded (globaltimer); on expiry a kernel records
+// TERN_ERR_TIMEOUT in g_gemm_status, raises a CTA-wide abort flag, waits (again
+// bounded) for its own TMA copies and MMAs in flight, frees TMEM and returns.
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace tern {
+
+__device__ int g_gemm_status;
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kThreads = 192;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait; a healthy wait takes microseconds
+
+enum { EPI_FWD = 0, EPI_DX = 1, EPI_DW = 2 };
+enum { SW128 = 2, SW64 = 4 };   // tcgen05 descriptor layout codes
+
+struct GemmArgs {
+    int Mg, Ng, Kg;
+    int tiles_m, tiles_n, num_tiles, num_kb;
+    float* out;               // [Mg][Ng] fp32 (Y, dX or gq); may be null for EPI_DW
+    const float* scale;       // [Ng] column scale (EPI_FWD, EPI_DW)
+    const uint32_t* packed;   // [Mg][Ng/16] 2-bit ternary codes (EPI_DW)
+    float* partial;           // [tiles_m*4][Ng] per-lane-quarter sgrad partials (EPI_DW)
+};
+
+template <int BN_, int BK_, bool A_MN_, bool B_MN_, int NB_, int EPI_, int STAGES_>
+struct Cfg {
+    static constexpr int BN = BN_, BK = BK_, NB = NB_, EPI = EPI_, STAGES = STAGES_;
+    static constexpr bool A_MN = A_MN_, B_MN = B_MN_;
+    static constexpr int A_BYTES = kBM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+    static_assert(BK == 64 || (BK == 32 && !A_MN && !B_MN), "MN-major operands use 64-deep k-blocks");
+    static_assert(BN % 64 == 0 && BN <= 256, "BN");
+    static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of two");
+    static_assert(SMEM_BYTES <= 232448, "shared memory");
+};
+
+using FwdCfg = Cfg<256, 64, false, true, 1, EPI_FWD, 4>;   // A = X (K-major), B = T [K][N] (MN-major)
+using DxCfg = Cfg<256, 32, false, false, 2, EPI_DX, 5>;    // A = dY (K-major), B = W_hi, W_lo (K-major)
+using DwCfg = Cfg<256, 64, true, true, 1, EPI_DW, 4>;      // A = X^T, B = dY^T (both MN-major)
+
+// tcgen05 instruction descriptor, kind::f16: bf16 A/B, fp32 D, M x N, operand majors.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool a_mn, bool b_mn) {
+    return (1u << 4)                       // D format: f32
+           | (1u << 7)                     // A format: bf16
+           | (1u << 10)                    // B format: bf16
+           | (static_cast<uint32_t>(a_mn) << 15)
+           | (static_cast<uint32_t>(b_mn) << 16)
+           | (static_cast<uint32_t>(N >> 3) << 17)
+           | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// tcgen05 shared-memory matrix descriptor.
+__device__ __forceinline__ uint64_t make_sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
+    return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+           (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) |
+           (static_cast<uint64_t>(layout) << 61);
+}
+
+// Descriptor of the kk-th 16-deep k-slice of an operand tile at `base`.
+//  K-major, BK = 64: rows of 128 B (SW128), 8-row atoms 1024 B apart; the slice
+//                    starts 32 B further along the row.
+//  K-major, BK = 32: rows of 64 B (SW64), 8-row atoms 512 B apart.
+//  MN-major (BK 64): 64-element MN chunks of BK k-rows (128 B each, SW128);
+//                    chunks LBO = 64*BK*2 B apart, 8-k-row groups SBO = 1024 B
+//                    apart; the slice starts two groups (2048 B) further.
+template <bool MN, int BK>
+__device__ __forceinline__ uint64_t op_desc(uint32_t base, int kk) {
+    if constexpr (MN) {
+        return make_sdesc(base + kk * 2048u, 64u * BK * 2u, 1024u, SW128);
+    } else if constexpr (BK == 64) {
+        return make_sdesc(base + kk * 32u, 16u, 1024u, SW128);
+    } else {
+        return make_sdesc(base + kk * 32u, 16u, 512u, SW64);
+    }
+}
+
+// Grouped raster: runs of 16 m-tiles share an n-tile, so neighbouring CTAs reuse
+// the same B panel and A panels stay resident in L2.
+__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int& mt, int& nt) {
+    constexpr int GM = 16;
+    const int group = tile / (GM * tiles_n);
+    const int first_m = group * GM;
+    const int gm = min(GM, tiles_m - first_m);
+    const int local = tile - group * GM * tiles_n;
+    mt = first_m + local % gm;
+    nt = local / gm;
+}
+
+// Bounded wait on an mbarrier phase.  Returns false on timeout (after recording
+// it) or, when `watch_abort`, once another role has raised the abort flag.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                             bool watch_abort) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (watch_abort && *abort_flag) return false;
+            if (ptx::globaltimer() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                atomicExch(&g_gemm_status, 1);
+                return false;
+            }
+        }
+    }
+}
+
+// Sum over the 32 lanes of v[0..31] (lane l's row of a 32 x 32 block); on
+// return lane l's v[0] holds the sum of column l.  Recursive halving, 31
+// shuffles, fixed order.
+__device__ __forceinline__ float warp_column_sums(float (&v)[32], int lane) {
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) {
+        const bool upper = (lane & s) != 0;
+#pragma unroll
+        for (int i = 0; i < s; ++i) {
+            const float send = upper ? v[i] : v[i + s];
+            const float keep = upper ? v[i + s] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+        }
+    }
+    return v[0];
+}
+
+template <class C>
+__device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const uint32_t (&r)[32], int row, int c0,
+                                               int mt, int quad, int lane) {
+    const bool row_ok = row < a.Mg;
+    if constexpr (C::EPI == EPI_FWD || C::EPI == EPI_DX || C::EPI == EPI_DW) {
+        if (row_ok && a.out != nullptr) {
+            float* o = a.out + static_cast<int64_t>(row) * a.Ng + c0;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if (c0 + 16 * h < a.Ng) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int j = 16 * h + 4 * q;
+                        float4 v = make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                                               __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+                        if constexpr (C::EPI != EPI_DX) {
+                            const float4 s = __ldg(reinterpret_cast<const float4*>(a.scale + c0 + j));
+                            v.x *= s.x;
+                            v.y *= s.y;
+                            v.z *= s.z;
+                            v.w *= s.w;
+                        }
+                        *reinterpret_cast<float4*>(o + j) = v;
+                    }
+                }
+            }
+        }
+    }
+    if constexpr (C::EPI == EPI_DW) {
+        // sgrad partial over this warp's 32 rows: sum_r G[r][c] * T[r][c]
+        uint32_t w0 = 0, w1 = 0;
+        if (row_ok) {
+            const uint32_t* pr = a.packed + static_cast<int64_t>(row) * (a.Ng / 16) + c0 / 16;
+            w0 = __ldg(pr);
+            if (c0 + 16 < a.Ng) w1 = __ldg(pr + 1);
+        }
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const uint32_t code = ((i < 16 ? w0 : w1) >> (2 * (i & 15))) & 3u;
+            const float g = __uint_as_float(r[i]);
+            v[i] = (code & 1u) ? ((code & 2u) ? -g : g) : 0.0f;
+        }
+        const float colsum = warp_column_sums(v, lane);
+        if (c0 + lane < a.Ng) a.partial[static_cast<int64_t>(mt * 4 + quad) * a.Ng + c0 + lane] = colsum;
+    }
+}
+
+template <class C>
+__device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensorMap* tmB0,
+                                          const CUtensorMap* tmB1, const GemmArgs& a) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + C::STAGES * C::STAGE_BYTES);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 5);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const uint32_t bar0 = ptx::smem_u32(bars);
+    const uint32_t FULL0 = bar0, EMPTY0 = bar0 + 8u * C::STAGES;
+    const uint32_t TFULL0 = bar0 + 16u * C::STAGES, TEMPTY0 = TFULL0 + 16u, DRAIN = TFULL0 + 32u;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            ptx::mbar_init(FULL0 + 8u * s, 1);
+            ptx::mbar_init(EMPTY0 + 8u * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(TFULL0 + 8u * b, 1);
+            ptx::mbar_init(TEMPTY0 + 8u * b, 4);
+        }
+        ptx::mbar_init(DRAIN, 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+        ptx::fence_proxy_async_smem();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    uint32_t issued = 0, issued_parity = 0;   // producer: stages with a copy issued, and its phase
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------------------ TMA producer
+        ptx::tma_prefetch_desc(tmA);
+        ptx::tma_prefetch_desc(tmB0);
+        if (C::NB == 2) ptx::tma_prefetch_desc(tmB1);
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < a.num_tiles; tile += gridDim.x) {
+            int mt, nt;
+            tile_coords(tile, a.tiles_m, a.tiles_n, mt, nt);
+            for (int kb = 0; kb < a.num_kb; ++kb) {
+                if (!wait_bounded(EMPTY0 + 8u * stage, phase ^ 1u, abort_flag, true)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t full = FULL0 + 8u * stage;
+                const uint32_t sA = base + stage * C::STAGE_BYTES;
+                const uint32_t sB0 = sA + C::A_BYTES;
+                ptx::mbar_arrive_expect_tx(full, C::STAGE_BYTES);
+                const int k0 = kb * C::BK;
+                if constexpr (C::A_MN) {
+#pragma unroll
+                    for (int j = 0; j < kBM / 64; ++j)
+                        ptx::tma_load_2d(sA + j * 64 * C::BK * 2, tmA, mt * kBM + j * 64, k0, full);
+                } else {
+                    ptx::tma_load_2d(sA, tmA, k0, mt * kBM, full);
+                }
+#pragma unroll
+                for (int b = 0; b < C::NB; ++b) {
+                    const CUtensorMap* tmB = b == 0 ? tmB0 : tmB1;
+                    const uint32_t sB = sB0 + b * C::B_BYTES;
+                    if constexpr (C::B_MN) {
+#pragma unroll
+                        for (int j = 0; j < C::BN / 64; ++j)
+                            ptx::tma_load_2d(sB + j * 64 * C::BK * 2, tmB, nt * C::BN + j * 64, k0, full);
+                    } else {
+                        ptx::tma_load_2d(sB, tmB, k0, nt * C::BN, full);
+                    }
+                }
+                issued |= 1u << stage;
+                issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                if (++stage == C::STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------------------ MMA issuer
+        constexpr uint32_t IDESC = make_idesc(kBM, C::BN, C::A_MN, C::B_MN);
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        int local = 0;
+        for (int tile = blockIdx.x; ok && tile < a.num_tiles; tile += gridDim.x, ++local) {
+            const int acc = local & 1;
+            const uint32_t acc_parity = (local >> 1) & 1;
+            if (!wait_bounded(TEMPTY0 + 8u * acc, acc_parity ^ 1u, abort_flag, true)) break;
+            ptx::tc_fence_after();
+            const uint32_t d_tmem = tmem_base + acc * C::BN;
+            for (int kb = 0; kb < a.num_kb; ++kb) {
+                if (!wait_bounded(FULL0 + 8u * stage, phase, abort_flag, true)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t sA = base + stage * C::STAGE_BYTES;
+                const uint32_t sB0 = sA + C::A_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < C::BK / 16; ++kk) {
+                    const uint64_t da = op_desc<C::A_MN, C::BK>(sA, kk);
+                    ptx::mma_bf16(d_tmem, da, op_desc<C::B_MN, C::BK>(sB0, kk), IDESC, (kb | kk) != 0);
+                    if constexpr (C::NB == 2)
+                        ptx::mma_bf16(d_tmem, da, op_desc<C::B_MN, C::BK>(sB0 + C::B_BYTES, kk), IDESC, 1u);
+                }
+                ptx::mma_commit(EMPTY0 + 8u * stage);   // frees the stage once these MMAs are done
+                if (++stage == C::STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            ptx::mma_commit(TFULL0 + 8u * acc);          // accumulator ready for the epilogue
+        }
+        // every MMA this thread issued completes before TMEM and shared memory go away
+        ptx::mma_commit(DRAIN);
+        wait_bounded(DRAIN, 0, abort_flag, false);
+    } else if (warp >= 2) {
+        // ------------------------------------------------------------ epilogue
+        const int quad = warp & 3;   // a warp may touch TMEM lanes 32*(warp%4) .. +31
+        int local = 0;
+        for (int tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x, ++local) {
+            const int acc = local & 1;
+            const uint32_t acc_parity = (local >> 1) & 1;
+            if (!wait_bounded(TFULL0 + 8u * acc, acc_parity, abort_flag, true)) break;
+            ptx::tc_fence_after();
+            int mt, nt;
+            tile_coords(tile, a.tiles_m, a.tiles_n, mt, nt);
+            const int row = mt * kBM + quad * 32 + lane;
+            const uint32_t trow = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * C::BN;
+#pragma unroll 1
+            for (int j = 0; j < C::BN / 32; ++j) {
+                const int c0 = nt * C::BN + j * 32;
+                if (c0 >= a.Ng) break;
+                uint32_t r[32];
+                ptx::tmem_ld_32x32b_x32(trow + j * 32, r);
+                ptx::tmem_wait_ld();
+                epilogue_chunk<C>(a, r, row, c0, mt, quad, lane);
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(TEMPTY0 + 8u * acc);
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+    if (warp == 0 && lane == 0 && *abort_flag) {
+        // after an abort, copies still in flight must land before the CTA's shared memory is released
+        for (int s = 0; s < C::STAGES; ++s)
+            if (issued & (1u << s)) wait_bounded(FULL0 + 8u * s, (issued_parity >> s) & 1u, abort_flag, false);
+    }
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads, 1)
+    tern_fwd_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                  const GemmArgs a) {
+    gemm_body<FwdCfg>(&tmA, &tmB, &tmB, a);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    tern_dx_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmBhi,
+                 const __grid_constant__ CUtensorMap tmBlo, const GemmArgs a) {
+    gemm_body<DxCfg>(&tmA, &tmBhi, &tmBlo, a);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    tern_dw_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const GemmArgs a) {
+    gemm_body<DwCfg>(&tmA, &tmB, &tmB, a);
+}
+
+// sgrad[c] = sum over the partial rows in ascending order (deterministic).
+__global__ void tern_sgrad_reduce(const float* __restrict__ partial, int nparts, int N, float* __restrict__ sgrad) {
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= N) return;
+    float s = 0.0f;
+    for (int i = 0; i < nparts; ++i) s += partial[static_cast<int64_t>(i) * N + c];
+    sgrad[c] = s;
+}
+
+// ===================================================================== host side
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Tensor map of a row-major bf16 matrix [outer][inner] read in boxes of box_outer x box_inner.
+int map_bf16(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, int box_inner, int box_outer,
+             CUtensorMapSwizzle sw) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return TERN_ERR_CUDA;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? TERN_OK : TERN_ERR_CUDA;
+}
+
+template <class C>
+GemmArgs make_args(int64_t Mg, int64_t Ng, int64_t Kg) {
+    GemmArgs a{};
+    a.Mg = static_cast<int>(Mg);
+    a.Ng = static_cast<int>(Ng);
+    a.Kg = static_cast<int>(Kg);
+    a.tiles_m = static_cast<int>((Mg + kBM - 1) / kBM);
+    a.tiles_n = static_cast<int>((Ng + C::BN - 1) / C::BN);
+    a.num_tiles = a.tiles_m * a.tiles_n;
+    a.num_kb = static_cast<int>((Kg + C::BK - 1) / C::BK);
+    return a;
+}
+
+template <class C, class K, class... Maps>
+int launch(K kernel, const GemmArgs& a, int num_sms, cudaStream_t s, const Maps&... maps) {
+    TERN_CUDA_TRY(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES));
+    const int grid = std::min(a.num_tiles, num_sms);
+    kernel<<<grid, kThreads, C::SMEM_BYTES, s>>>(maps..., a);
+    TERN_CUDA_TRY(cudaGetLastError());
+    return TERN_OK;
+}
+
+bool dims_ok(int64_t M, int64_t K, int64_t N) {
+    return M >= 1 && K >= 16 && N >= 16 && M < (1ll << 31) && K < (1ll << 31) && N < (1ll << 31) &&
+           M * K < (1ll << 40) && K * N < (1ll << 40) && M * N < (1ll << 40);
+}
+
+}  // namespace
+
+int gemm_status_read(int clear) {
+    int v = 0;
+    TERN_CUDA_TRY(cudaMemcpyFromSymbol(&v, g_gemm_status, sizeof(int)));
+    if (clear) {
+        const int zero = 0;
+        TERN_CUDA_TRY(cudaMemcpyToSymbol(g_gemm_status, &zero, sizeof(int)));
+    }
+    return v ? TERN_ERR_TIMEOUT : TERN_OK;
+}
+
+}  // namespace tern
+
+using namespace tern;
+
+extern "C" int tern_linear_fwd(const uint16_t* X, const tern_tiles* W, const float* scale, float* Y, int64_t M,
+                               int64_t K, int64_t N, void* stream) {
+    if (!X || !W || !W->t_bf16 || !scale || !Y) return TERN_ERR_ARG;
+    if (!dims_ok(M, K, N)) return TERN_ERR_ARG;
+    if (K % 16 || N % 16) return TERN_ERR_ALIGN;
+    if (!aligned16(X) || !aligned16(W->t_bf16) || !aligned16(scale) || !aligned16(Y)) return TERN_ERR_ALIGN;
+    int num_sms = 0;
+    if (int st = check_device(&num_sms)) return st;
+    CUtensorMap mA, mB;
+    if (int st = map_bf16(&mA, X, K, M, 64, kBM, CU_TENSOR_MAP_SWIZZLE_128B)) return st;
+    if (int st = map_bf16(&mB, W->t_bf16, N, K, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)) return st;
+    GemmArgs a = make_args<FwdCfg>(M, N, K);
+    a.out = Y;
+    a.scale = scale;
+    return launch<FwdCfg>(tern_fwd_gemm, a, num_sms, static_cast<cudaStream_t>(stream), mA, mB);
+}
+
+extern "C" size_t tern_linear_bwd_workspace(int64_t M, int64_t K, int64_t N) {
+    if (!dims_ok(M, K, N)) return 0;
+    const int64_t tiles_r = (K + kBM - 1) / kBM;
+    return static_cast<size_t>(tiles_r * 4 * N) * sizeof(float);
+}
+
+extern "C" int tern_linear_bwd(const uint16_t* X, const uint16_t* dY, const tern_tiles* W, const float* scale,
+                               float* dX, float* gq, float* sgrad, void* workspace, size_t ws_bytes, int64_t M,
+                               int64_t K, int64_t N, void* stream) {
+    if (!X || !dY || !W || !W->packed || !scale || !sgrad) return TERN_ERR_ARG;
+    if (dX && (!W->whi_bf16 || !W->wlo_bf16)) return TERN_ERR_ARG;
+    if (!dims_ok(M, K, N)) return TERN_ERR_ARG;
+    if (K % 16 || N % 16) return TERN_ERR_ALIGN;
+    if (!aligned16(X) || !aligned16(dY) || !aligned16(W->packed) || !aligned16(scale) || !aligned16(sgrad) ||
+        !aligned16(workspace) || (gq && !aligned16(gq)))
+        return TERN_ERR_ALIGN;
+    if (dX && (!aligned16(dX) || !aligned16(W->whi_bf16) || !aligned16(W->wlo_bf16))) return TERN_ERR_ALIGN;
+    const size_t need = tern_linear_bwd_workspace(M, K, N);
+    if (!workspace || ws_bytes < need) return TERN_ERR_WORKSPACE;
+    int num_sms = 0;
+    if (int st = check_device(&num_sms)) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    if (dX) {
+        CUtensorMap mA, mHi, mLo;
+        if (int st = map_bf16(&mA, dY, N, M, 32, kBM, CU_TENSOR_MAP_SWIZZLE_64B)) return st;
+        if (int st = map_bf16(&mHi, W->whi_bf16, N, K, 32, DxCfg::BN, CU_TENSOR_MAP_SWIZZLE_64B)) return st;
+        if (int st = map_bf16(&mLo, W->wlo_bf16, N, K, 32, DxCfg::BN, CU_TENSOR_MAP_SWIZZLE_64B)) return st;
+        GemmArgs a = make_args<DxCfg>(M, K, N);
+        a.out = dX;
+        if (int st = launch<DxCfg>(tern_dx_gemm, a, num_sms, s, mA, mHi, mLo)) return st;
+    }
+    {
+        CUtensorMap mA, mB;
+        if (int st = map_bf16(&mA, X, K, M, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)) return st;
+        if (int st = map_bf16(&mB, dY, N, M, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)) return st;
+        GemmArgs a = make_args<DwCfg>(K, N, M);
+        a.out = gq;
+        a.scale = scale;
+        a.packed = W->packed;
+        a.partial = static_cast<float*>(workspace);
+        if (int st = launch<DwCfg>(tern_dw_gemm, a, num_sms, s, mA, mB)) return st;
+        const int nparts = a.tiles_m * 4;
+        tern_sgrad_reduce<<<static_cast<unsigned>((N + 255) / 256), 256, 0, s>>>(a.partial, nparts,
+                                                                                 static_cast<int>(N), sgrad);
+        TERN_CUDA_TRY(cudaGetLastError());
+    }
+    return TERN_OK;
+}

@@ -1,0 +1,145 @@
+/*
+ * tern.h — C ABI of the GB300 (sm_103a) ternary-weight linear layer library.
+ *
+ * The layer (page "train_gpu.cu", header comment "Optimizer split" and the device
+ * glue kernels tg_tern_from_q / tg_apply_scale / tg_gq / tg_scale_grad):
+ *
+ *   ternary(q)[r,c] = +1 if q >= theta, -1 if q <= -theta, else 0
+ *   W_eff[r,c]      = scale[c] * ternary(q)[r,c]        (row-major [K][N])
+ *   Y               = X * W_eff                          (forward)
+ *   dX              = dY * W_eff^T                       (input gradient)
+ *   gq[r,c]         = (X^T * dY)[r,c] * scale[c]         (straight-through gradient)
+ *   sgrad[c]        = sum_r (X^T * dY)[r,c] * ternary(q)[r,c]   (scale gradient)
+ *
+ * followed by AdamW on continuous parameters, the scales included (same page,
+ * resident optimizer launchers: adamw_dev and its bias corrections 1 - beta^t).
+ *
+ * Shapes: M tokens, K input features (rows r of q), N output features (columns
+ * c of q).  Every matrix is row-major and dense.  Element types: X, dY bf16 (as
+ * uint16 bit patterns), q int8, scale and every output fp32.
+ *
+ * Ownership and ordering: the caller allocates and owns every buffer (device
+ * memory unless stated otherwise).  No call allocates, frees or synchronises.
+ * Each call enqueues its kernels on `stream` (a cudaStream_t; NULL is the
+ * legacy default stream) and returns once they are enqueued; outputs are valid
+ * when the stream reaches that point.  Calls may be captured into a CUDA graph
+ * after the first call on a device (which loads the driver's tensor-map
+ * encoder).  Inputs must not alias outputs.
+ *
+ * Errors: every call returns TERN_OK (0) or a negative status, checks its
+ * arguments before enqueueing anything, and never exits the process.  Kernels
+ * that wait on the tensor-core pipeline give up after a bounded time and
+ * record TERN_ERR_TIMEOUT in a device status word that tern_device_status()
+ * reads back.
+ */
+#ifndef TERN_H
+#define TERN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TERN_OK 0
+#define TERN_ERR_ARG (-1)         /* null pointer, non-positive size, theta < 1, clamp < theta */
+#define TERN_ERR_ALIGN (-2)       /* K or N not a multiple of 16, pointer not 16-byte aligned */
+#define TERN_ERR_CUDA (-3)        /* a CUDA runtime/driver call failed (launch, attribute, map) */
+#define TERN_ERR_TIMEOUT (-4)     /* a bounded device-side wait gave up */
+#define TERN_ERR_WORKSPACE (-5)   /* workspace smaller than tern_linear_bwd_workspace() */
+#define TERN_ERR_DEVICE (-6)      /* current device is not an sm_103 (GB300) part */
+
+/* Weight operands produced by tern_materialize from q and scale; caller-owned
+ * device buffers.  Any pointer may be NULL to skip that output; the GEMM calls
+ * state which ones they read. */
+typedef struct tern_tiles {
+    uint32_t* packed;   /* [K][N/16] 2-bit codes, element (r,c) at word r*(N/16)+c/16,
+                           bits 2*(c%16): 0 -> 00, +1 -> 01, -1 -> 11 (10 never written) */
+    uint16_t* t_bf16;   /* [K][N] bf16 of ternary(q): 0x0000, 0x3F80, 0xBF80 (forward operand) */
+    uint16_t* whi_bf16; /* [K][N] bf16 of s_hi[c]*ternary(q), s_hi = bf16_rne(scale[c]) */
+    uint16_t* wlo_bf16; /* [K][N] bf16 of s_lo[c]*ternary(q), s_lo = bf16_rne(scale[c]-s_hi) */
+} tern_tiles;
+
+#define TERN_TILE_PACKED 0
+#define TERN_TILE_T 1
+#define TERN_TILE_WHI 2
+#define TERN_TILE_WLO 3
+
+/* Bytes of one tern_tiles buffer (`which` = TERN_TILE_*) for a K x N weight; 0 on bad args. */
+size_t tern_tiles_bytes(int64_t K, int64_t N, int which);
+
+/*
+ * Ternarise and encode one weight matrix (page "train_gpu.cu", tg_tern_from_q,
+ * and the accumulator clamp SR4_Q_CLAMP).
+ *   q         [K][N] int8 accumulator (device, read)
+ *   q_clamped [K][N] int8, min(max(q,-q_clamp),q_clamp) (device, written; NULL to skip;
+ *             may equal q for an in-place clamp)
+ *   scale     [N] fp32 (device, read; may be NULL when out->whi_bf16 and out->wlo_bf16 are NULL)
+ *   out       tiles to write (host struct of device pointers; NULL members skipped)
+ *   theta >= 1, q_clamp >= theta (clamping then keeps every ternary value).
+ * K >= 1, N >= 16 with N % 16 == 0; every pointer 16-byte aligned.  Bit-exact.
+ */
+int tern_materialize(const int8_t* q, int8_t* q_clamped, const float* scale, int64_t K, int64_t N,
+                     int theta, int q_clamp, const tern_tiles* out, void* stream);
+
+/*
+ * Forward: Y[m][c] = scale[c] * sum_r X[m][r] * T[r][c] (page "train_gpu.cu",
+ * header comment: W_eff = scale[c]*ternary(q); the forward GEMM itself is the
+ * off-page fm_forward).  The scale is applied in the epilogue, so W_eff is never
+ * formed.  Reads W->t_bf16.
+ *   X [M][K] bf16 (device), scale [N] fp32 (device), Y [M][N] fp32 (device, written).
+ * M >= 1; K, N >= 16 and multiples of 16; pointers 16-byte aligned.
+ * Tensor cores, bf16 x {-1,0,+1} products (exact), fp32 accumulation.
+ */
+int tern_linear_fwd(const uint16_t* X, const tern_tiles* W, const float* scale, float* Y, int64_t M,
+                    int64_t K, int64_t N, void* stream);
+
+/* Bytes of device workspace tern_linear_bwd needs for sgrad's per-tile partials. */
+size_t tern_linear_bwd_workspace(int64_t M, int64_t K, int64_t N);
+
+/*
+ * Backward (page "train_gpu.cu": the backward GEMMs are the off-page fm_backward;
+ * tg_gq and tg_scale_grad give gq and sgrad from grad = X^T * dY).
+ *   dX[m][r]  = sum_c dY[m][c] * scale[c] * T[r][c]   fp32 [M][K]  (NULL to skip)
+ *               computed as dY*W_hi^T + dY*W_lo^T (reads W->whi_bf16, W->wlo_bf16)
+ *   gq[r][c]  = G[r][c] * scale[c], G = X^T * dY      fp32 [K][N]
+ *   sgrad[c]  = sum_r G[r][c] * T[r][c]               fp32 [N]    (reads W->packed)
+ * gq and sgrad come from one fused epilogue of the G GEMM; G itself is never
+ * stored.  sgrad is reduced over r in a fixed order (deterministic run to run).
+ *   X [M][K] bf16, dY [M][N] bf16, scale [N] fp32: device, read.
+ *   workspace: device, >= tern_linear_bwd_workspace(M,K,N) bytes, 16-byte aligned,
+ *   contents ignored and overwritten (may be NULL when that size is 0).
+ * Same shape rules as the forward.
+ */
+int tern_linear_bwd(const uint16_t* X, const uint16_t* dY, const tern_tiles* W, const float* scale,
+                    float* dX, float* gq, float* sgrad, void* workspace, size_t ws_bytes, int64_t M,
+                    int64_t K, int64_t N, void* stream);
+
+/*
+ * AdamW on n fp32 elements (page "train_gpu.cu", adamw_dev: bias corrections
+ * bc_i = 1 - beta_i^t, is_adamw; page "heal_gpu.rs": eps outside the root).
+ *   g' = gmul*g (+ wd*w when decoupled == 0)
+ *   m  = b1*m + (1-b1)*g';  v = b2*v + (1-b2)*g'^2
+ *   w  = w - [decoupled] lr*wd*w - lr*(m/bc1)/(sqrt(v/bc2)+eps)      (decay uses the old w)
+ * w, m, v updated in place; g read.  All device, 16-byte aligned; t >= 1; n >= 0
+ * (n == 0 enqueues nothing).  gmul is the page's scale_lr/lr factor (1 for none).
+ */
+int adamw_step(float* w, const float* g, float* m, float* v, int64_t n, int t, float lr, float b1,
+               float b2, float eps, float wd, float gmul, int decoupled, void* stream);
+
+/* Text of a status code (static storage). */
+const char* tern_strerror(int status);
+
+/*
+ * Synchronise `stream`, then return TERN_ERR_TIMEOUT if any kernel since the last
+ * clear gave up on a bounded wait, else TERN_OK (TERN_ERR_CUDA if the sync fails).
+ * clear != 0 resets the device status word.  This is the one call that blocks.
+ */
+int tern_device_status(void* stream, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TERN_H */

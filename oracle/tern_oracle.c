@@ -89,6 +89,8 @@ uint16_t or_bf16_round(double x) {
  *   t      [K][N]    bf16 of T (may be NULL)
  *   whi    [K][N]    bf16 of s_hi[c]*T, s_hi = bf16(scale[c]) (may be NULL)
  *   wlo    [K][N]    bf16 of s_lo[c]*T, s_lo = bf16(scale[c] - s_hi) (may be NULL)
+ *                    (T = 0 gives +0 = 0x0000 in t, whi and wlo; T = -1 with
+ *                    s_lo = +0 gives -0 = 0x8000, the IEEE product)
  * N must be a multiple of 16 when packed is requested.
  */
 void or_materialize(const int8_t* q, const float* scale, int64_t K, int64_t N, int theta, int clamp,
@@ -110,8 +112,9 @@ void or_materialize(const int8_t* q, const float* scale, int64_t K, int64_t N, i
                 double s = (double)scale[c];
                 double shi = or_bf16_value(or_bf16_round(s));
                 double slo = or_bf16_value(or_bf16_round(s - shi));
-                if (whi) whi[i] = or_bf16_round(shi * w);
-                if (wlo) wlo[i] = or_bf16_round(slo * w);
+                /* a zero weight encodes as +0 in every plane */
+                if (whi) whi[i] = w == 0 ? 0x0000u : or_bf16_round(shi * w);
+                if (wlo) wlo[i] = w == 0 ? 0x0000u : or_bf16_round(slo * w);
             }
         }
     }

@@ -1,0 +1,114 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every function the
+header declares, and rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bit_linear_gb300 import build as b
+    b.build()
+    import bit_linear_gb300 as bl
+    return bl
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "tern.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_four_calls():
+    names = _declared()
+    for n in ("tern_materialize", "tern_linear_fwd", "tern_linear_bwd", "adamw_step"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    so = ctypes.CDLL(lib.LIB_PATH)
+    for name in _declared():
+        assert hasattr(so, name), f"libtern.so does not export {name}"
+    assert set(_declared()) == set(lib.ABI_SYMBOLS)
+
+
+def test_strerror_covers_every_status(lib):
+    for st in (0, -1, -2, -3, -4, -5, -6):
+        assert lib.strerror(st) and lib.strerror(st) != "unknown status"
+    assert lib.strerror(-99) == "unknown status"
+
+
+def test_sizes(lib):
+    assert lib.tern_tiles_bytes(4096, 12288, lib.TERN_TILE_PACKED) == 4096 * 768 * 4
+    assert lib.tern_tiles_bytes(4096, 12288, lib.TERN_TILE_T) == 4096 * 12288 * 2
+    assert lib.tern_tiles_bytes(7, 24, lib.TERN_TILE_T) == 0           # N not a multiple of 16
+    assert lib.tern_tiles_bytes(7, 32, 9) == 0
+    assert lib.tern_linear_bwd_workspace(32768, 4096, 12288) == 32 * 4 * 12288 * 4
+    assert lib.tern_linear_bwd_workspace(64, 129, 16) == 2 * 4 * 16 * 4
+    assert lib.tern_linear_bwd_workspace(0, 16, 16) == 0
+
+
+P = ctypes.c_void_p
+
+
+def _tiles(lib, base=0x10000):
+    return lib._Tiles(P(base), P(base + 0x1000), P(base + 0x2000), P(base + 0x3000))
+
+
+def test_forward_argument_checks(lib):
+    f = lib.lib.tern_linear_fwd
+    t = _tiles(lib)
+    ok = (P(0x20000), ctypes.byref(t), P(0x30000), P(0x40000))
+    assert f(None, ctypes.byref(t), P(0x30000), P(0x40000), 64, 128, 128, None) == lib.TERN_ERR_ARG
+    assert f(*ok, 0, 128, 128, None) == lib.TERN_ERR_ARG           # M = 0
+    assert f(*ok, 64, 8, 128, None) == lib.TERN_ERR_ARG            # K < 16
+    assert f(*ok, 64, 24 + 16, 128, None) == lib.TERN_ERR_ALIGN    # K = 40
+    assert f(*ok, 64, 128, 136, None) == lib.TERN_ERR_ALIGN        # N = 136
+    assert f(P(0x20002), ctypes.byref(t), P(0x30000), P(0x40000), 64, 128, 128, None) == lib.TERN_ERR_ALIGN
+    nul = lib._Tiles(P(0x10000), None, None, None)                 # no bf16 T operand
+    assert f(P(0x20000), ctypes.byref(nul), P(0x30000), P(0x40000), 64, 128, 128, None) == lib.TERN_ERR_ARG
+
+
+def test_backward_argument_checks(lib):
+    f = lib.lib.tern_linear_bwd
+    t = _tiles(lib)
+    args = lambda dX, ws, n: (P(0x20000), P(0x21000), ctypes.byref(t), P(0x30000), dX, P(0x50000),  # noqa
+                              P(0x60000), ws, n, 64, 128, 128, None)
+    need = lib.tern_linear_bwd_workspace(64, 128, 128)
+    assert f(*args(P(0x40000), P(0x70000), need - 4)) == lib.TERN_ERR_WORKSPACE
+    assert f(*args(P(0x40000), None, need)) == lib.TERN_ERR_WORKSPACE
+    nohl = lib._Tiles(P(0x10000), P(0x11000), None, None)           # dX asked without W_hi/W_lo
+    assert f(P(0x20000), P(0x21000), ctypes.byref(nohl), P(0x30000), P(0x40000), P(0x50000), P(0x60000),
+             P(0x70000), need, 64, 128, 128, None) == lib.TERN_ERR_ARG
+    assert f(P(0x20000), P(0x21000), ctypes.byref(t), P(0x30000), P(0x40004), P(0x50000), P(0x60000),
+             P(0x70000), need, 64, 128, 128, None) == lib.TERN_ERR_ALIGN
+    assert f(P(0x20000), P(0x21000), ctypes.byref(t), P(0x30000), P(0x40000), P(0x50000), None,
+             P(0x70000), need, 64, 128, 128, None) == lib.TERN_ERR_ARG     # sgrad is required
+
+
+def test_materialize_argument_checks(lib):
+    f = lib.lib.tern_materialize
+    t = _tiles(lib)
+    q, s = P(0x20000), P(0x30000)
+    assert f(q, None, s, 16, 32, 0, 7, ctypes.byref(t), None) == lib.TERN_ERR_ARG      # theta < 1
+    assert f(q, None, s, 16, 32, 3, 2, ctypes.byref(t), None) == lib.TERN_ERR_ARG      # clamp < theta
+    assert f(q, None, s, 16, 32, 2, 128, ctypes.byref(t), None) == lib.TERN_ERR_ARG    # clamp > 127
+    assert f(q, None, None, 16, 32, 2, 7, ctypes.byref(t), None) == lib.TERN_ERR_ARG   # hi/lo need scale
+    assert f(q, None, s, 16, 40, 2, 7, ctypes.byref(t), None) == lib.TERN_ERR_ALIGN
+    assert f(P(0x20001), None, s, 16, 32, 2, 7, ctypes.byref(t), None) == lib.TERN_ERR_ALIGN
+    assert f(q, None, s, 0, 32, 2, 7, ctypes.byref(t), None) == lib.TERN_ERR_ARG
+
+
+def test_adamw_argument_checks(lib):
+    f = lib.lib.adamw_step
+    a = (P(0x10000), P(0x20000), P(0x30000), P(0x40000))
+    hp = (1e-3, 0.9, 0.95, 1e-8, 0.1, 1.0, 1, None)
+    assert f(*a, 0, 1, *hp) == lib.TERN_OK           # nothing to do: nothing enqueued
+    assert f(*a, -1, 1, *hp) == lib.TERN_ERR_ARG
+    assert f(*a, 10, 0, *hp) == lib.TERN_ERR_ARG     # t >= 1
+    assert f(P(0x10008), *a[1:], 10, 1, *hp) == lib.TERN_ERR_ALIGN
+    assert f(None, *a[1:], 10, 1, *hp) == lib.TERN_ERR_ARG
