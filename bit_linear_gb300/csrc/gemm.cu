@@ -189,6 +189,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const uint32_t
         }
     }
     if constexpr (C::EPI == EPI_DW) {
+        if (a.partial == nullptr) return;   // gq only
         // sgrad partial over this warp's 32 rows: sum_r G[r][c] * T[r][c]
         uint32_t w0 = 0, w1 = 0;
         if (row_ok) {
@@ -512,16 +513,17 @@ extern "C" size_t tern_linear_bwd_workspace(int64_t M, int64_t K, int64_t N) {
 extern "C" int tern_linear_bwd(const uint16_t* X, const uint16_t* dY, const tern_tiles* W, const float* scale,
                                float* dX, float* gq, float* sgrad, void* workspace, size_t ws_bytes, int64_t M,
                                int64_t K, int64_t N, void* stream) {
-    if (!X || !dY || !W || !W->packed || !scale || !sgrad) return TERN_ERR_ARG;
+    if (!X || !dY || !W || !scale) return TERN_ERR_ARG;
     if (dX && (!W->whi_bf16 || !W->wlo_bf16)) return TERN_ERR_ARG;
+    if (sgrad && !W->packed) return TERN_ERR_ARG;
+    if (!dX && !gq && !sgrad) return TERN_ERR_ARG;
     if (!dims_ok(M, K, N)) return TERN_ERR_ARG;
     if (K % 16 || N % 16) return TERN_ERR_ALIGN;
-    if (!aligned16(X) || !aligned16(dY) || !aligned16(W->packed) || !aligned16(scale) || !aligned16(sgrad) ||
-        !aligned16(workspace) || (gq && !aligned16(gq)))
-        return TERN_ERR_ALIGN;
+    if (!aligned16(X) || !aligned16(dY) || !aligned16(scale)) return TERN_ERR_ALIGN;
+    if (sgrad && (!aligned16(sgrad) || !aligned16(W->packed) || !aligned16(workspace))) return TERN_ERR_ALIGN;
+    if (gq && !aligned16(gq)) return TERN_ERR_ALIGN;
     if (dX && (!aligned16(dX) || !aligned16(W->whi_bf16) || !aligned16(W->wlo_bf16))) return TERN_ERR_ALIGN;
-    const size_t need = tern_linear_bwd_workspace(M, K, N);
-    if (!workspace || ws_bytes < need) return TERN_ERR_WORKSPACE;
+    if (sgrad && (!workspace || ws_bytes < tern_linear_bwd_workspace(M, K, N))) return TERN_ERR_WORKSPACE;
     int num_sms = 0;
     if (int st = check_device(&num_sms)) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -535,7 +537,7 @@ extern "C" int tern_linear_bwd(const uint16_t* X, const uint16_t* dY, const tern
         a.out = dX;
         if (int st = launch<DxCfg>(tern_dx_gemm, a, num_sms, s, mA, mHi, mLo)) return st;
     }
-    {
+    if (gq || sgrad) {
         CUtensorMap mA, mB;
         if (int st = map_bf16(&mA, X, K, M, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)) return st;
         if (int st = map_bf16(&mB, dY, N, M, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)) return st;
@@ -543,8 +545,9 @@ extern "C" int tern_linear_bwd(const uint16_t* X, const uint16_t* dY, const tern
         a.out = gq;
         a.scale = scale;
         a.packed = W->packed;
-        a.partial = static_cast<float*>(workspace);
+        a.partial = sgrad ? static_cast<float*>(workspace) : nullptr;
         if (int st = launch<DwCfg>(tern_dw_gemm, a, num_sms, s, mA, mB)) return st;
+        if (!sgrad) return TERN_OK;
         const int nparts = a.tiles_m * 4;
         tern_sgrad_reduce<<<static_cast<unsigned>((N + 255) / 256), 256, 0, s>>>(a.partial, nparts,
                                                                                  static_cast<int>(N), sgrad);

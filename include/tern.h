@@ -103,13 +103,17 @@ size_t tern_linear_bwd_workspace(int64_t M, int64_t K, int64_t N);
  * tg_gq and tg_scale_grad give gq and sgrad from grad = X^T * dY).
  *   dX[m][r]  = sum_c dY[m][c] * scale[c] * T[r][c]   fp32 [M][K]  (NULL to skip)
  *               computed as dY*W_hi^T + dY*W_lo^T (reads W->whi_bf16, W->wlo_bf16)
- *   gq[r][c]  = G[r][c] * scale[c], G = X^T * dY      fp32 [K][N]
- *   sgrad[c]  = sum_r G[r][c] * T[r][c]               fp32 [N]    (reads W->packed)
+ *   gq[r][c]  = G[r][c] * scale[c], G = X^T * dY      fp32 [K][N]  (NULL to skip)
+ *   sgrad[c]  = sum_r G[r][c] * T[r][c]               fp32 [N]    (NULL to skip;
+ *               reads W->packed)
  * gq and sgrad come from one fused epilogue of the G GEMM; G itself is never
  * stored.  sgrad is reduced over r in a fixed order (deterministic run to run).
+ * At least one of dX, gq, sgrad must be given; with gq and sgrad both NULL the
+ * G GEMM is not run, with dX NULL the dX GEMM is not run.
  *   X [M][K] bf16, dY [M][N] bf16, scale [N] fp32: device, read.
- *   workspace: device, >= tern_linear_bwd_workspace(M,K,N) bytes, 16-byte aligned,
- *   contents ignored and overwritten (may be NULL when that size is 0).
+ *   workspace: device, >= tern_linear_bwd_workspace(M,K,N) bytes when sgrad is
+ *   requested (else unused, may be NULL), 16-byte aligned, contents ignored and
+ *   overwritten.
  * Same shape rules as the forward.
  */
 int tern_linear_bwd(const uint16_t* X, const uint16_t* dY, const tern_tiles* W, const float* scale,

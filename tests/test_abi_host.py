@@ -86,8 +86,11 @@ def test_backward_argument_checks(lib):
              P(0x70000), need, 64, 128, 128, None) == lib.TERN_ERR_ARG
     assert f(P(0x20000), P(0x21000), ctypes.byref(t), P(0x30000), P(0x40004), P(0x50000), P(0x60000),
              P(0x70000), need, 64, 128, 128, None) == lib.TERN_ERR_ALIGN
-    assert f(P(0x20000), P(0x21000), ctypes.byref(t), P(0x30000), P(0x40000), P(0x50000), None,
-             P(0x70000), need, 64, 128, 128, None) == lib.TERN_ERR_ARG     # sgrad is required
+    assert f(P(0x20000), P(0x21000), ctypes.byref(t), P(0x30000), None, None, None,
+             None, 0, 64, 128, 128, None) == lib.TERN_ERR_ARG     # nothing requested
+    nopk = lib._Tiles(None, P(0x11000), P(0x12000), P(0x13000))     # sgrad needs the 2-bit tiles
+    assert f(P(0x20000), P(0x21000), ctypes.byref(nopk), P(0x30000), None, None, P(0x60000),
+             P(0x70000), need, 64, 128, 128, None) == lib.TERN_ERR_ARG
 
 
 def test_materialize_argument_checks(lib):
