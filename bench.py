@@ -1,0 +1,443 @@
+#!/usr/bin/env python3
+"""Benchmark of the ternary-weight linear layer's training step on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  tern_materialize (q -> 2-bit tiles + bf16 operand planes)
+  tern_linear_fwd  (Y = scale * (X T))
+  tern_linear_bwd  (dX = dY W_eff^T; gq and sgrad from the fused G epilogue)
+  adamw_step       (AdamW on the per-column scales, gradient sgrad)
+on the large single projection X [32768 x 4096], q [4096 x 12288],
+dY [32768 x 12288] (inputs larger than L2).  `value` is the credited work of
+the layer, 6*M*K*N flops per step, in TFLOP/s over the device-timed step.
+
+Extra keys: per-kernel times, the roofline of the dominant kernel, AdamW and
+ternarise bandwidth at their large sizes, the end-to-end figure through the
+C ABI with the step's inputs copied from pinned host memory, the CPU oracle
+timed on a bounded sample, the clocks seen during the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs an independent replica of the step
+(the layer's step has no exchange on one GPU); rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import tern_synth as syn  # noqa: E402
+
+METRIC = "ternary-linear fwd+bwd TFLOP/s (% bf16 TC peak); AdamW/ternarise HBM GB/s"
+WORKLOADS = {
+    "large_single_projection": dict(M=32768, K=4096, N=12288, scale_lo=0.005, scale_hi=0.05, zero_prob=0.0),
+    "tiny": dict(M=64, K=128, N=128, scale_lo=0.01, scale_hi=0.1, zero_prob=0.0),
+}
+ADAM_HP = dict(lr=1e-3, b1=0.9, b2=0.95, eps=1e-8, wd=0.1)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sus=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- CPU oracle leg
+
+def oracle_sample(inp, budget_s, seed=7):
+    """Time the CPU oracle on sampled outputs of the layer for about budget_s seconds.
+
+    Y, dX and gq entries cost 2K, 2N and 2M flops each and each family totals
+    2MKN flops, so the time of the whole layer is extrapolated per family from
+    the mean cost of its sampled entries.  Single-threaded (the sampled oracle
+    entries run on one core).  Returns (TFLOP/s, description).
+    """
+    import oracle
+    M, K, N = inp.M, inp.K, inp.N
+    rng = np.random.default_rng(seed)
+    pool = 64
+    ms, cs, rs = rng.integers(0, M, pool), rng.integers(0, N, pool), rng.integers(0, K, pool)
+    xrows = [np.ascontiguousarray(inp.X[m]) for m in ms]
+    qcols = [np.ascontiguousarray(inp.q[:, c]) for c in cs]
+    dyrows = [np.ascontiguousarray(inp.dY[m]) for m in ms]
+    qrows = [np.ascontiguousarray(inp.q[r]) for r in rs]
+    xcols = [np.ascontiguousarray(inp.X[:, r]) for r in rs]
+    dycols = [np.ascontiguousarray(inp.dY[:, c]) for c in cs]
+    t = {"Y": 0.0, "dX": 0.0, "gq": 0.0}
+    n = {"Y": 0, "dX": 0, "gq": 0}
+    start = time.perf_counter()
+    i = 0
+    while time.perf_counter() - start < budget_s or min(n.values()) == 0:
+        j = i % pool
+        t0 = time.perf_counter()
+        oracle.fwd_at(xrows[j], qcols[j], inp.scale[cs[j]])
+        t1 = time.perf_counter()
+        oracle.dx_at(dyrows[j], qrows[j], inp.scale)
+        t2 = time.perf_counter()
+        oracle.gq_at(xcols[j], dycols[j], inp.scale[cs[j]])
+        t3 = time.perf_counter()
+        t["Y"] += t1 - t0
+        t["dX"] += t2 - t1
+        t["gq"] += t3 - t2
+        for k in n:
+            n[k] += 1
+        i += 1
+    full_s = (t["Y"] / n["Y"]) * M * N + (t["dX"] / n["dX"]) * M * K + (t["gq"] / n["gq"]) * K * N
+    tflops = 6.0 * M * K * N / full_s / 1e12
+    desc = (f"{n['Y']} Y, {n['dX']} dX and {n['gq']} gq entries of the same layer (fp64 dot products "
+            f"over K, N and M), extrapolated to all M*N + M*K + K*N outputs; one thread")
+    return tflops, desc, 1
+
+
+def make_inputs(wl):
+    c = WORKLOADS[wl]
+    return syn.linear_inputs(c["M"], c["K"], c["N"], seed=0, scale_lo=c["scale_lo"], scale_hi=c["scale_hi"],
+                             zero_prob=c["zero_prob"])
+
+
+# --------------------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    inp = make_inputs(args.workload)
+    total = args.steps + args.warmup
+    per_step = max(0.5, min(2.0, 150.0 / max(total, 1)))
+    for _ in range(args.warmup):
+        oracle_sample(inp, per_step / 4)
+    vals, desc, cores = [], "", 1
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        v, desc, cores = oracle_sample(inp, per_step)
+        vals.append(v)
+    wall = time.perf_counter() - t0
+    value = statistics.median(vals)
+    M, K, N = inp.M, inp.K, inp.N
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 6.0 * M * K * N / (value * 1e12) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "M": M, "K": K, "N": N},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"per step: {desc}; {args.steps} steps in {wall:.1f} s"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------- our arm
+
+def traffic_from_profiles(kernel, src_files):
+    """dram bytes per launch committed under profiles/, if the kernel source is unchanged since."""
+    p = os.path.join(ROOT, "profiles", "traffic.md")
+    if not os.path.exists(p):
+        return None
+    h = hashlib.sha256()
+    for f in src_files:
+        h.update(open(f, "rb").read())
+    digest = h.hexdigest()[:16]
+    for ln in open(p):
+        m = re.match(r"^\|\s*(\w+)\s*\|\s*([0-9.eE+]+)\s*\|\s*(\w+)\s*\|", ln)
+        if m and m.group(1) == kernel and m.group(3) == digest:
+            return float(m.group(2))
+    return None
+
+
+def run_ours(args):
+    import torch
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    import __graft_entry__
+    __graft_entry__._builder().build()
+    import bit_linear_gb300 as bl
+
+    pk = peaks()
+    inp = make_inputs(args.workload)
+    M, K, N = inp.M, inp.K, inp.N
+    dev = torch.device("cuda")
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+
+    X_h, dY_h = bf(inp.X).pin_memory(), bf(inp.dY).pin_memory()
+    X, dY = X_h.to(dev), dY_h.to(dev)
+    q = torch.from_numpy(inp.q).to(dev)
+    scale0 = torch.from_numpy(inp.scale).to(dev)
+    scale = scale0.clone()
+    ms, vs = torch.zeros(N, device=dev), torch.zeros(N, device=dev)
+    tiles = bl.Tiles.empty(K, N)
+    Y = torch.empty(M, N, device=dev)
+    dX = torch.empty(M, K, device=dev)
+    gq = torch.empty(K, N, device=dev)
+    sgrad = torch.empty(N, device=dev)
+    wsp = bl.workspace_for(M, K, N)
+    stream = torch.cuda.current_stream()
+    names = ["materialize", "fwd", "dx", "dw", "adamw"]
+    step_no = [0]
+
+    def step(ev=None):
+        step_no[0] += 1
+        if ev is not None:
+            ev[0].record(stream)
+        bl.tern_materialize(q, scale, tiles, 2, 7)
+        if ev is not None:
+            ev[1].record(stream)
+        bl.tern_linear_fwd(X, tiles, scale, Y)
+        if ev is not None:
+            ev[2].record(stream)
+        bl.tern_linear_bwd(X, dY, tiles, scale, dX, None, None, None)
+        if ev is not None:
+            ev[3].record(stream)
+        bl.tern_linear_bwd(X, dY, tiles, scale, None, gq, sgrad, wsp)
+        if ev is not None:
+            ev[4].record(stream)
+        bl.adamw_step(scale, sgrad, ms, vs, step_no[0], **ADAM_HP)
+        if ev is not None:
+            ev[5].record(stream)
+
+    launches_per_step = 6   # materialise, fwd, dX, G(+gq/sgrad), sgrad reduce, AdamW
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if bl.tern_device_status() != bl.TERN_OK:
+        raise RuntimeError("a kernel gave up on a bounded wait during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            step(evs[i])
+        torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    st = bl.tern_device_status()
+    if st != bl.TERN_OK:
+        raise RuntimeError(f"device status: {bl.strerror(st)}")
+    total_ms = evs[0][0].elapsed_time(evs[-1][5])
+    per = {n: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j, n in enumerate(names)}
+    if ws > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    flops = 6.0 * M * K * N
+    value = flops * ws / (ms_step * 1e-3) / 1e12
+
+    # kernel rooflines: credited flops per launch / average launch time
+    credited = {"fwd": 2.0 * M * K * N, "dx": 2.0 * M * K * N, "dw": 2.0 * M * K * N}
+    kern = {}
+    for n in names:
+        kern[n] = {"ms": per[n]}
+    for n, f in credited.items():
+        kern[n]["tflops"] = f / (per[n] * 1e-3) / 1e12
+        kern[n]["frac_of_sustained"] = kern[n]["tflops"] / pk["bf16_sus"]
+    mat_bytes = K * N * (1 + 0.25 + 2 + 2 + 2) + N * 4
+    kern["materialize"]["gbs"] = mat_bytes / (per["materialize"] * 1e-3) / 1e9
+    dom = max(credited, key=lambda n: per[n])
+    kname = {"fwd": "tern_fwd_gemm", "dx": "tern_dx_gemm", "dw": "tern_dw_gemm"}[dom]
+    gemm_src = [os.path.join(ROOT, "bit_linear_gb300", "csrc", f) for f in ("gemm.cu", "common.cuh")]
+    traffic = traffic_from_profiles(kname, gemm_src)
+    roof = {"kernel": kname, "bound": "tensor", "achieved": kern[dom]["tflops"], "peak": pk["bf16_sus"],
+            "unit": "TFLOP/s", "frac": kern[dom]["tflops"] / pk["bf16_sus"], "traffic": traffic,
+            "peak_kind": f"{pk['src']} sustained bf16 (kernel timed inside a long run of steps)"}
+
+    # ---- AdamW and ternarise bandwidth at their large sizes (separate timed loops)
+    def bw_loop(fn, nbytes, reps=10, warm=3):
+        for _ in range(warm):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms_ = e0.elapsed_time(e1) / reps
+        return {"ms": ms_, "gbs": nbytes / (ms_ * 1e-3) / 1e9, "frac": nbytes / (ms_ * 1e-3) / 1e9 / pk["hbm"]}
+
+    extra = {}
+    if not args.skip_bandwidth and args.workload == "large_single_projection":
+        del Y
+        torch.cuda.empty_cache()
+        n_ad = 400_000_000
+        w_ = torch.empty(n_ad, device=dev).normal_(0, 0.02)
+        g_ = torch.empty(n_ad, device=dev).normal_(0, 1e-3)
+        m_, v_ = torch.zeros(n_ad, device=dev), torch.zeros(n_ad, device=dev)
+        tcount = [0]
+
+        def ad():
+            tcount[0] += 1
+            bl.adamw_step(w_, g_, m_, v_, tcount[0], **ADAM_HP)
+        extra["adamw"] = dict(n=n_ad, bytes_per_elem=28, **bw_loop(ad, 28 * n_ad))
+        del w_, g_, m_, v_
+        torch.cuda.empty_cache()
+        Kt, Nt = 65536, 15264          # 1.0003e9 weights, N a multiple of 16
+        qt = torch.randint(-7, 8, (Kt, Nt), dtype=torch.int8, device=dev)
+        tt = bl.Tiles(Kt, Nt, packed=torch.empty((Kt, Nt // 16), dtype=torch.int32, device=dev))
+        extra["ternarise"] = dict(n=Kt * Nt, bytes_per_elem=1.25,
+                                  **bw_loop(lambda: bl.tern_materialize(qt, None, tt, 2, 7), 1.25 * Kt * Nt))
+        del qt, tt
+        torch.cuda.empty_cache()
+        Y = torch.empty(M, N, device=dev)
+
+    # ---- end to end through the C ABI: inputs from pinned host memory each step,
+    #      the step's result (updated scales and their gradient) read back
+    e2e_steps = min(args.steps, 10)
+    res_h = torch.empty(2, N, dtype=torch.float32).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        X.copy_(X_h, non_blocking=True)
+        dY.copy_(dY_h, non_blocking=True)
+        step()
+        res_h[0].copy_(scale, non_blocking=True)
+        res_h[1].copy_(sgrad, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    h2d = X.numel() * 2 + dY.numel() * 2
+    d2h = 2 * N * 4
+
+    line = None
+    if rank == 0:
+        cpu = None
+        if ws == 1 and not args.skip_cpu:
+            v, desc, cores = oracle_sample(inp, args.cpu_budget)
+            cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+        csum = clk.summary()
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": args.workload, "M": M, "K": K, "N": N, "theta": 2, "q_clamp": 7,
+                       "step": "materialise + fwd + bwd (dX, gq, sgrad) + AdamW on scale",
+                       "flops_per_step": flops, "l2": "inputs larger than L2 (X 268 MB, dY 805 MB)",
+                       "parallelism": f"replicas x{ws}"},
+            "frac_of_peak": {"measured_burst": value / ws / pk["bf16"], "measured_sustained": value / ws / pk["bf16_sus"],
+                             "spec_2250": value / ws / 2250.0, "peaks": pk["src"]},
+            "roofline": roof,
+            "kernels": kern,
+            "cpu_baseline": cpu,
+            "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12 * ws, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": csum,
+        }
+        line.update(extra)
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="large_single_projection")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of CPU oracle sampling")
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--skip-bandwidth", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -11,8 +11,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def lib():
-    from bit_linear_gb300 import build as b
-    b.build()
+    import __graft_entry__
+    __graft_entry__._builder().build()
     import bit_linear_gb300 as bl
     return bl
 
