@@ -44,6 +44,9 @@ METRIC = "ternary-linear fwd+bwd TFLOP/s (% bf16 TC peak); AdamW/ternarise HBM G
 WORKLOADS = {
     "large_single_projection": dict(M=32768, K=4096, N=12288, scale_lo=0.005, scale_hi=0.05, zero_prob=0.0),
     "tiny": dict(M=64, K=128, N=128, scale_lo=0.01, scale_hi=0.1, zero_prob=0.0),
+    # the large projection's weight with a quarter of its tokens: a profiling case whose
+    # operands still exceed L2 (dY 201 MB) while the device holds under 1 GB
+    "profile_quarter_tokens": dict(M=8192, K=4096, N=12288, scale_lo=0.005, scale_hi=0.05, zero_prob=0.0),
 }
 ADAM_HP = dict(lr=1e-3, b1=0.9, b2=0.95, eps=1e-8, wd=0.1)
 

@@ -30,12 +30,15 @@ TERN_ERR_CUDA = -3
 TERN_ERR_TIMEOUT = -4
 TERN_ERR_WORKSPACE = -5
 TERN_ERR_DEVICE = -6
+TERN_ERR_SCRATCH_LIMIT = -7
+TERN_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 TERN_TILE_PACKED, TERN_TILE_T, TERN_TILE_WHI, TERN_TILE_WLO = 0, 1, 2, 3
 
 # the C ABI's exported symbols (tests check the library exports every one)
 ABI_SYMBOLS = ("tern_tiles_bytes", "tern_materialize", "tern_linear_fwd", "tern_linear_bwd_workspace",
-               "tern_linear_bwd", "adamw_step", "tern_strerror", "tern_device_status")
+               "tern_linear_bwd", "tern_linear_bwd_noalloc", "adamw_step", "tern_strerror",
+               "tern_device_status")
 
 
 class TernError(RuntimeError):
@@ -61,6 +64,7 @@ def _load():
         "tern_linear_fwd": ([vp, tp, vp, vp, i64, i64, i64, vp], ci),
         "tern_linear_bwd_workspace": ([i64, i64, i64], sz),
         "tern_linear_bwd": ([vp, vp, tp, vp, vp, vp, vp, vp, sz, i64, i64, i64, vp], ci),
+        "tern_linear_bwd_noalloc": ([vp, vp, tp, vp, vp, vp, vp, i64, i64, i64, vp], ci),
         "adamw_step": ([vp, vp, vp, vp, i64, ci, cf, cf, cf, cf, cf, cf, ci, vp], ci),
         "tern_strerror": ([ci], ctypes.c_char_p),
         "tern_device_status": ([vp, ci], ci),
@@ -178,6 +182,20 @@ def tern_linear_bwd(X, dY, tiles: Tiles, scale, dX, gq, sgrad, workspace, stream
                                _ptr(sgrad, torch.float32, (N,), "sgrad"), ws_ptr, ws_bytes, M, K, N,
                                _stream(stream)),
            "tern_linear_bwd")
+
+
+def tern_linear_bwd_noalloc(X, dY, tiles: Tiles, scale, dX, gq, sgrad, stream=None):
+    """tern_linear_bwd without a caller workspace, for callers that cannot allocate
+    device memory: the sgrad partials live in a fixed 8 MiB array inside the
+    library (see tern.h for the size limit and the rule that overlapping calls race)."""
+    M, K = X.shape
+    N = tiles.N
+    ct = tiles._c()
+    _check(lib.tern_linear_bwd_noalloc(_ptr(X, torch.bfloat16, (M, K), "X"), _ptr(dY, torch.bfloat16, (M, N), "dY"),
+                                       ctypes.byref(ct), _ptr(scale, torch.float32, (N,), "scale"),
+                                       _ptr(dX, torch.float32, (M, K), "dX"), _ptr(gq, torch.float32, (K, N), "gq"),
+                                       _ptr(sgrad, torch.float32, (N,), "sgrad"), M, K, N, _stream(stream)),
+           "tern_linear_bwd_noalloc")
 
 
 def adamw_step(w, g, m, v, t, lr, b1, b2, eps, wd, gmul=1.0, decoupled=True, stream=None):

@@ -47,6 +47,8 @@ extern "C" const char* tern_strerror(int status) {
     case TERN_ERR_TIMEOUT: return "a bounded device-side wait gave up";
     case TERN_ERR_WORKSPACE: return "workspace too small";
     case TERN_ERR_DEVICE: return "current device is not an sm_103 (GB300) GPU";
+    case TERN_ERR_SCRATCH_LIMIT:
+        return "problem too large for the built-in scratch of tern_linear_bwd_noalloc (use tern_linear_bwd)";
     default: return "unknown status";
     }
 }

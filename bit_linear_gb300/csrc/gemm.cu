@@ -555,3 +555,61 @@ extern "C" int tern_linear_bwd(const uint16_t* X, const uint16_t* dY, const tern
     }
     return TERN_OK;
 }
+
+// ===================================================================== backward without a workspace
+//
+// tern_linear_bwd needs a device workspace for the sgrad partials, which the
+// caller allocates.  Some callers cannot allocate device memory: a plugin run
+// by a host program that owns every device allocation and hands none to its
+// plugins, or a loop that must never pay cudaMalloc's implicit device-wide
+// synchronisation.  tern_linear_bwd_noalloc serves them with a fixed scratch
+// array that lives in this library's device image: every GPU that loads the
+// library holds TERN_NOALLOC_SCRATCH_BYTES of it until the process exits.
+//
+// The host cannot pass the array's name to a kernel (in host code it is only a
+// host-side stand-in for the symbol), so the first call on each device looks up
+// its device address with cudaGetSymbolAddress while that device is current,
+// and later calls on that device reuse it.  Make that first call on each device
+// before any stream capture.
+//
+// Every call shares the one array and leaves its last contents behind.  Nothing
+// needs clearing: the G kernel writes every partial the reduction reads.  Two
+// calls whose kernels overlap on a GPU (different streams, no ordering between
+// them) race on the array and give wrong sgrad values.
+
+namespace tern {
+
+static __device__ __align__(256) float g_noalloc_partials[TERN_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+namespace {
+
+struct NoallocScratch {
+    std::once_flag once;
+    cudaError_t err = cudaErrorUnknown;
+    void* ptr = nullptr;
+};
+NoallocScratch g_noalloc_scratch[64];
+
+// Device address of g_noalloc_partials on the current device (set up once per device).
+int noalloc_scratch(void** out) {
+    int dev = 0;
+    TERN_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return TERN_ERR_DEVICE;
+    NoallocScratch& s = g_noalloc_scratch[dev];
+    std::call_once(s.once, [&s] { s.err = cudaGetSymbolAddress(&s.ptr, g_noalloc_partials); });
+    if (s.err != cudaSuccess || s.ptr == nullptr) return TERN_ERR_CUDA;
+    *out = s.ptr;
+    return TERN_OK;
+}
+
+}  // namespace
+}  // namespace tern
+
+extern "C" int tern_linear_bwd_noalloc(const uint16_t* X, const uint16_t* dY, const tern_tiles* W,
+                                       const float* scale, float* dX, float* gq, float* sgrad, int64_t M,
+                                       int64_t K, int64_t N, void* stream) {
+    if (sgrad && tern_linear_bwd_workspace(M, K, N) > TERN_NOALLOC_SCRATCH_BYTES) return TERN_ERR_SCRATCH_LIMIT;
+    void* scratch = nullptr;
+    if (int st = noalloc_scratch(&scratch)) return st;
+    return tern_linear_bwd(X, dY, W, scale, dX, gq, sgrad, scratch, TERN_NOALLOC_SCRATCH_BYTES, M, K, N, stream);
+}

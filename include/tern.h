@@ -49,6 +49,7 @@ extern "C" {
 #define TERN_ERR_TIMEOUT (-4)     /* a bounded device-side wait gave up */
 #define TERN_ERR_WORKSPACE (-5)   /* workspace smaller than tern_linear_bwd_workspace() */
 #define TERN_ERR_DEVICE (-6)      /* current device is not an sm_103 (GB300) part */
+#define TERN_ERR_SCRATCH_LIMIT (-7) /* problem larger than tern_linear_bwd_noalloc's built-in scratch */
 
 /* Weight operands produced by tern_materialize from q and scale; caller-owned
  * device buffers.  Any pointer may be NULL to skip that output; the GEMM calls
@@ -119,6 +120,30 @@ size_t tern_linear_bwd_workspace(int64_t M, int64_t K, int64_t N);
 int tern_linear_bwd(const uint16_t* X, const uint16_t* dY, const tern_tiles* W, const float* scale,
                     float* dX, float* gq, float* sgrad, void* workspace, size_t ws_bytes, int64_t M,
                     int64_t K, int64_t N, void* stream);
+
+/*
+ * tern_linear_bwd for callers that cannot allocate device memory.  The paper
+ * has no counterpart of this call; it is a convenience of this library.
+ *
+ * Same arguments, outputs and rules as tern_linear_bwd, minus the workspace.
+ * Some callers cannot call cudaMalloc (for example a plugin whose host program
+ * owns every device allocation, or a loop that must not pay cudaMalloc's
+ * device-wide synchronisation), so they cannot provide one.  This entry point
+ * keeps the sgrad partials in a fixed array inside the library's device image
+ * instead; it allocates nothing.
+ *   Limit: tern_linear_bwd_workspace(M, K, N) <= TERN_NOALLOC_SCRATCH_BYTES
+ *   (8 MiB: ceil(K/128)*4*N <= 2^21, e.g. K = 4096 with N <= 16384) when sgrad
+ *   is requested, else TERN_ERR_SCRATCH_LIMIT and nothing is enqueued.
+ *   Every GPU that loads the library holds the 8 MiB until the process exits.
+ *   The first call on each device looks up the array's device address (with
+ *   that device current); make it before any stream capture.
+ *   All calls share the array: calls whose kernels overlap on a GPU race and
+ *   corrupt each other's sgrad.  Order them on one stream (or with events).
+ */
+#define TERN_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+int tern_linear_bwd_noalloc(const uint16_t* X, const uint16_t* dY, const tern_tiles* W, const float* scale,
+                            float* dX, float* gq, float* sgrad, int64_t M, int64_t K, int64_t N,
+                            void* stream);
 
 /*
  * AdamW on n fp32 elements (page "train_gpu.cu", adamw_dev: bias corrections

@@ -115,3 +115,12 @@ def test_adamw_argument_checks(lib):
     assert f(*a, 10, 0, *hp) == lib.TERN_ERR_ARG     # t >= 1
     assert f(P(0x10008), *a[1:], 10, 1, *hp) == lib.TERN_ERR_ALIGN
     assert f(None, *a[1:], 10, 1, *hp) == lib.TERN_ERR_ARG
+
+
+def test_noalloc_rejects_sizes_beyond_its_scratch_before_touching_the_device(lib):
+    f = lib.lib.tern_linear_bwd_noalloc
+    t = _tiles(lib)
+    # ceil(4096/128) * 4 * 16400 partials > 2^21 floats of built-in scratch
+    assert f(P(0x20000), P(0x21000), ctypes.byref(t), P(0x30000), None, None, P(0x60000),
+             1, 4096, 16400, None) == lib.TERN_ERR_SCRATCH_LIMIT
+    assert lib.strerror(lib.TERN_ERR_SCRATCH_LIMIT) != "unknown status"
