@@ -9,9 +9,10 @@
 //           scale[c]*T used by the dX GEMM (s_hi = bf16(scale), s_lo =
 //           bf16(scale - s_hi)); a zero weight is +0 in every plane
 //   qc      the clamped accumulator
-// The kernel is HBM-bound: each thread owns one 16-element group (one packed
-// word) per iteration, loads it as one 16-byte vector and stores every output
-// with 16-byte (or 4-byte for packed) coalesced accesses.
+// The kernel is HBM-bound.  Each thread takes four 16-weight groups (one packed
+// word each) per iteration, issues their four 16-byte loads before using any,
+// and works on four weights at a time with byte-SIMD compares; every output is
+// written with 16-byte (packed: 4-byte) coalesced streaming stores.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -21,98 +22,124 @@ namespace tern {
 namespace {
 
 struct MatArgs {
-    const int8_t* q;
+    const int8_t* q;     // q and qc may be the same buffer (in-place clamp)
     int8_t* qc;
-    const float* scale;
-    uint32_t* packed;
-    uint16_t* t;
-    uint16_t* whi;
-    uint16_t* wlo;
-    int64_t groups;      // K * N / 16
+    const float* __restrict__ scale;
+    uint32_t* __restrict__ packed;
+    uint16_t* __restrict__ t;
+    uint16_t* __restrict__ whi;
+    uint16_t* __restrict__ wlo;
+    int64_t groups;        // K * N / 16
     uint32_t ngroups_row;  // N / 16
-    int theta, clamp;
+    uint32_t th_pos;       // theta in every byte
+    uint32_t th_neg;       // -theta in every byte
+    uint32_t cl_pos;       // clamp in every byte
+    uint32_t cl_neg;       // -clamp in every byte
 };
 
 __device__ __forceinline__ uint32_t bf16_bits(float x) {
     return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(x)));
 }
 
-}  // namespace
+// Two weights' 16-bit lanes from byte masks (0xFF / 0x00) of bytes b and b+1.
+__device__ __forceinline__ uint32_t lanes16(uint32_t bytemask, uint32_t sel) {
+    return __byte_perm(bytemask, 0u, sel);
+}
 
-__global__ void __launch_bounds__(256) tern_materialize_kernel(const MatArgs a) {
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t gi = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; gi < a.groups; gi += stride) {
-        const int64_t e0 = gi * 16;
-        const int4 raw = __ldcs(reinterpret_cast<const int4*>(a.q + e0));
-        const uint32_t words[4] = {static_cast<uint32_t>(raw.x), static_cast<uint32_t>(raw.y),
-                                   static_cast<uint32_t>(raw.z), static_cast<uint32_t>(raw.w)};
-        int w[16];
-        uint32_t qcw[4] = {0, 0, 0, 0};
-        uint32_t code = 0;
+__device__ __forceinline__ void encode_group(const MatArgs& a, int4 raw, int64_t gi) {
+    const uint32_t w[4] = {static_cast<uint32_t>(raw.x), static_cast<uint32_t>(raw.y),
+                           static_cast<uint32_t>(raw.z), static_cast<uint32_t>(raw.w)};
+    uint32_t pos[4], neg[4];
+    uint32_t code = 0;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            int v = static_cast<int8_t>((words[j >> 2] >> (8 * (j & 3))) & 0xFFu);
-            v = v > a.clamp ? a.clamp : (v < -a.clamp ? -a.clamp : v);
-            qcw[j >> 2] |= (static_cast<uint32_t>(v) & 0xFFu) << (8 * (j & 3));
-            w[j] = v >= a.theta ? 1 : (v <= -a.theta ? -1 : 0);
-            code |= (w[j] == 1 ? 1u : (w[j] == -1 ? 3u : 0u)) << (2 * j);
+    for (int k = 0; k < 4; ++k) {
+        pos[k] = __vcmpges4(w[k], a.th_pos);   // 0xFF where q >= theta
+        neg[k] = __vcmples4(w[k], a.th_neg);   // 0xFF where q <= -theta
+        // per byte: +1 -> 01, -1 -> 11, 0 -> 00; then gather the four 2-bit codes
+        uint32_t x = (pos[k] & 0x01010101u) | (neg[k] & 0x03030303u);
+        x = (x | (x >> 6) | (x >> 12) | (x >> 18)) & 0xFFu;
+        code |= x << (8 * k);
+    }
+    const int64_t e0 = gi * 16;
+    if (a.qc) {
+        int4 c;
+        c.x = static_cast<int>(__vmaxs4(__vmins4(w[0], a.cl_pos), a.cl_neg));
+        c.y = static_cast<int>(__vmaxs4(__vmins4(w[1], a.cl_pos), a.cl_neg));
+        c.z = static_cast<int>(__vmaxs4(__vmins4(w[2], a.cl_pos), a.cl_neg));
+        c.w = static_cast<int>(__vmaxs4(__vmins4(w[3], a.cl_pos), a.cl_neg));
+        __stcs(reinterpret_cast<int4*>(a.qc + e0), c);
+    }
+    if (a.packed) __stcs(a.packed + gi, code);
+    // 16-bit lane masks of weight pairs (2i, 2i+1): nz = weight != 0, ng = weight < 0
+    uint32_t nz[8], ng[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        nz[2 * k] = lanes16(pos[k] | neg[k], 0x1100u);
+        nz[2 * k + 1] = lanes16(pos[k] | neg[k], 0x3322u);
+        ng[2 * k] = lanes16(neg[k], 0x1100u);
+        ng[2 * k + 1] = lanes16(neg[k], 0x3322u);
+    }
+    if (a.t) {
+        uint32_t p[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) p[i] = (nz[i] & 0x3F803F80u) | (ng[i] & 0x80008000u);
+        int4* dst = reinterpret_cast<int4*>(a.t + e0);
+        __stcs(dst, make_int4(p[0], p[1], p[2], p[3]));
+        __stcs(dst + 1, make_int4(p[4], p[5], p[6], p[7]));
+    }
+    if (a.whi || a.wlo) {
+        const uint32_t cg = static_cast<uint32_t>(gi % a.ngroups_row);
+        const float4* sp = reinterpret_cast<const float4*>(a.scale + static_cast<int64_t>(cg) * 16);
+        uint32_t hi2[8], lo2[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 s4 = __ldg(sp + i);
+            const float s[4] = {s4.x, s4.y, s4.z, s4.w};
+            uint32_t hb[4], lb[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                hb[k] = bf16_bits(s[k]);
+                lb[k] = bf16_bits(s[k] - __uint_as_float(hb[k] << 16));   // exact difference in fp32
+            }
+            hi2[2 * i] = hb[0] | (hb[1] << 16);
+            hi2[2 * i + 1] = hb[2] | (hb[3] << 16);
+            lo2[2 * i] = lb[0] | (lb[1] << 16);
+            lo2[2 * i + 1] = lb[2] | (lb[3] << 16);
         }
-        if (a.qc) __stcs(reinterpret_cast<int4*>(a.qc + e0), make_int4(qcw[0], qcw[1], qcw[2], qcw[3]));
-        if (a.packed) __stcs(a.packed + gi, code);
-        if (a.t) {
+        // a zero weight is +0; a negative weight flips the sign bit of s_hi / s_lo
+        if (a.whi) {
             uint32_t p[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint32_t lo = w[2 * i] == 0 ? 0u : (w[2 * i] > 0 ? 0x3F80u : 0xBF80u);
-                const uint32_t hi = w[2 * i + 1] == 0 ? 0u : (w[2 * i + 1] > 0 ? 0x3F80u : 0xBF80u);
-                p[i] = lo | (hi << 16);
-            }
-            int4* dst = reinterpret_cast<int4*>(a.t + e0);
+            for (int i = 0; i < 8; ++i) p[i] = (hi2[i] & nz[i]) ^ (ng[i] & 0x80008000u);
+            int4* dst = reinterpret_cast<int4*>(a.whi + e0);
             __stcs(dst, make_int4(p[0], p[1], p[2], p[3]));
             __stcs(dst + 1, make_int4(p[4], p[5], p[6], p[7]));
         }
-        if (a.whi || a.wlo) {
-            const uint32_t cg = static_cast<uint32_t>(gi % a.ngroups_row);
-            const float4* sp = reinterpret_cast<const float4*>(a.scale + static_cast<int64_t>(cg) * 16);
-            uint32_t hi_b[16], lo_b[16];
+        if (a.wlo) {
+            uint32_t p[8];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float4 s4 = __ldg(sp + i);
-                const float s[4] = {s4.x, s4.y, s4.z, s4.w};
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint32_t hb = bf16_bits(s[k]);
-                    const float hv = __uint_as_float(hb << 16);
-                    hi_b[4 * i + k] = hb;
-                    lo_b[4 * i + k] = bf16_bits(s[k] - hv);   // exact difference in fp32
-                }
-            }
-            uint32_t ph[8], pl[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                uint32_t h2[2], l2[2];
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const int j = 2 * i + k;
-                    const uint32_t neg = w[j] < 0 ? 0x8000u : 0u;
-                    h2[k] = w[j] == 0 ? 0u : (hi_b[j] ^ neg);
-                    l2[k] = w[j] == 0 ? 0u : (lo_b[j] ^ neg);
-                }
-                ph[i] = h2[0] | (h2[1] << 16);
-                pl[i] = l2[0] | (l2[1] << 16);
-            }
-            if (a.whi) {
-                int4* dst = reinterpret_cast<int4*>(a.whi + e0);
-                __stcs(dst, make_int4(ph[0], ph[1], ph[2], ph[3]));
-                __stcs(dst + 1, make_int4(ph[4], ph[5], ph[6], ph[7]));
-            }
-            if (a.wlo) {
-                int4* dst = reinterpret_cast<int4*>(a.wlo + e0);
-                __stcs(dst, make_int4(pl[0], pl[1], pl[2], pl[3]));
-                __stcs(dst + 1, make_int4(pl[4], pl[5], pl[6], pl[7]));
-            }
+            for (int i = 0; i < 8; ++i) p[i] = (lo2[i] & nz[i]) ^ (ng[i] & 0x80008000u);
+            int4* dst = reinterpret_cast<int4*>(a.wlo + e0);
+            __stcs(dst, make_int4(p[0], p[1], p[2], p[3]));
+            __stcs(dst + 1, make_int4(p[4], p[5], p[6], p[7]));
         }
     }
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(256) tern_materialize_kernel(const MatArgs a) {
+    const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    int64_t gi = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int4* q4 = reinterpret_cast<const int4*>(a.q);
+    for (; gi + 3 * nth < a.groups; gi += 4 * nth) {
+        int4 r[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) r[j] = __ldcs(q4 + gi + j * nth);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) encode_group(a, r[j], gi + j * nth);
+    }
+    for (; gi < a.groups; gi += nth) encode_group(a, __ldcs(q4 + gi), gi);
 }
 
 }  // namespace tern
@@ -141,10 +168,20 @@ extern "C" int tern_materialize(const int8_t* q, int8_t* q_clamped, const float*
     a.wlo = out->wlo_bf16;
     a.groups = K * N / 16;
     a.ngroups_row = static_cast<uint32_t>(N / 16);
-    a.theta = theta;
-    a.clamp = q_clamp;
+    const uint32_t tb = static_cast<uint8_t>(theta), tn = static_cast<uint8_t>(-theta);
+    const uint32_t cb = static_cast<uint8_t>(q_clamp), cn = static_cast<uint8_t>(-q_clamp);
+    a.th_pos = tb * 0x01010101u;
+    a.th_neg = tn * 0x01010101u;
+    a.cl_pos = cb * 0x01010101u;
+    a.cl_neg = cn * 0x01010101u;
+    static int per_sm = 0;   // resident CTAs per SM (the grid strides over the rest)
+    if (per_sm == 0) {
+        int b = 0;
+        TERN_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, tern_materialize_kernel, 256, 0));
+        per_sm = b > 0 ? b : 1;
+    }
     const int64_t want = (a.groups + 255) / 256;
-    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    const int64_t cap = static_cast<int64_t>(num_sms) * per_sm;
     const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
     tern_materialize_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
     TERN_CUDA_TRY(cudaGetLastError());

@@ -26,7 +26,7 @@ def _within(name, a, b, ab):
     assert np.all(err <= REL * ab), f"{name}: worst |noalloc - workspace| / sum|term| = {(err / ab).max():.3e}"
 
 
-@pytest.mark.parametrize("first,second", [((300, 520, 400), (130, 144, 272))])
+@pytest.mark.parametrize("first,second", [((300, 528, 400), (130, 144, 272))])
 def test_noalloc_matches_workspace_entry_point(cuda_lib, first, second):
     bl = cuda_lib
     for M, K, N in (first, second):
