@@ -32,6 +32,7 @@
 // bounded) for its own TMA copies and MMAs in flight, frees TMEM and returns.
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -41,7 +42,7 @@ __device__ int g_gemm_status;
 
 namespace {
 
-constexpr int kBM = 128;
+constexpr int kBM = 128;           // rows of A (and of D) per CTA
 constexpr int kThreads = 192;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait; a healthy wait takes microseconds
 
@@ -54,27 +55,42 @@ struct GemmArgs {
     float* out;               // [Mg][Ng] fp32 (Y, dX or gq); may be null for EPI_DW
     const float* scale;       // [Ng] column scale (EPI_FWD, EPI_DW)
     const uint32_t* packed;   // [Mg][Ng/16] 2-bit ternary codes (EPI_DW)
-    float* partial;           // [tiles_m*4][Ng] per-lane-quarter sgrad partials (EPI_DW)
+    float* partial;           // [ceil(Mg/128)*4][Ng] per-lane-quarter sgrad partials (EPI_DW)
 };
 
-template <int BN_, int BK_, bool A_MN_, bool B_MN_, int NB_, int EPI_, int STAGES_>
+// CG CTAs (1, or a 2-CTA cluster) share one MMA of M = 128*CG rows by N = BN columns.
+// Each CTA loads its 128 rows of A and BN/CG rows of B per k-block of BK, and its
+// TMEM holds its own 128 rows of D.
+template <int CG_, int BN_, int BK_, bool A_MN_, bool B_MN_, int NB_, int EPI_, int STAGES_>
 struct Cfg {
-    static constexpr int BN = BN_, BK = BK_, NB = NB_, EPI = EPI_, STAGES = STAGES_;
+    static constexpr int CG = CG_, BN = BN_, BK = BK_, NB = NB_, EPI = EPI_, STAGES = STAGES_;
     static constexpr bool A_MN = A_MN_, B_MN = B_MN_;
+    static constexpr int TILE_M = kBM * CG;
+    static constexpr int B_ROWS = BN / CG;
     static constexpr int A_BYTES = kBM * BK * 2;
-    static constexpr int B_BYTES = BN * BK * 2;
-    static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES;
+    static constexpr int B_BYTES = B_ROWS * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES;   // per CTA
+    static constexpr int TX_BYTES = CG * STAGE_BYTES;            // landing on the leader's barrier
     static constexpr int TMEM_COLS = 2 * BN;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+    // A pair keeps 32 KB of slack past the last stage: an MMA operand read of a
+    // whole B tile (not half) from the last stage would still stay inside the
+    // CTA's shared memory.
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + (CG == 2 ? 32768 : 0) + 1024 + 256;
+    static_assert(CG == 1 || CG == 2, "CTA group");
     static_assert(BK == 64 || (BK == 32 && !A_MN && !B_MN), "MN-major operands use 64-deep k-blocks");
-    static_assert(BN % 64 == 0 && BN <= 256, "BN");
+    static_assert(BN % 64 == 0 && BN <= 256 && B_ROWS % 64 == 0, "BN");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of two");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
-using FwdCfg = Cfg<256, 64, false, true, 1, EPI_FWD, 4>;   // A = X (K-major), B = T [K][N] (MN-major)
-using DxCfg = Cfg<256, 32, false, false, 2, EPI_DX, 5>;    // A = dY (K-major), B = W_hi, W_lo (K-major)
-using DwCfg = Cfg<256, 64, true, true, 1, EPI_DW, 4>;      // A = X^T, B = dY^T (both MN-major)
+// One CTA per 128 x 256 tile (small problems).
+using Fwd1 = Cfg<1, 256, 64, false, true, 1, EPI_FWD, 4>;   // A = X (K-major), B = T [K][N] (MN-major)
+using Dx1 = Cfg<1, 256, 32, false, false, 2, EPI_DX, 5>;    // A = dY (K-major), B = W_hi, W_lo (K-major)
+using Dw1 = Cfg<1, 256, 64, true, true, 1, EPI_DW, 4>;      // A = X^T, B = dY^T (both MN-major)
+// A CTA pair per 256 x 256 tile: half the shared-memory operand traffic per MMA.
+using Fwd2 = Cfg<2, 256, 64, false, true, 1, EPI_FWD, 6>;
+using Dx2 = Cfg<2, 256, 64, false, false, 2, EPI_DX, 4>;
+using Dw2 = Cfg<2, 256, 64, true, true, 1, EPI_DW, 6>;
 
 // tcgen05 instruction descriptor, kind::f16: bf16 A/B, fp32 D, M x N, operand majors.
 __host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool a_mn, bool b_mn) {
@@ -112,10 +128,10 @@ __device__ __forceinline__ uint64_t op_desc(uint32_t base, int kk) {
     }
 }
 
-// Grouped raster: runs of 16 m-tiles share an n-tile, so neighbouring CTAs reuse
+// Grouped raster: runs of GM m-tiles share an n-tile, so neighbouring CTAs reuse
 // the same B panel and A panels stay resident in L2.
+template <int GM>
 __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int& mt, int& nt) {
-    constexpr int GM = 16;
     const int group = tile / (GM * tiles_n);
     const int first_m = group * GM;
     const int gm = min(GM, tiles_m - first_m);
@@ -160,30 +176,30 @@ __device__ __forceinline__ float warp_column_sums(float (&v)[32], int lane) {
     return v[0];
 }
 
+// One 32-column chunk of a warp's 32 rows: r[] is row `row`, columns c0..c0+31.
+// tile128 is the index of the 128-row block the row lies in.
 template <class C>
 __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const uint32_t (&r)[32], int row, int c0,
-                                               int mt, int quad, int lane) {
+                                               int tile128, int quad, int lane) {
     const bool row_ok = row < a.Mg;
-    if constexpr (C::EPI == EPI_FWD || C::EPI == EPI_DX || C::EPI == EPI_DW) {
-        if (row_ok && a.out != nullptr) {
-            float* o = a.out + static_cast<int64_t>(row) * a.Ng + c0;
+    if (row_ok && a.out != nullptr) {
+        float* o = a.out + static_cast<int64_t>(row) * a.Ng + c0;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                if (c0 + 16 * h < a.Ng) {
+        for (int h = 0; h < 2; ++h) {
+            if (c0 + 16 * h < a.Ng) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int j = 16 * h + 4 * q;
-                        float4 v = make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                                               __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
-                        if constexpr (C::EPI != EPI_DX) {
-                            const float4 s = __ldg(reinterpret_cast<const float4*>(a.scale + c0 + j));
-                            v.x *= s.x;
-                            v.y *= s.y;
-                            v.z *= s.z;
-                            v.w *= s.w;
-                        }
-                        *reinterpret_cast<float4*>(o + j) = v;
+                for (int q = 0; q < 4; ++q) {
+                    const int j = 16 * h + 4 * q;
+                    float4 v = make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                                           __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+                    if constexpr (C::EPI != EPI_DX) {
+                        const float4 s = __ldg(reinterpret_cast<const float4*>(a.scale + c0 + j));
+                        v.x *= s.x;
+                        v.y *= s.y;
+                        v.z *= s.z;
+                        v.w *= s.w;
                     }
+                    *reinterpret_cast<float4*>(o + j) = v;
                 }
             }
         }
@@ -205,13 +221,14 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const uint32_t
             v[i] = (code & 1u) ? ((code & 2u) ? -g : g) : 0.0f;
         }
         const float colsum = warp_column_sums(v, lane);
-        if (c0 + lane < a.Ng) a.partial[static_cast<int64_t>(mt * 4 + quad) * a.Ng + c0 + lane] = colsum;
+        if (c0 + lane < a.Ng) a.partial[static_cast<int64_t>(tile128 * 4 + quad) * a.Ng + c0 + lane] = colsum;
     }
 }
 
 template <class C>
 __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensorMap* tmB0,
                                           const CUtensorMap* tmB1, const GemmArgs& a) {
+    constexpr int CG = C::CG;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -224,6 +241,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
     const uint32_t TFULL0 = bar0 + 16u * C::STAGES, TEMPTY0 = TFULL0 + 16u, DRAIN = TFULL0 + 32u;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = CG == 2 ? ptx::cluster_ctarank() : 0u;   // 0 = leader of the pair
+    const int unit = CG == 2 ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int units = CG == 2 ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
@@ -232,7 +252,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(TFULL0 + 8u * b, 1);
-            ptx::mbar_init(TEMPTY0 + 8u * b, 4);
+            ptx::mbar_init(TEMPTY0 + 8u * b, 4 * CG);   // every epilogue warp of the group
         }
         ptx::mbar_init(DRAIN, 1);
         *abort_flag = 0;
@@ -240,11 +260,16 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
         ptx::fence_proxy_async_smem();
     }
     if (warp == 1) {
-        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::TMEM_COLS);
-        ptx::tmem_relinquish();
+        if constexpr (CG == 2) {
+            ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), C::TMEM_COLS);
+            ptx::tmem_relinquish_pair();
+        } else {
+            ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::TMEM_COLS);
+            ptx::tmem_relinquish();
+        }
     }
     ptx::tc_fence_before();
-    __syncthreads();
+    if constexpr (CG == 2) ptx::cluster_sync(); else __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -257,25 +282,32 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < a.num_tiles; tile += gridDim.x) {
+        for (int tile = unit; ok && tile < a.num_tiles; tile += units) {
             int mt, nt;
-            tile_coords(tile, a.tiles_m, a.tiles_n, mt, nt);
+            tile_coords<16 / CG>(tile, a.tiles_m, a.tiles_n, mt, nt);
+            const int arow = mt * C::TILE_M + static_cast<int>(rank) * kBM;
+            const int brow = nt * C::BN + static_cast<int>(rank) * C::B_ROWS;
             for (int kb = 0; kb < a.num_kb; ++kb) {
                 if (!wait_bounded(EMPTY0 + 8u * stage, phase ^ 1u, abort_flag, true)) {
                     ok = false;
                     break;
                 }
                 const uint32_t full = FULL0 + 8u * stage;
+                // the pair's copies all count on the leader's barrier
+                const uint32_t full_at = CG == 2 ? ptx::mapa_shared(full, 0) : full;
                 const uint32_t sA = base + stage * C::STAGE_BYTES;
                 const uint32_t sB0 = sA + C::A_BYTES;
-                ptx::mbar_arrive_expect_tx(full, C::STAGE_BYTES);
+                if (rank == 0) ptx::mbar_arrive_expect_tx(full, C::TX_BYTES);
+                auto load = [&](uint32_t dst, const CUtensorMap* m, int x, int y) {
+                    if constexpr (CG == 2) ptx::tma_load_2d_pair(dst, m, x, y, full_at);
+                    else ptx::tma_load_2d(dst, m, x, y, full_at);
+                };
                 const int k0 = kb * C::BK;
                 if constexpr (C::A_MN) {
 #pragma unroll
-                    for (int j = 0; j < kBM / 64; ++j)
-                        ptx::tma_load_2d(sA + j * 64 * C::BK * 2, tmA, mt * kBM + j * 64, k0, full);
+                    for (int j = 0; j < kBM / 64; ++j) load(sA + j * 64 * C::BK * 2, tmA, arow + j * 64, k0);
                 } else {
-                    ptx::tma_load_2d(sA, tmA, k0, mt * kBM, full);
+                    load(sA, tmA, k0, arow);
                 }
 #pragma unroll
                 for (int b = 0; b < C::NB; ++b) {
@@ -283,10 +315,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
                     const uint32_t sB = sB0 + b * C::B_BYTES;
                     if constexpr (C::B_MN) {
 #pragma unroll
-                        for (int j = 0; j < C::BN / 64; ++j)
-                            ptx::tma_load_2d(sB + j * 64 * C::BK * 2, tmB, nt * C::BN + j * 64, k0, full);
+                        for (int j = 0; j < C::B_ROWS / 64; ++j) load(sB + j * 64 * C::BK * 2, tmB, brow + j * 64, k0);
                     } else {
-                        ptx::tma_load_2d(sB, tmB, k0, nt * C::BN, full);
+                        load(sB, tmB, k0, brow);
                     }
                 }
                 issued |= 1u << stage;
@@ -297,14 +328,22 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
                 }
             }
         }
-    } else if (warp == 1 && lane == 0) {
-        // ------------------------------------------------------------ MMA issuer
-        constexpr uint32_t IDESC = make_idesc(kBM, C::BN, C::A_MN, C::B_MN);
+    } else if (warp == 1 && lane == 0 && rank == 0) {
+        // ------------------------------------------------------------ MMA issuer (leader only)
+        constexpr uint32_t IDESC = make_idesc(C::TILE_M, C::BN, C::A_MN, C::B_MN);
+        auto mma = [&](uint32_t d, uint64_t da, uint64_t db, uint32_t acc) {
+            if constexpr (CG == 2) ptx::mma_bf16_pair(d, da, db, IDESC, acc);
+            else ptx::mma_bf16(d, da, db, IDESC, acc);
+        };
+        auto commit_all = [&](uint32_t bar) {   // arrive on `bar` in every CTA of the group
+            if constexpr (CG == 2) ptx::mma_commit_pair_mc(bar, 0x3);
+            else ptx::mma_commit(bar);
+        };
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
         int local = 0;
-        for (int tile = blockIdx.x; ok && tile < a.num_tiles; tile += gridDim.x, ++local) {
+        for (int tile = unit; ok && tile < a.num_tiles; tile += units, ++local) {
             const int acc = local & 1;
             const uint32_t acc_parity = (local >> 1) & 1;
             if (!wait_bounded(TEMPTY0 + 8u * acc, acc_parity ^ 1u, abort_flag, true)) break;
@@ -321,81 +360,99 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
 #pragma unroll
                 for (int kk = 0; kk < C::BK / 16; ++kk) {
                     const uint64_t da = op_desc<C::A_MN, C::BK>(sA, kk);
-                    ptx::mma_bf16(d_tmem, da, op_desc<C::B_MN, C::BK>(sB0, kk), IDESC, (kb | kk) != 0);
-                    if constexpr (C::NB == 2)
-                        ptx::mma_bf16(d_tmem, da, op_desc<C::B_MN, C::BK>(sB0 + C::B_BYTES, kk), IDESC, 1u);
+                    mma(d_tmem, da, op_desc<C::B_MN, C::BK>(sB0, kk), (kb | kk) != 0);
+                    if constexpr (C::NB == 2) mma(d_tmem, da, op_desc<C::B_MN, C::BK>(sB0 + C::B_BYTES, kk), 1u);
                 }
-                ptx::mma_commit(EMPTY0 + 8u * stage);   // frees the stage once these MMAs are done
+                commit_all(EMPTY0 + 8u * stage);   // frees the stage once these MMAs are done
                 if (++stage == C::STAGES) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
             if (!ok) break;
-            ptx::mma_commit(TFULL0 + 8u * acc);          // accumulator ready for the epilogue
+            commit_all(TFULL0 + 8u * acc);          // accumulator ready for the epilogue
         }
         // every MMA this thread issued completes before TMEM and shared memory go away
-        ptx::mma_commit(DRAIN);
+        if constexpr (CG == 2) ptx::mma_commit_pair(DRAIN); else ptx::mma_commit(DRAIN);
         wait_bounded(DRAIN, 0, abort_flag, false);
     } else if (warp >= 2) {
         // ------------------------------------------------------------ epilogue
         const int quad = warp & 3;   // a warp may touch TMEM lanes 32*(warp%4) .. +31
+        const uint32_t tempty_leader = CG == 2 ? ptx::mapa_shared(TEMPTY0, 0) : TEMPTY0;
         int local = 0;
-        for (int tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x, ++local) {
+        for (int tile = unit; tile < a.num_tiles; tile += units, ++local) {
             const int acc = local & 1;
             const uint32_t acc_parity = (local >> 1) & 1;
             if (!wait_bounded(TFULL0 + 8u * acc, acc_parity, abort_flag, true)) break;
             ptx::tc_fence_after();
             int mt, nt;
-            tile_coords(tile, a.tiles_m, a.tiles_n, mt, nt);
-            const int row = mt * kBM + quad * 32 + lane;
-            const uint32_t trow = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * C::BN;
+            tile_coords<16 / CG>(tile, a.tiles_m, a.tiles_n, mt, nt);
+            const int row0 = mt * C::TILE_M + static_cast<int>(rank) * kBM;
+            if (row0 < a.Mg) {   // a pair's second half may lie wholly past the last row
+                const int tile128 = mt * CG + static_cast<int>(rank);
+                const int row = row0 + quad * 32 + lane;
+                const uint32_t trow = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * C::BN;
 #pragma unroll 1
-            for (int j = 0; j < C::BN / 32; ++j) {
-                const int c0 = nt * C::BN + j * 32;
-                if (c0 >= a.Ng) break;
-                uint32_t r[32];
-                ptx::tmem_ld_32x32b_x32(trow + j * 32, r);
-                ptx::tmem_wait_ld();
-                epilogue_chunk<C>(a, r, row, c0, mt, quad, lane);
+                for (int j = 0; j < C::BN / 32; ++j) {
+                    const int c0 = nt * C::BN + j * 32;
+                    if (c0 >= a.Ng) break;
+                    uint32_t r[32];
+                    ptx::tmem_ld_32x32b_x32(trow + j * 32, r);
+                    ptx::tmem_wait_ld();
+                    epilogue_chunk<C>(a, r, row, c0, tile128, quad, lane);
+                }
             }
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(TEMPTY0 + 8u * acc);
+            if (lane == 0) {
+                if constexpr (CG == 2) ptx::mbar_arrive_cluster(tempty_leader + 8u * acc);
+                else ptx::mbar_arrive(TEMPTY0 + 8u * acc);
+            }
         }
     }
 
     ptx::tc_fence_before();
-    __syncthreads();
+    if constexpr (CG == 2) ptx::cluster_sync(); else __syncthreads();
     if (warp == 1) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
+        if constexpr (CG == 2) ptx::tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+        else ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
     if (warp == 0 && lane == 0 && *abort_flag) {
         // after an abort, copies still in flight must land before the CTA's shared memory is released
-        for (int s = 0; s < C::STAGES; ++s)
-            if (issued & (1u << s)) wait_bounded(FULL0 + 8u * s, (issued_parity >> s) & 1u, abort_flag, false);
+        if constexpr (CG == 1) {
+            for (int s = 0; s < C::STAGES; ++s)
+                if (issued & (1u << s)) wait_bounded(FULL0 + 8u * s, (issued_parity >> s) & 1u, abort_flag, false);
+        } else {
+            // a pair's copies complete on the leader's barriers; give them time to land
+            const uint64_t t0 = ptx::globaltimer();
+            while (ptx::globaltimer() - t0 < 100000ull) {
+            }
+        }
     }
 }
 
 }  // namespace
 
+template <int CG>
 __global__ void __launch_bounds__(kThreads, 1)
     tern_fwd_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const GemmArgs a) {
-    gemm_body<FwdCfg>(&tmA, &tmB, &tmB, a);
+    gemm_body<std::conditional_t<CG == 2, Fwd2, Fwd1>>(&tmA, &tmB, &tmB, a);
 }
 
+template <int CG>
 __global__ void __launch_bounds__(kThreads, 1)
     tern_dx_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmBhi,
                  const __grid_constant__ CUtensorMap tmBlo, const GemmArgs a) {
-    gemm_body<DxCfg>(&tmA, &tmBhi, &tmBlo, a);
+    gemm_body<std::conditional_t<CG == 2, Dx2, Dx1>>(&tmA, &tmBhi, &tmBlo, a);
 }
 
+template <int CG>
 __global__ void __launch_bounds__(kThreads, 1)
     tern_dw_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const GemmArgs a) {
-    gemm_body<DwCfg>(&tmA, &tmB, &tmB, a);
+    gemm_body<std::conditional_t<CG == 2, Dw2, Dw1>>(&tmA, &tmB, &tmB, a);
 }
 
 // sgrad[c] = sum over the partial rows in ascending order (deterministic).
@@ -444,31 +501,104 @@ int map_bf16(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, int 
     return r == CUDA_SUCCESS ? TERN_OK : TERN_ERR_CUDA;
 }
 
+// Boxes of one operand: K-major tiles are read as one box of BK x rows; MN-major
+// tiles as 64-wide boxes of BK k-rows.
+template <class C>
+int map_operand(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, bool mn, int rows) {
+    const CUtensorMapSwizzle sw = C::BK == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    return mn ? map_bf16(m, ptr, inner, outer, 64, C::BK, sw) : map_bf16(m, ptr, inner, outer, C::BK, rows, sw);
+}
+
 template <class C>
 GemmArgs make_args(int64_t Mg, int64_t Ng, int64_t Kg) {
     GemmArgs a{};
     a.Mg = static_cast<int>(Mg);
     a.Ng = static_cast<int>(Ng);
     a.Kg = static_cast<int>(Kg);
-    a.tiles_m = static_cast<int>((Mg + kBM - 1) / kBM);
+    a.tiles_m = static_cast<int>((Mg + C::TILE_M - 1) / C::TILE_M);
     a.tiles_n = static_cast<int>((Ng + C::BN - 1) / C::BN);
     a.num_tiles = a.tiles_m * a.tiles_n;
     a.num_kb = static_cast<int>((Kg + C::BK - 1) / C::BK);
     return a;
 }
 
+// Persistent launch: one CTA (or CTA pair) per SM (pair of SMs), at most one per tile.
 template <class C, class K, class... Maps>
 int launch(K kernel, const GemmArgs& a, int num_sms, cudaStream_t s, const Maps&... maps) {
     TERN_CUDA_TRY(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES));
-    const int grid = std::min(a.num_tiles, num_sms);
-    kernel<<<grid, kThreads, C::SMEM_BYTES, s>>>(maps..., a);
-    TERN_CUDA_TRY(cudaGetLastError());
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = s;
+    if constexpr (C::CG == 2) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        static int max_clusters = 0;   // co-resident CTA pairs of this kernel
+        if (max_clusters == 0) {
+            cfg.gridDim = dim3(2 * (num_sms / 2));
+            int n = 0;
+            TERN_CUDA_TRY(cudaOccupancyMaxActiveClusters(&n, kernel, &cfg));
+            max_clusters = n > 0 ? n : 1;
+        }
+        cfg.gridDim = dim3(2 * std::min(a.num_tiles, max_clusters));
+    } else {
+        cfg.attrs = nullptr;
+        cfg.numAttrs = 0;
+        cfg.gridDim = dim3(std::min(a.num_tiles, num_sms));
+    }
+    TERN_CUDA_TRY(cudaLaunchKernelEx(&cfg, kernel, maps..., a));
     return TERN_OK;
 }
 
 bool dims_ok(int64_t M, int64_t K, int64_t N) {
     return M >= 1 && K >= 16 && N >= 16 && M < (1ll << 31) && K < (1ll << 31) && N < (1ll << 31) &&
            M * K < (1ll << 40) && K * N < (1ll << 40) && M * N < (1ll << 40);
+}
+
+// A CTA pair per tile once the output has at least two 128-row blocks.
+bool use_pair(int64_t Mg) { return Mg > kBM; }
+
+template <class C, class K>
+int run_fwd(K kernel, const uint16_t* X, const uint16_t* T, const float* scale, float* Y, int64_t M, int64_t K_,
+            int64_t N, int num_sms, cudaStream_t s) {
+    CUtensorMap mA, mB;
+    if (int st = map_operand<C>(&mA, X, K_, M, C::A_MN, kBM)) return st;
+    if (int st = map_operand<C>(&mB, T, N, K_, C::B_MN, C::B_ROWS)) return st;
+    GemmArgs a = make_args<C>(M, N, K_);
+    a.out = Y;
+    a.scale = scale;
+    return launch<C>(kernel, a, num_sms, s, mA, mB);
+}
+
+template <class C, class K>
+int run_dx(K kernel, const uint16_t* dY, const uint16_t* whi, const uint16_t* wlo, float* dX, int64_t M,
+           int64_t K_, int64_t N, int num_sms, cudaStream_t s) {
+    CUtensorMap mA, mHi, mLo;
+    if (int st = map_operand<C>(&mA, dY, N, M, C::A_MN, kBM)) return st;
+    if (int st = map_operand<C>(&mHi, whi, N, K_, C::B_MN, C::B_ROWS)) return st;
+    if (int st = map_operand<C>(&mLo, wlo, N, K_, C::B_MN, C::B_ROWS)) return st;
+    GemmArgs a = make_args<C>(M, K_, N);
+    a.out = dX;
+    return launch<C>(kernel, a, num_sms, s, mA, mHi, mLo);
+}
+
+template <class C, class K>
+int run_dw(K kernel, const uint16_t* X, const uint16_t* dY, const float* scale, const uint32_t* packed, float* gq,
+           float* partial, int64_t M, int64_t K_, int64_t N, int num_sms, cudaStream_t s) {
+    CUtensorMap mA, mB;
+    if (int st = map_operand<C>(&mA, X, K_, M, C::A_MN, kBM)) return st;
+    if (int st = map_operand<C>(&mB, dY, N, M, C::B_MN, C::B_ROWS)) return st;
+    GemmArgs a = make_args<C>(K_, N, M);
+    a.out = gq;
+    a.scale = scale;
+    a.packed = packed;
+    a.partial = partial;
+    return launch<C>(kernel, a, num_sms, s, mA, mB);
 }
 
 }  // namespace
@@ -495,13 +625,9 @@ extern "C" int tern_linear_fwd(const uint16_t* X, const tern_tiles* W, const flo
     if (!aligned16(X) || !aligned16(W->t_bf16) || !aligned16(scale) || !aligned16(Y)) return TERN_ERR_ALIGN;
     int num_sms = 0;
     if (int st = check_device(&num_sms)) return st;
-    CUtensorMap mA, mB;
-    if (int st = map_bf16(&mA, X, K, M, 64, kBM, CU_TENSOR_MAP_SWIZZLE_128B)) return st;
-    if (int st = map_bf16(&mB, W->t_bf16, N, K, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)) return st;
-    GemmArgs a = make_args<FwdCfg>(M, N, K);
-    a.out = Y;
-    a.scale = scale;
-    return launch<FwdCfg>(tern_fwd_gemm, a, num_sms, static_cast<cudaStream_t>(stream), mA, mB);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (use_pair(M)) return run_fwd<Fwd2>(tern_fwd_gemm<2>, X, W->t_bf16, scale, Y, M, K, N, num_sms, s);
+    return run_fwd<Fwd1>(tern_fwd_gemm<1>, X, W->t_bf16, scale, Y, M, K, N, num_sms, s);
 }
 
 extern "C" size_t tern_linear_bwd_workspace(int64_t M, int64_t K, int64_t N) {
@@ -529,27 +655,21 @@ extern "C" int tern_linear_bwd(const uint16_t* X, const uint16_t* dY, const tern
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     if (dX) {
-        CUtensorMap mA, mHi, mLo;
-        if (int st = map_bf16(&mA, dY, N, M, 32, kBM, CU_TENSOR_MAP_SWIZZLE_64B)) return st;
-        if (int st = map_bf16(&mHi, W->whi_bf16, N, K, 32, DxCfg::BN, CU_TENSOR_MAP_SWIZZLE_64B)) return st;
-        if (int st = map_bf16(&mLo, W->wlo_bf16, N, K, 32, DxCfg::BN, CU_TENSOR_MAP_SWIZZLE_64B)) return st;
-        GemmArgs a = make_args<DxCfg>(M, K, N);
-        a.out = dX;
-        if (int st = launch<DxCfg>(tern_dx_gemm, a, num_sms, s, mA, mHi, mLo)) return st;
+        const int st = use_pair(M)
+                           ? run_dx<Dx2>(tern_dx_gemm<2>, dY, W->whi_bf16, W->wlo_bf16, dX, M, K, N, num_sms, s)
+                           : run_dx<Dx1>(tern_dx_gemm<1>, dY, W->whi_bf16, W->wlo_bf16, dX, M, K, N, num_sms, s);
+        if (st) return st;
     }
     if (gq || sgrad) {
-        CUtensorMap mA, mB;
-        if (int st = map_bf16(&mA, X, K, M, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)) return st;
-        if (int st = map_bf16(&mB, dY, N, M, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)) return st;
-        GemmArgs a = make_args<DwCfg>(K, N, M);
-        a.out = gq;
-        a.scale = scale;
-        a.packed = W->packed;
-        a.partial = sgrad ? static_cast<float*>(workspace) : nullptr;
-        if (int st = launch<DwCfg>(tern_dw_gemm, a, num_sms, s, mA, mB)) return st;
+        float* partial = sgrad ? static_cast<float*>(workspace) : nullptr;
+        const int st = use_pair(K) ? run_dw<Dw2>(tern_dw_gemm<2>, X, dY, scale, W->packed, gq, partial, M, K, N,
+                                                 num_sms, s)
+                                   : run_dw<Dw1>(tern_dw_gemm<1>, X, dY, scale, W->packed, gq, partial, M, K, N,
+                                                 num_sms, s);
+        if (st) return st;
         if (!sgrad) return TERN_OK;
-        const int nparts = a.tiles_m * 4;
-        tern_sgrad_reduce<<<static_cast<unsigned>((N + 255) / 256), 256, 0, s>>>(a.partial, nparts,
+        const int nparts = static_cast<int>((K + kBM - 1) / kBM) * 4;
+        tern_sgrad_reduce<<<static_cast<unsigned>((N + 255) / 256), 256, 0, s>>>(partial, nparts,
                                                                                  static_cast<int>(N), sgrad);
         TERN_CUDA_TRY(cudaGetLastError());
     }
