@@ -46,6 +46,7 @@ __device__ __forceinline__ uint32_t lanes16(uint32_t bytemask, uint32_t sel) {
     return __byte_perm(bytemask, 0u, sel);
 }
 
+template <bool QC, bool PK, bool TT, bool HL>
 __device__ __forceinline__ void encode_group(const MatArgs& a, int4 raw, int64_t gi) {
     const uint32_t w[4] = {static_cast<uint32_t>(raw.x), static_cast<uint32_t>(raw.y),
                            static_cast<uint32_t>(raw.z), static_cast<uint32_t>(raw.w)};
@@ -61,7 +62,7 @@ __device__ __forceinline__ void encode_group(const MatArgs& a, int4 raw, int64_t
         code |= x << (8 * k);
     }
     const int64_t e0 = gi * 16;
-    if (a.qc) {
+    if constexpr (QC) {
         int4 c;
         c.x = static_cast<int>(__vmaxs4(__vmins4(w[0], a.cl_pos), a.cl_neg));
         c.y = static_cast<int>(__vmaxs4(__vmins4(w[1], a.cl_pos), a.cl_neg));
@@ -69,7 +70,8 @@ __device__ __forceinline__ void encode_group(const MatArgs& a, int4 raw, int64_t
         c.w = static_cast<int>(__vmaxs4(__vmins4(w[3], a.cl_pos), a.cl_neg));
         __stcs(reinterpret_cast<int4*>(a.qc + e0), c);
     }
-    if (a.packed) __stcs(a.packed + gi, code);
+    if constexpr (PK) __stcs(a.packed + gi, code);
+    if constexpr (!TT && !HL) return;
     // 16-bit lane masks of weight pairs (2i, 2i+1): nz = weight != 0, ng = weight < 0
     uint32_t nz[8], ng[8];
 #pragma unroll
@@ -79,7 +81,7 @@ __device__ __forceinline__ void encode_group(const MatArgs& a, int4 raw, int64_t
         ng[2 * k] = lanes16(neg[k], 0x1100u);
         ng[2 * k + 1] = lanes16(neg[k], 0x3322u);
     }
-    if (a.t) {
+    if constexpr (TT) {
         uint32_t p[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) p[i] = (nz[i] & 0x3F803F80u) | (ng[i] & 0x80008000u);
@@ -87,7 +89,7 @@ __device__ __forceinline__ void encode_group(const MatArgs& a, int4 raw, int64_t
         __stcs(dst, make_int4(p[0], p[1], p[2], p[3]));
         __stcs(dst + 1, make_int4(p[4], p[5], p[6], p[7]));
     }
-    if (a.whi || a.wlo) {
+    if constexpr (HL) {
         const uint32_t cg = static_cast<uint32_t>(gi % a.ngroups_row);
         const float4* sp = reinterpret_cast<const float4*>(a.scale + static_cast<int64_t>(cg) * 16);
         uint32_t hi2[8], lo2[8];
@@ -128,19 +130,58 @@ __device__ __forceinline__ void encode_group(const MatArgs& a, int4 raw, int64_t
 
 }  // namespace
 
+// Which encodings a launch writes is a template choice, so the packed-only
+// ternarisation carries no registers for the bf16 planes and keeps eight 16-byte
+// loads in flight per thread.
+template <bool QC, bool PK, bool TT, bool HL>
 __global__ void __launch_bounds__(256) tern_materialize_kernel(const MatArgs a) {
+    constexpr int U = (TT || HL) ? 4 : 8;
     const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
     int64_t gi = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int4* q4 = reinterpret_cast<const int4*>(a.q);
-    for (; gi + 3 * nth < a.groups; gi += 4 * nth) {
-        int4 r[4];
+    for (; gi + (U - 1) * nth < a.groups; gi += U * nth) {
+        int4 r[U];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) r[j] = __ldcs(q4 + gi + j * nth);
+        for (int j = 0; j < U; ++j) r[j] = __ldcs(q4 + gi + j * nth);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) encode_group(a, r[j], gi + j * nth);
+        for (int j = 0; j < U; ++j) encode_group<QC, PK, TT, HL>(a, r[j], gi + j * nth);
     }
-    for (; gi < a.groups; gi += nth) encode_group(a, __ldcs(q4 + gi), gi);
+    for (; gi < a.groups; gi += nth) encode_group<QC, PK, TT, HL>(a, __ldcs(q4 + gi), gi);
 }
+
+namespace {
+
+template <bool QC, bool PK, bool TT, bool HL>
+int launch_materialize(const MatArgs& a, int num_sms, cudaStream_t s) {
+    auto kernel = tern_materialize_kernel<QC, PK, TT, HL>;
+    static int per_sm = 0;   // resident CTAs per SM (the grid strides over the rest)
+    if (per_sm == 0) {
+        int b = 0;
+        TERN_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, 256, 0));
+        per_sm = b > 0 ? b : 1;
+    }
+    const int64_t want = (a.groups + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(num_sms) * per_sm;
+    const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
+    kernel<<<grid, 256, 0, s>>>(a);
+    TERN_CUDA_TRY(cudaGetLastError());
+    return TERN_OK;
+}
+
+template <bool QC, bool PK, bool TT>
+int dispatch_hl(const MatArgs& a, bool hl, int n, cudaStream_t s) {
+    return hl ? launch_materialize<QC, PK, TT, true>(a, n, s) : launch_materialize<QC, PK, TT, false>(a, n, s);
+}
+template <bool QC, bool PK>
+int dispatch_t(const MatArgs& a, bool tt, bool hl, int n, cudaStream_t s) {
+    return tt ? dispatch_hl<QC, PK, true>(a, hl, n, s) : dispatch_hl<QC, PK, false>(a, hl, n, s);
+}
+template <bool QC>
+int dispatch_pk(const MatArgs& a, bool pk, bool tt, bool hl, int n, cudaStream_t s) {
+    return pk ? dispatch_t<QC, true>(a, tt, hl, n, s) : dispatch_t<QC, false>(a, tt, hl, n, s);
+}
+
+}  // namespace
 
 }  // namespace tern
 
@@ -174,18 +215,11 @@ extern "C" int tern_materialize(const int8_t* q, int8_t* q_clamped, const float*
     a.th_neg = tn * 0x01010101u;
     a.cl_pos = cb * 0x01010101u;
     a.cl_neg = cn * 0x01010101u;
-    static int per_sm = 0;   // resident CTAs per SM (the grid strides over the rest)
-    if (per_sm == 0) {
-        int b = 0;
-        TERN_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, tern_materialize_kernel, 256, 0));
-        per_sm = b > 0 ? b : 1;
-    }
-    const int64_t want = (a.groups + 255) / 256;
-    const int64_t cap = static_cast<int64_t>(num_sms) * per_sm;
-    const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
-    tern_materialize_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
-    TERN_CUDA_TRY(cudaGetLastError());
-    return TERN_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool qc = q_clamped != nullptr, pk = out->packed != nullptr, tt = out->t_bf16 != nullptr;
+    const bool hl = out->whi_bf16 != nullptr || out->wlo_bf16 != nullptr;
+    if (!qc && !pk && !tt && !hl) return TERN_OK;   // nothing requested
+    return qc ? dispatch_pk<true>(a, pk, tt, hl, num_sms, s) : dispatch_pk<false>(a, pk, tt, hl, num_sms, s);
 }
 
 extern "C" size_t tern_tiles_bytes(int64_t K, int64_t N, int which) {
