@@ -72,10 +72,7 @@ struct Cfg {
     static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES;   // per CTA
     static constexpr int TX_BYTES = CG * STAGE_BYTES;            // landing on the leader's barrier
     static constexpr int TMEM_COLS = 2 * BN;
-    // A pair keeps 32 KB of slack past the last stage: an MMA operand read of a
-    // whole B tile (not half) from the last stage would still stay inside the
-    // CTA's shared memory.
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + (CG == 2 ? 32768 : 0) + 1024 + 256;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
     static_assert(CG == 1 || CG == 2, "CTA group");
     static_assert(BK == 64 || (BK == 32 && !A_MN && !B_MN), "MN-major operands use 64-deep k-blocks");
     static_assert(BN % 64 == 0 && BN <= 256 && B_ROWS % 64 == 0, "BN");
@@ -88,9 +85,9 @@ using Fwd1 = Cfg<1, 256, 64, false, true, 1, EPI_FWD, 4>;   // A = X (K-major), 
 using Dx1 = Cfg<1, 256, 32, false, false, 2, EPI_DX, 5>;    // A = dY (K-major), B = W_hi, W_lo (K-major)
 using Dw1 = Cfg<1, 256, 64, true, true, 1, EPI_DW, 4>;      // A = X^T, B = dY^T (both MN-major)
 // A CTA pair per 256 x 256 tile: half the shared-memory operand traffic per MMA.
-using Fwd2 = Cfg<2, 256, 64, false, true, 1, EPI_FWD, 6>;
+using Fwd2 = Cfg<2, 256, 64, false, true, 1, EPI_FWD, 7>;
 using Dx2 = Cfg<2, 256, 64, false, false, 2, EPI_DX, 4>;
-using Dw2 = Cfg<2, 256, 64, true, true, 1, EPI_DW, 6>;
+using Dw2 = Cfg<2, 256, 64, true, true, 1, EPI_DW, 7>;
 
 // tcgen05 instruction descriptor, kind::f16: bf16 A/B, fp32 D, M x N, operand majors.
 __host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool a_mn, bool b_mn) {
