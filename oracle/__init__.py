@@ -60,6 +60,11 @@ def _L():
             "or_gq_at": ([vp, vp, flt, i64, vp, vp], None),
             "or_sgrad_at": ([vp, vp, vp, i64, i64, ci, vp, vp, ci], None),
             "or_adamw": ([vp, vp, vp, vp, i64, ci, dbl, dbl, dbl, dbl, dbl, dbl, ci, vp, vp, vp], None),
+            "or_mix64": ([ctypes.c_uint64], ctypes.c_uint64),
+            "or_sr4_uniform": ([ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64], flt),
+            "or_sr4_scale": ([vp, i64, flt, flt], flt),
+            "or_sr4_update": ([vp, vp, i64, flt, flt, ctypes.c_uint64, i64, ctypes.c_uint64, ci, ci, vp, vp],
+                              None),
         }
         for name, (args, res) in sig.items():
             f = getattr(lib, name)
@@ -180,3 +185,28 @@ def adamw(w, g, m, v, t, lr, b1, b2, eps, wd, gmul=1.0, decoupled=True):
     _L().or_adamw(_p(w), _p(g), _p(m), _p(v), n, int(t), f32(lr), f32(b1), f32(b2), f32(eps), f32(wd),
                   f32(gmul), 1 if decoupled else 0, _p(wo), _p(mo), _p(vo))
     return wo, mo, vo
+
+
+# ----------------------------------------------------------------- SR4 (parity unpinned)
+
+def mix64(z: int) -> int:
+    return int(_L().or_mix64(int(z) & 0xFFFFFFFFFFFFFFFF))
+
+
+def sr4_uniform(seed, counter, j) -> float:
+    return float(_L().or_sr4_uniform(seed, counter, j))
+
+
+def sr4_scale(gq, inv_bs=1.0, target_step=0.003) -> float:
+    gq = _c(gq, np.float32)
+    return float(_L().or_sr4_scale(_p(gq), gq.size, float(inv_bs), float(target_step)))
+
+
+def sr4_update(q, gq, s, inv_bs=1.0, seed=42, idx_base=0, counter=0, q_clamp=SR4_Q_CLAMP, dither=True):
+    """New q (int8) and the fp32 value y = x + u whose floor is the step taken."""
+    q, gq = _c(q, np.int8), _c(gq, np.float32)
+    out = np.empty_like(q)
+    y = np.empty(q.shape, np.float32)
+    _L().or_sr4_update(_p(q), _p(gq), q.size, float(inv_bs), float(s), int(seed), int(idx_base), int(counter),
+                       int(q_clamp), 1 if dither else 0, _p(out), _p(y))
+    return out, y

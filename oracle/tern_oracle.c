@@ -27,6 +27,10 @@
  * index order.  "abs" outputs are the sums of |term| of each output's dot
  * product, the denominators of the comparison tolerance.
  *
+ * SR4 q-update (or_sr4_*): PARITY UNPINNED.  The page names fc_sr4_scale and
+ * fc_sr4_update but does not print their bodies; the functions below state the
+ * plainest reading of their arguments and are pinned only by invariants.
+ *
  * Readings where the pages leave a step open:
  *   - the AdamW body is not on the pages: decoupled decay uses the old weight,
  *     w' = w - lr*wd*w - lr*mhat/(sqrt(vhat)+eps); with decoupled = 0 the decay
@@ -400,5 +404,75 @@ void or_adamw(const float* w, const float* g, const float* m, const float* v, in
         w_out[i] = wi - decay - step;
         m_out[i] = mi;
         v_out[i] = vi;
+    }
+}
+
+/* ------------------------------------------------------------ SR4 q-update */
+
+/*
+ * SR4 step on one ternary matrix's accumulator q (page "train_gpu.cu": sr4_dev
+ * calls fc_sr4_scale<<<1,1>>>(gq, numel, inv_bs, target_step, d_s) and then
+ * fc_sr4_update(q, gq, numel, inv_bs, d_s, seed, idx_base, counter, q_clamp,
+ * use_dither); both bodies are off the page).  PARITY UNPINNED: the oracle
+ * states the plainest reading of those names, and only invariants pin it:
+ *
+ *   step scalar   s = target_step / mean_i |gq_i * inv_bs|      (s = 0 when the mean is 0)
+ *                 so that the mean requested step is target_step accumulator units;
+ *   update        x_i = (gq_i * inv_bs) * s
+ *                 q_i <- clamp(q_i - floor(x_i + u_i), -q_clamp, q_clamp)
+ *                 with u_i ~ U[0,1) from the counter RNG (use_dither), else u_i = 1/2:
+ *                 stochastic rounding of the descent step -x_i into the int4 accumulator
+ *                 ("SR4"), E[q_new - q] = -x_i away from the clamp;
+ *                 a non-finite x_i leaves q_i unchanged.
+ *
+ * Precision: the decisions are taken in fp32 as the GPU takes them: gq*inv_bs, *s
+ * and +u are separate fp32 operations (no fused multiply-add); the mean is an fp64
+ * sum of the fp32 products, divided by n in fp64 and rounded to fp32; s is an fp32
+ * division.
+ *
+ * Counter RNG (splitmix64, Steele, Lea and Flood, OOPSLA 2014): mix is the
+ * splitmix64 output function, G = 0x9E3779B97F4A7C15, key = mix(seed ^ (counter*G)),
+ * u(j) = (mix(key + (j+1)*G) >> 40) * 2^-24 for global element index j = idx_base + i.
+ */
+uint64_t or_mix64(uint64_t z) {
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBULL;
+    return z ^ (z >> 31);
+}
+
+#define OR_G 0x9E3779B97F4A7C15ULL
+
+float or_sr4_uniform(uint64_t seed, uint64_t counter, uint64_t j) {
+    uint64_t key = or_mix64(seed ^ (counter * OR_G));
+    uint64_t d = or_mix64(key + (j + 1) * OR_G);
+    return (float)(d >> 40) * (1.0f / 16777216.0f);
+}
+
+float or_sr4_scale(const float* gq, int64_t n, float inv_bs, float target_step) {
+    double sum = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        float g = gq[i] * inv_bs;
+        sum += fabs((double)g);
+    }
+    float mean = n > 0 ? (float)(sum / (double)n) : 0.0f;
+    if (!(mean > 0.0f) || !isfinite(mean)) return 0.0f;
+    return target_step / mean;
+}
+
+void or_sr4_update(const int8_t* q, const float* gq, int64_t n, float inv_bs, float s, uint64_t seed,
+                   int64_t idx_base, uint64_t counter, int clamp, int dither, int8_t* q_out, float* y_out) {
+    for (int64_t i = 0; i < n; ++i) {
+        float x = (gq[i] * inv_bs) * s;
+        float u = dither ? or_sr4_uniform(seed, counter, (uint64_t)(idx_base + i)) : 0.5f;
+        float y = x + u;
+        if (y_out) y_out[i] = y;
+        int v = q[i];
+        if (isfinite(y)) {
+            float d = floorf(y);
+            if (d > 300.0f) d = 300.0f;
+            if (d < -300.0f) d = -300.0f;
+            v = or_clamp(v - (int)d, clamp);
+        }
+        q_out[i] = (int8_t)v;
     }
 }
