@@ -37,8 +37,8 @@ TERN_TILE_PACKED, TERN_TILE_T, TERN_TILE_WHI, TERN_TILE_WLO = 0, 1, 2, 3
 
 # the C ABI's exported symbols (tests check the library exports every one)
 ABI_SYMBOLS = ("tern_tiles_bytes", "tern_materialize", "tern_linear_fwd", "tern_linear_bwd_workspace",
-               "tern_linear_bwd", "tern_linear_bwd_noalloc", "adamw_step", "tern_strerror",
-               "tern_device_status")
+               "tern_linear_bwd", "tern_linear_bwd_noalloc", "adamw_step", "tern_sr4_workspace",
+               "tern_sr4_step", "tern_strerror", "tern_device_status")
 
 
 class TernError(RuntimeError):
@@ -66,6 +66,8 @@ def _load():
         "tern_linear_bwd": ([vp, vp, tp, vp, vp, vp, vp, vp, sz, i64, i64, i64, vp], ci),
         "tern_linear_bwd_noalloc": ([vp, vp, tp, vp, vp, vp, vp, i64, i64, i64, vp], ci),
         "adamw_step": ([vp, vp, vp, vp, i64, ci, cf, cf, cf, cf, cf, cf, ci, vp], ci),
+        "tern_sr4_workspace": ([i64], sz),
+        "tern_sr4_step": ([vp, vp, i64, cf, cf, ctypes.c_uint64, i64, ctypes.c_uint64, ci, ci, vp, vp, sz, vp], ci),
         "tern_strerror": ([ci], ctypes.c_char_p),
         "tern_device_status": ([vp, ci], ci),
     }
@@ -208,6 +210,24 @@ def adamw_step(w, g, m, v, t, lr, b1, b2, eps, wd, gmul=1.0, decoupled=True, str
                           float(lr), float(b1), float(b2), float(eps), float(wd), float(gmul),
                           1 if decoupled else 0, _stream(stream)),
            "adamw_step")
+
+
+def tern_sr4_workspace(numel) -> int:
+    return int(lib.tern_sr4_workspace(int(numel)))
+
+
+def tern_sr4_step(q, gq, workspace, inv_bs=1.0, target_step=0.003, seed=42, idx_base=0, counter=0, q_clamp=7,
+                  use_dither=True, s_out=None, stream=None):
+    """SR4 step: q (int8, in place) moves by stochastic rounding of -gq*inv_bs*s (see tern.h)."""
+    n = q.numel()
+    if gq.numel() != n:
+        raise ValueError("q and gq differ in size")
+    _check(lib.tern_sr4_step(_ptr(q, torch.int8, None, "q"), _ptr(gq, torch.float32, None, "gq"), n,
+                             float(inv_bs), float(target_step), int(seed), int(idx_base), int(counter),
+                             int(q_clamp), 1 if use_dither else 0, _ptr(s_out, torch.float32, None, "s_out"),
+                             _ptr(workspace, workspace.dtype, None, "workspace"),
+                             workspace.numel() * workspace.element_size(), _stream(stream)),
+           "tern_sr4_step")
 
 
 def tern_device_status(stream=None, clear=True) -> int:

@@ -1,0 +1,171 @@
+// SR4 step: stochastic-rounding update of the int4 accumulator q from the
+// straight-through gradient gq (page "train_gpu.cu": sr4_dev runs
+// fc_sr4_scale<<<1,1>>> and then fc_sr4_update; the bodies are off the page).
+// Reading implemented here (the same reading the oracle states):
+//
+//   s    = target_step / mean_i |gq_i * inv_bs|             (0 when the mean is 0)
+//   q_i <- clamp(q_i - floor(x_i + u_i), +-q_clamp),  x_i = (gq_i * inv_bs) * s
+//
+// u_i ~ U[0,1) from a counter-based splitmix64 stream keyed by (seed, counter)
+// and indexed by the global element index idx_base + i (u_i = 1/2 without
+// dither); a non-finite x_i leaves q_i unchanged.
+//
+// Three launches instead of the page's single-thread scale kernel:
+//   1. tern_sr4_absum     per-CTA fp64 sums of |gq*inv_bs| over fixed contiguous
+//                         slices (deterministic), written to the workspace;
+//   2. tern_sr4_finalize  one CTA: fixed-order sum, mean, s (fp32);
+//   3. tern_sr4_update    streaming update, 16 weights per thread per iteration
+//                         (16-byte q loads/stores, 4 float4 gq loads).
+// The update's arithmetic uses explicitly rounded fp32 operations (no fused
+// multiply-add), so the rounding decision is the oracle's decision.
+#include "common.cuh"
+
+namespace tern {
+
+namespace {
+
+constexpr int kAbsumBlocks = 1024;   // fixed slicing: the sum order does not depend on the GPU
+constexpr uint64_t kG = 0x9E3779B97F4A7C15ull;
+
+__host__ __device__ __forceinline__ uint64_t mix64(uint64_t z) {
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+struct Sr4Args {
+    int8_t* q;
+    const float* gq;
+    int64_t n;
+    float inv_bs, target;
+    uint64_t key;        // mix64(seed ^ counter*G)
+    int64_t idx_base;
+    int clamp, dither;
+    double* partial;     // [kAbsumBlocks]
+    float* s;            // device step scalar
+    float* s_out;        // optional copy for the caller
+};
+
+__device__ __forceinline__ int8_t sr4_one(const Sr4Args& a, int8_t q, float g, float s, int64_t i) {
+    const float x = __fmul_rn(__fmul_rn(g, a.inv_bs), s);
+    float u = 0.5f;
+    if (a.dither) {
+        const uint64_t d = mix64(a.key + static_cast<uint64_t>(a.idx_base + i + 1) * kG);
+        u = static_cast<float>(d >> 40) * (1.0f / 16777216.0f);
+    }
+    const float y = __fadd_rn(x, u);
+    if (!isfinite(y)) return q;
+    const float f = fminf(fmaxf(floorf(y), -300.0f), 300.0f);
+    int v = static_cast<int>(q) - static_cast<int>(f);
+    v = v > a.clamp ? a.clamp : (v < -a.clamp ? -a.clamp : v);
+    return static_cast<int8_t>(v);
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(256) tern_sr4_absum(const Sr4Args a) {
+    // block b owns the contiguous slice [b*n/B, (b+1)*n/B)
+    const int64_t lo = a.n * blockIdx.x / gridDim.x, hi = a.n * (blockIdx.x + 1) / gridDim.x;
+    double acc = 0.0;
+    for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x)
+        acc += fabs(static_cast<double>(__fmul_rn(a.gq[i], a.inv_bs)));
+    __shared__ double red[256];
+    red[threadIdx.x] = acc;
+    __syncthreads();
+    for (int w = 128; w > 0; w >>= 1) {
+        if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) a.partial[blockIdx.x] = red[0];
+}
+
+__global__ void __launch_bounds__(256) tern_sr4_finalize(const Sr4Args a, int nparts) {
+    __shared__ double red[256];
+    double acc = 0.0;
+    for (int i = threadIdx.x; i < nparts; i += blockDim.x) acc += a.partial[i];
+    red[threadIdx.x] = acc;
+    __syncthreads();
+    for (int w = 128; w > 0; w >>= 1) {
+        if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        const float mean = a.n > 0 ? static_cast<float>(red[0] / static_cast<double>(a.n)) : 0.0f;
+        const float s = (mean > 0.0f && isfinite(mean)) ? __fdiv_rn(a.target, mean) : 0.0f;
+        *a.s = s;
+        if (a.s_out) *a.s_out = s;
+    }
+}
+
+__global__ void __launch_bounds__(256) tern_sr4_update(const Sr4Args a) {
+    const float s = *a.s;
+    const int64_t groups = a.n / 16;
+    const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (int64_t g = tid; g < groups; g += nth) {
+        const int64_t e0 = g * 16;
+        int4 qv = *reinterpret_cast<const int4*>(a.q + e0);
+        const float4* gp = reinterpret_cast<const float4*>(a.gq + e0);
+        float gv[16];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float4 f = __ldcs(gp + k);
+            gv[4 * k] = f.x;
+            gv[4 * k + 1] = f.y;
+            gv[4 * k + 2] = f.z;
+            gv[4 * k + 3] = f.w;
+        }
+        int8_t* qb = reinterpret_cast<int8_t*>(&qv);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) qb[j] = sr4_one(a, qb[j], gv[j], s, e0 + j);
+        *reinterpret_cast<int4*>(a.q + e0) = qv;
+    }
+    const int64_t t = groups * 16 + tid;   // scalar tail
+    if (t < a.n) a.q[t] = sr4_one(a, a.q[t], a.gq[t], s, t);
+}
+
+}  // namespace tern
+
+using namespace tern;
+
+extern "C" size_t tern_sr4_workspace(int64_t numel) {
+    if (numel < 0) return 0;
+    return kAbsumBlocks * sizeof(double) + 16;
+}
+
+extern "C" int tern_sr4_step(int8_t* q, const float* gq, int64_t numel, float inv_bs, float target_step,
+                             uint64_t seed, int64_t idx_base, uint64_t counter, int q_clamp, int use_dither,
+                             float* s_out, void* workspace, size_t ws_bytes, void* stream) {
+    if (numel < 0 || q_clamp < 1 || q_clamp > 127 || idx_base < 0) return TERN_ERR_ARG;
+    if (numel == 0) return TERN_OK;
+    if (!q || !gq || !workspace) return TERN_ERR_ARG;
+    if (!aligned16(q) || !aligned16(gq) || !aligned16(workspace)) return TERN_ERR_ALIGN;
+    if (ws_bytes < tern_sr4_workspace(numel)) return TERN_ERR_WORKSPACE;
+    int num_sms = 0;
+    if (int st = check_device(&num_sms)) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    Sr4Args a;
+    a.q = q;
+    a.gq = gq;
+    a.n = numel;
+    a.inv_bs = inv_bs;
+    a.target = target_step;
+    a.key = mix64(seed ^ (counter * kG));
+    a.idx_base = idx_base;
+    a.clamp = q_clamp;
+    a.dither = use_dither ? 1 : 0;
+    a.partial = static_cast<double*>(workspace);
+    a.s = reinterpret_cast<float*>(static_cast<char*>(workspace) + kAbsumBlocks * sizeof(double));
+    a.s_out = s_out;
+    const int nparts = static_cast<int>(numel < kAbsumBlocks ? numel : kAbsumBlocks);
+    tern_sr4_absum<<<nparts, 256, 0, s>>>(a);
+    TERN_CUDA_TRY(cudaGetLastError());
+    tern_sr4_finalize<<<1, 256, 0, s>>>(a, nparts);
+    TERN_CUDA_TRY(cudaGetLastError());
+    const int64_t want = (numel / 16 + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    const unsigned grid = static_cast<unsigned>(want < 1 ? 1 : (want < cap ? want : cap));
+    tern_sr4_update<<<grid, 256, 0, s>>>(a);
+    TERN_CUDA_TRY(cudaGetLastError());
+    return TERN_OK;
+}

@@ -157,6 +157,28 @@ int tern_linear_bwd_noalloc(const uint16_t* X, const uint16_t* dY, const tern_ti
 int adamw_step(float* w, const float* g, float* m, float* v, int64_t n, int t, float lr, float b1,
                float b2, float eps, float wd, float gmul, int decoupled, void* stream);
 
+/*
+ * SR4 step on one weight's int4 accumulator (page "train_gpu.cu": sr4_dev calls
+ * fc_sr4_scale<<<1,1>>>(gq, numel, inv_bs, target_step, d_s) then
+ * fc_sr4_update(q, gq, numel, inv_bs, d_s, seed, idx_base, counter, q_clamp,
+ * use_dither); the bodies are off the page, so this is the plainest reading of
+ * those arguments):
+ *   s   = target_step / mean_i |gq_i*inv_bs|                 (s = 0 when the mean is 0)
+ *   q_i = clamp(q_i - floor((gq_i*inv_bs)*s + u_i), -q_clamp, q_clamp)
+ * i.e. stochastic rounding of the descent step into the accumulator, with
+ * u_i ~ U[0,1) from splitmix64 keyed by (seed, counter) at global index
+ * idx_base + i (use_dither = 0: u_i = 1/2).  A non-finite step leaves q_i as is.
+ *   q [numel] int8 (device, updated in place), gq [numel] fp32 (device, read).
+ *   s_out: device float receiving s (NULL to skip).
+ *   workspace: device, >= tern_sr4_workspace(numel) bytes, 16-byte aligned.
+ * q and gq 16-byte aligned; numel >= 0; 1 <= q_clamp <= 127; idx_base >= 0.
+ * The sum behind s is reduced in a fixed order (deterministic).
+ */
+size_t tern_sr4_workspace(int64_t numel);
+int tern_sr4_step(int8_t* q, const float* gq, int64_t numel, float inv_bs, float target_step, uint64_t seed,
+                  int64_t idx_base, uint64_t counter, int q_clamp, int use_dither, float* s_out,
+                  void* workspace, size_t ws_bytes, void* stream);
+
 /* Text of a status code (static storage). */
 const char* tern_strerror(int status);
 
