@@ -60,6 +60,8 @@ def _L():
             "or_gq_at": ([vp, vp, flt, i64, vp, vp], None),
             "or_sgrad_at": ([vp, vp, vp, i64, i64, ci, vp, vp, ci], None),
             "or_adamw": ([vp, vp, vp, vp, i64, ci, dbl, dbl, dbl, dbl, dbl, dbl, ci, vp, vp, vp], None),
+            "or_sumsq": ([vp, i64], dbl),
+            "or_clip_factor": ([dbl, dbl], dbl),
             "or_mix64": ([ctypes.c_uint64], ctypes.c_uint64),
             "or_sr4_uniform": ([ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64], flt),
             "or_sr4_scale": ([vp, i64, flt, flt], flt),
@@ -185,6 +187,27 @@ def adamw(w, g, m, v, t, lr, b1, b2, eps, wd, gmul=1.0, decoupled=True):
     _L().or_adamw(_p(w), _p(g), _p(m), _p(v), n, int(t), f32(lr), f32(b1), f32(b2), f32(eps), f32(wd),
                   f32(gmul), 1 if decoupled else 0, _p(wo), _p(mo), _p(vo))
     return wo, mo, vo
+
+
+def sumsq(g) -> float:
+    g = _c(g, np.float32)
+    return float(_L().or_sumsq(_p(g), g.size))
+
+
+def clip_factor(sumsq_total, max_norm) -> float:
+    """-1 to skip the step (non-finite norm), else the gradient multiplier."""
+    return float(_L().or_clip_factor(float(sumsq_total), float(max_norm)))
+
+
+def adamw_clipped(tensors, t, lr, b1, b2, eps, wd, gmul=1.0, max_norm=0.0, decoupled=True):
+    """AdamW over several (w, g, m, v) tensors with the global-norm clip and the
+    non-finite skip: returns (list of (w, m, v) fp64, skipped)."""
+    total = sum(sumsq(g) for _, g, _, _ in tensors)
+    f = clip_factor(total, max_norm)
+    if f < 0:
+        return [tuple(np.asarray(a, np.float64) for a in (w, m, v)) for w, _, m, v in tensors], True
+    gm = float(np.float32(np.float32(gmul) * np.float32(f)))
+    return [adamw(w, g, m, v, t, lr, b1, b2, eps, wd, gm, decoupled) for w, g, m, v in tensors], False
 
 
 # ----------------------------------------------------------------- SR4 (parity unpinned)

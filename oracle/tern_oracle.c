@@ -476,3 +476,28 @@ void or_sr4_update(const int8_t* q, const float* gq, int64_t n, float inv_bs, fl
         q_out[i] = (int8_t)v;
     }
 }
+
+/* ------------------------------------------------------------ gradient norm, clip, skip */
+
+/*
+ * Global gradient L2 over several tensors and the clip / skip rule around AdamW
+ * (page "train_gpu.cu": grad_l2_gpu sums squares over every parameter gradient in
+ * double; page "nvg_train.rs": grad_norm is NaN/inf when a gradient is, and adam
+ * multiplies the gradients by gmul; page "heal_gpu.rs": a non-finite norm skips the
+ * step, otherwise gmul = clip / gn when gn > clip, else 1).
+ *   or_sumsq       sum_i g_i^2 in fp64, ascending i
+ *   or_clip_factor -1 when sqrt(sumsq) is not finite (skip the step); otherwise
+ *                  max_norm / norm when max_norm > 0 and norm > max_norm, else 1
+ */
+double or_sumsq(const float* g, int64_t n) {
+    double s = 0.0;
+    for (int64_t i = 0; i < n; ++i) s += (double)g[i] * (double)g[i];
+    return s;
+}
+
+double or_clip_factor(double sumsq, double max_norm) {
+    double norm = sqrt(sumsq);
+    if (!isfinite(norm)) return -1.0;
+    if (max_norm > 0.0 && norm > max_norm) return max_norm / norm;
+    return 1.0;
+}

@@ -373,3 +373,53 @@ def test_adamw_gmul_scales_the_gradient_only():
     np.testing.assert_allclose(m1, 10 * m2, rtol=1e-12)
     np.testing.assert_allclose(v1, 100 * v2, rtol=1e-12)
     np.testing.assert_allclose(w1, w2, rtol=1e-5)
+
+
+# ----------------------------------------------------------------- gradient norm, clip, skip
+
+def test_sumsq_and_norm():
+    g = np.array([3.0, 4.0], np.float32)
+    assert oracle.sumsq(g) == 25.0
+    assert oracle.clip_factor(25.0, 10.0) == 1.0          # norm 5 under the clip
+    assert oracle.clip_factor(25.0, 2.5) == 0.5           # clipped to norm 2.5
+    assert oracle.clip_factor(25.0, 0.0) == 1.0           # no clipping asked
+    assert oracle.clip_factor(float("inf"), 1.0) == -1.0  # skip
+    assert oracle.clip_factor(float("nan"), 0.0) == -1.0
+
+
+def test_clipped_gradient_has_the_clip_norm():
+    gs = [syn.normal_f32(5, 30 + i, n, 0.0, 1.0) for i, n in enumerate((7, 100, 1000))]
+    total = sum(oracle.sumsq(g) for g in gs)
+    f = oracle.clip_factor(total, 3.0)
+    assert 0 < f < 1
+    clipped = np.sqrt(sum(np.sum((g.astype(np.float64) * f) ** 2) for g in gs))
+    assert abs(clipped - 3.0) < 1e-12
+
+
+def test_clip_leaves_the_first_adam_step_and_scales_the_moments():
+    # t = 1 with |g| >> eps: the step is lr*sign(g) whatever the gradient scale
+    gs = [syn.normal_f32(6, 40 + i, n, 0.0, 1.0) for i, n in enumerate((5, 64))]
+    ws = [syn.normal_f32(6, 50 + i, g.size, 0.0, 0.02) for i, g in enumerate(gs)]
+    zs = [np.zeros_like(g) for g in gs]
+    tensors = [(w, g, z, z) for w, g, z in zip(ws, gs, zs)]
+    hp = dict(lr=1e-3, b1=0.9, b2=0.95, eps=1e-12, wd=0.0)
+    plain, sk = oracle.adamw_clipped(tensors, 1, **hp)
+    clipped, sk2 = oracle.adamw_clipped(tensors, 1, max_norm=0.5, **hp)
+    assert not sk and not sk2
+    f = oracle.clip_factor(sum(oracle.sumsq(g) for g in gs), 0.5)
+    for (w0, m0, v0), (w1, m1, v1) in zip(plain, clipped):
+        np.testing.assert_allclose(w1, w0, rtol=1e-9, atol=1e-11)   # the step is 1e-3 either way
+        np.testing.assert_allclose(m1, m0 * np.float32(f), rtol=1e-6)
+        np.testing.assert_allclose(v1, v0 * np.float32(f) ** 2, rtol=1e-5)
+
+
+def test_non_finite_gradient_skips_every_tensor():
+    g1 = np.array([1.0, np.inf], np.float32)
+    g2 = np.array([0.5], np.float32)
+    w1, w2 = np.array([0.1, 0.2], np.float32), np.array([0.3], np.float32)
+    out, skipped = oracle.adamw_clipped([(w1, g1, np.zeros(2, np.float32), np.zeros(2, np.float32)),
+                                         (w2, g2, np.zeros(1, np.float32), np.zeros(1, np.float32))],
+                                        1, 1e-3, 0.9, 0.95, 1e-8, 0.1)
+    assert skipped
+    np.testing.assert_array_equal(out[0][0], w1)
+    np.testing.assert_array_equal(out[1][0], w2)
