@@ -34,11 +34,13 @@ TERN_ERR_SCRATCH_LIMIT = -7
 TERN_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 TERN_TILE_PACKED, TERN_TILE_T, TERN_TILE_WHI, TERN_TILE_WLO = 0, 1, 2, 3
+TERN_ADAM_MAX_TENSORS = 128
 
 # the C ABI's exported symbols (tests check the library exports every one)
 ABI_SYMBOLS = ("tern_tiles_bytes", "tern_materialize", "tern_linear_fwd", "tern_linear_bwd_workspace",
-               "tern_linear_bwd", "tern_linear_bwd_noalloc", "adamw_step", "tern_sr4_workspace",
-               "tern_sr4_step", "tern_strerror", "tern_device_status")
+               "tern_linear_bwd", "tern_linear_bwd_noalloc", "adamw_step", "tern_grad_sumsq_workspace",
+               "tern_grad_sumsq", "adamw_step_multi", "tern_sr4_workspace", "tern_sr4_step", "tern_strerror",
+               "tern_device_status")
 
 
 class TernError(RuntimeError):
@@ -66,6 +68,10 @@ def _load():
         "tern_linear_bwd": ([vp, vp, tp, vp, vp, vp, vp, vp, sz, i64, i64, i64, vp], ci),
         "tern_linear_bwd_noalloc": ([vp, vp, tp, vp, vp, vp, vp, i64, i64, i64, vp], ci),
         "adamw_step": ([vp, vp, vp, vp, i64, ci, cf, cf, cf, cf, cf, cf, ci, vp], ci),
+        "tern_grad_sumsq_workspace": ([ctypes.POINTER(i64), ci], sz),
+        "tern_grad_sumsq": ([ctypes.POINTER(vp), ctypes.POINTER(i64), ci, vp, vp, sz, vp], ci),
+        "adamw_step_multi": ([ctypes.POINTER(vp)] * 4 + [ctypes.POINTER(i64), ci, vp, cf, cf, cf, cf, ci, vp, cf,
+                                                          vp, vp], ci),
         "tern_sr4_workspace": ([i64], sz),
         "tern_sr4_step": ([vp, vp, i64, cf, cf, ctypes.c_uint64, i64, ctypes.c_uint64, ci, ci, vp, vp, sz, vp], ci),
         "tern_strerror": ([ci], ctypes.c_char_p),
@@ -210,6 +216,52 @@ def adamw_step(w, g, m, v, t, lr, b1, b2, eps, wd, gmul=1.0, decoupled=True, str
                           float(lr), float(b1), float(b2), float(eps), float(wd), float(gmul),
                           1 if decoupled else 0, _stream(stream)),
            "adamw_step")
+
+
+def _ptr_array(ts, dtype, name):
+    arr = (ctypes.c_void_p * len(ts))()
+    for i, t in enumerate(ts):
+        arr[i] = _ptr(t, dtype, None, f"{name}[{i}]")
+    return arr
+
+
+def _n_array(ts):
+    return (ctypes.c_int64 * len(ts))(*[t.numel() for t in ts])
+
+
+def tern_grad_sumsq_workspace(grads) -> int:
+    n = _n_array(grads)
+    return int(lib.tern_grad_sumsq_workspace(n, len(grads)))
+
+
+def tern_grad_sumsq(grads, sumsq, workspace, stream=None):
+    """sumsq (device float64 [1]) = sum of squares of every gradient tensor, fixed order."""
+    n = _n_array(grads)
+    _check(lib.tern_grad_sumsq(_ptr_array(grads, torch.float32, "g"), n, len(grads),
+                               _ptr(sumsq, torch.float64, None, "sumsq"),
+                               _ptr(workspace, workspace.dtype, None, "workspace"),
+                               workspace.numel() * workspace.element_size(), _stream(stream)),
+           "tern_grad_sumsq")
+
+
+def adamw_step_multi(ws, gs, ms, vs, scalars, b1, b2, eps, wd, decoupled=True, sumsq=None, max_norm=0.0,
+                     skipped=None, stream=None):
+    """AdamW over several tensors in one launch; `scalars` is a device float32 [4]
+    tensor {lr, bc1, bc2, gmul}; `sumsq` (device float64 [1]) enables the global-norm
+    clip (max_norm > 0) and the non-finite skip; `skipped` is a device int32 [1]."""
+    k = len(ws)
+    if not (len(gs) == len(ms) == len(vs) == k):
+        raise ValueError("w, g, m, v lists differ in length")
+    for i in range(k):
+        if not (ws[i].numel() == gs[i].numel() == ms[i].numel() == vs[i].numel()):
+            raise ValueError(f"tensor {i}: w, g, m, v sizes differ")
+    _check(lib.adamw_step_multi(_ptr_array(ws, torch.float32, "w"), _ptr_array(gs, torch.float32, "g"),
+                                _ptr_array(ms, torch.float32, "m"), _ptr_array(vs, torch.float32, "v"),
+                                _n_array(ws), k, _ptr(scalars, torch.float32, (4,), "scalars"), float(b1),
+                                float(b2), float(eps), float(wd), 1 if decoupled else 0,
+                                _ptr(sumsq, torch.float64, None, "sumsq"), float(max_norm),
+                                _ptr(skipped, torch.int32, None, "skipped"), _stream(stream)),
+           "adamw_step_multi")
 
 
 def tern_sr4_workspace(numel) -> int:

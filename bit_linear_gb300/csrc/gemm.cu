@@ -522,7 +522,17 @@ GemmArgs make_args(int64_t Mg, int64_t Ng, int64_t Kg) {
 // Persistent launch: one CTA (or CTA pair) per SM (pair of SMs), at most one per tile.
 template <class C, class K, class... Maps>
 int launch(K kernel, const GemmArgs& a, int num_sms, cudaStream_t s, const Maps&... maps) {
-    TERN_CUDA_TRY(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES));
+    // once per kernel and device: later calls, e.g. under stream capture, only
+    // enqueue the launch
+    static std::once_flag once[64];
+    static cudaError_t smem_attr[64];
+    int dev = 0;
+    TERN_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return TERN_ERR_DEVICE;
+    std::call_once(once[dev], [&] {
+        smem_attr[dev] = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    });
+    TERN_CUDA_TRY(smem_attr[dev]);
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[1];
     cfg.blockDim = dim3(kThreads);
@@ -535,14 +545,14 @@ int launch(K kernel, const GemmArgs& a, int num_sms, cudaStream_t s, const Maps&
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        static int max_clusters = 0;   // co-resident CTA pairs of this kernel
-        if (max_clusters == 0) {
+        static int max_clusters[64];   // co-resident CTA pairs of this kernel, per device
+        if (max_clusters[dev] == 0) {
             cfg.gridDim = dim3(2 * (num_sms / 2));
             int n = 0;
             TERN_CUDA_TRY(cudaOccupancyMaxActiveClusters(&n, kernel, &cfg));
-            max_clusters = n > 0 ? n : 1;
+            max_clusters[dev] = n > 0 ? n : 1;
         }
-        cfg.gridDim = dim3(2 * std::min(a.num_tiles, max_clusters));
+        cfg.gridDim = dim3(2 * std::min(a.num_tiles, max_clusters[dev]));
     } else {
         cfg.attrs = nullptr;
         cfg.numAttrs = 0;

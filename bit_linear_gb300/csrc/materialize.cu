@@ -154,7 +154,7 @@ namespace {
 template <bool QC, bool PK, bool TT, bool HL>
 int launch_materialize(const MatArgs& a, int num_sms, cudaStream_t s) {
     auto kernel = tern_materialize_kernel<QC, PK, TT, HL>;
-    static int per_sm = 0;   // resident CTAs per SM (the grid strides over the rest)
+    static int per_sm = 0;   // resident CTAs per SM (the grid strides over the rest); same on every GB300
     if (per_sm == 0) {
         int b = 0;
         TERN_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, 256, 0));

@@ -158,6 +158,44 @@ int adamw_step(float* w, const float* g, float* m, float* v, int64_t n, int t, f
                float b2, float eps, float wd, float gmul, int decoupled, void* stream);
 
 /*
+ * Per-step AdamW scalars kept in device memory (page "train_gpu.cu", opt#3: the
+ * captured training step reads {lr, bc1, bc2, scale_lr/lr} from a device buffer
+ * so that a replayed CUDA graph sees fresh values).  bc_i = 1 - beta_i^t; gmul
+ * multiplies the gradient.  The caller writes them before each step.
+ */
+typedef struct tern_adam_scalars {
+    float lr, bc1, bc2, gmul;
+} tern_adam_scalars;
+
+#define TERN_ADAM_MAX_TENSORS 128
+
+/*
+ * Global gradient sum of squares over several tensors, fp64, in a fixed order
+ * (page "train_gpu.cu": grad_l2_gpu; page "nvg_train.rs": grad_norm).
+ *   g[t], n[t]: host arrays of ntensors (1..TERN_ADAM_MAX_TENSORS) device pointers
+ *   and element counts; sumsq: device double, written.
+ *   workspace: device, >= tern_grad_sumsq_workspace(n, ntensors) bytes, 16-byte aligned.
+ */
+size_t tern_grad_sumsq_workspace(const int64_t* n, int ntensors);
+int tern_grad_sumsq(const float* const* g, const int64_t* n, int ntensors, double* sumsq, void* workspace,
+                    size_t ws_bytes, void* stream);
+
+/*
+ * AdamW (same update as adamw_step) over ntensors tensors in one launch, reading
+ * lr, bc1, bc2 and gmul from `scalars` in device memory.  When sumsq (device,
+ * from tern_grad_sumsq) is given: a non-finite norm sqrt(sumsq) skips the whole
+ * step (nothing is written); a norm above max_norm > 0 multiplies every gradient
+ * by max_norm / norm (page "heal_gpu.rs": skip non-finite steps, gmul = clip / gn;
+ * page "nvg_train.rs": adam's gmul).  skipped (device int, may be NULL) receives
+ * 1 for a skipped step, else 0.
+ *   w, g, m, v, n: host arrays of device pointers / element counts; every tensor
+ *   16-byte aligned; 1 <= ntensors <= TERN_ADAM_MAX_TENSORS.
+ */
+int adamw_step_multi(float* const* w, const float* const* g, float* const* m, float* const* v, const int64_t* n,
+                     int ntensors, const tern_adam_scalars* scalars, float b1, float b2, float eps, float wd,
+                     int decoupled, const double* sumsq, float max_norm, int* skipped, void* stream);
+
+/*
  * SR4 step on one weight's int4 accumulator (page "train_gpu.cu": sr4_dev calls
  * fc_sr4_scale<<<1,1>>>(gq, numel, inv_bs, target_step, d_s) then
  * fc_sr4_update(q, gq, numel, inv_bs, d_s, seed, idx_base, counter, q_clamp,

@@ -203,7 +203,7 @@ def adamw_clipped(tensors, t, lr, b1, b2, eps, wd, gmul=1.0, max_norm=0.0, decou
     """AdamW over several (w, g, m, v) tensors with the global-norm clip and the
     non-finite skip: returns (list of (w, m, v) fp64, skipped)."""
     total = sum(sumsq(g) for _, g, _, _ in tensors)
-    f = clip_factor(total, max_norm)
+    f = clip_factor(total, float(np.float32(max_norm)))
     if f < 0:
         return [tuple(np.asarray(a, np.float64) for a in (w, m, v)) for w, _, m, v in tensors], True
     gm = float(np.float32(np.float32(gmul) * np.float32(f)))
