@@ -35,11 +35,12 @@ TERN_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 TERN_TILE_PACKED, TERN_TILE_T, TERN_TILE_WHI, TERN_TILE_WLO = 0, 1, 2, 3
 TERN_ADAM_MAX_TENSORS = 128
+TERN_BWD_ACCUMULATE = 1
 
 # the C ABI's exported symbols (tests check the library exports every one)
 ABI_SYMBOLS = ("tern_tiles_bytes", "tern_materialize", "tern_linear_fwd", "tern_linear_bwd_workspace",
-               "tern_linear_bwd", "tern_linear_bwd_noalloc", "adamw_step", "tern_grad_sumsq_workspace",
-               "tern_grad_sumsq", "adamw_step_multi", "tern_sr4_workspace", "tern_sr4_step", "tern_strerror",
+               "tern_linear_bwd", "tern_linear_bwd_ex", "tern_linear_bwd_noalloc", "adamw_step", "tern_grad_sumsq_workspace",
+               "tern_grad_sumsq", "adamw_step_multi", "tern_sr4_workspace", "tern_sr4_step", "tern_sr4_panel", "tern_strerror",
                "tern_device_status")
 
 
@@ -66,6 +67,7 @@ def _load():
         "tern_linear_fwd": ([vp, tp, vp, vp, i64, i64, i64, vp], ci),
         "tern_linear_bwd_workspace": ([i64, i64, i64], sz),
         "tern_linear_bwd": ([vp, vp, tp, vp, vp, vp, vp, vp, sz, i64, i64, i64, vp], ci),
+        "tern_linear_bwd_ex": ([vp, vp, tp, vp, vp, vp, vp, vp, sz, i64, i64, i64, ctypes.c_uint, vp], ci),
         "tern_linear_bwd_noalloc": ([vp, vp, tp, vp, vp, vp, vp, i64, i64, i64, vp], ci),
         "adamw_step": ([vp, vp, vp, vp, i64, ci, cf, cf, cf, cf, cf, cf, ci, vp], ci),
         "tern_grad_sumsq_workspace": ([ctypes.POINTER(i64), ci], sz),
@@ -74,6 +76,7 @@ def _load():
                                                           vp, vp], ci),
         "tern_sr4_workspace": ([i64], sz),
         "tern_sr4_step": ([vp, vp, i64, cf, cf, ctypes.c_uint64, i64, ctypes.c_uint64, ci, ci, vp, vp, sz, vp], ci),
+        "tern_sr4_panel": ([vp, vp, vp, i64, i64, ci, ci, vp, vp, vp], ci),
         "tern_strerror": ([ci], ctypes.c_char_p),
         "tern_device_status": ([vp, ci], ci),
     }
@@ -178,18 +181,21 @@ def tern_linear_bwd_workspace(M, K, N) -> int:
     return int(lib.tern_linear_bwd_workspace(int(M), int(K), int(N)))
 
 
-def tern_linear_bwd(X, dY, tiles: Tiles, scale, dX, gq, sgrad, workspace, stream=None):
+def tern_linear_bwd(X, dY, tiles: Tiles, scale, dX, gq, sgrad, workspace, stream=None, accumulate=False):
+    """accumulate=True calls tern_linear_bwd_ex with TERN_BWD_ACCUMULATE (gq, sgrad +=)."""
     M, K = X.shape
     N = tiles.N
     ct = tiles._c()
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     ws_ptr = None if workspace is None else _ptr(workspace, workspace.dtype, None, "workspace")
-    _check(lib.tern_linear_bwd(_ptr(X, torch.bfloat16, (M, K), "X"), _ptr(dY, torch.bfloat16, (M, N), "dY"),
-                               ctypes.byref(ct), _ptr(scale, torch.float32, (N,), "scale"),
-                               _ptr(dX, torch.float32, (M, K), "dX"), _ptr(gq, torch.float32, (K, N), "gq"),
-                               _ptr(sgrad, torch.float32, (N,), "sgrad"), ws_ptr, ws_bytes, M, K, N,
-                               _stream(stream)),
-           "tern_linear_bwd")
+    args = (_ptr(X, torch.bfloat16, (M, K), "X"), _ptr(dY, torch.bfloat16, (M, N), "dY"), ctypes.byref(ct),
+            _ptr(scale, torch.float32, (N,), "scale"), _ptr(dX, torch.float32, (M, K), "dX"),
+            _ptr(gq, torch.float32, (K, N), "gq"), _ptr(sgrad, torch.float32, (N,), "sgrad"), ws_ptr, ws_bytes,
+            M, K, N)
+    if accumulate:
+        _check(lib.tern_linear_bwd_ex(*args, TERN_BWD_ACCUMULATE, _stream(stream)), "tern_linear_bwd_ex")
+    else:
+        _check(lib.tern_linear_bwd(*args, _stream(stream)), "tern_linear_bwd")
 
 
 def tern_linear_bwd_noalloc(X, dY, tiles: Tiles, scale, dX, gq, sgrad, stream=None):
@@ -280,6 +286,17 @@ def tern_sr4_step(q, gq, workspace, inv_bs=1.0, target_step=0.003, seed=42, idx_
                              _ptr(workspace, workspace.dtype, None, "workspace"),
                              workspace.numel() * workspace.element_size(), _stream(stream)),
            "tern_sr4_step")
+
+
+def tern_sr4_panel(q, scale, counts, scale_stats, packed_prev=None, theta=2, q_clamp=7, stream=None):
+    """counts: device int64 [6] (neg, zero, pos, rail, dead, churn); scale_stats: device float64 [3]."""
+    K, N = q.shape
+    _check(lib.tern_sr4_panel(_ptr(q, torch.int8, (K, N), "q"),
+                              _ptr(packed_prev, torch.int32, (K, N // 16), "packed_prev"),
+                              _ptr(scale, torch.float32, (N,), "scale"), K, N, int(theta), int(q_clamp),
+                              _ptr(counts, torch.int64, (6,), "counts"),
+                              _ptr(scale_stats, torch.float64, (3,), "scale_stats"), _stream(stream)),
+           "tern_sr4_panel")
 
 
 def tern_device_status(stream=None, clear=True) -> int:

@@ -56,6 +56,7 @@ struct GemmArgs {
     const float* scale;       // [Ng] column scale (EPI_FWD, EPI_DW)
     const uint32_t* packed;   // [Mg][Ng/16] 2-bit ternary codes (EPI_DW)
     float* partial;           // [ceil(Mg/128)*4][Ng] per-lane-quarter sgrad partials (EPI_DW)
+    int accumulate;           // EPI_DW: gq += G*scale instead of gq = G*scale
 };
 
 // CG CTAs (1, or a 2-CTA cluster) share one MMA of M = 128*CG rows by N = BN columns.
@@ -195,6 +196,15 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const uint32_t
                         v.y *= s.y;
                         v.z *= s.z;
                         v.w *= s.w;
+                    }
+                    if constexpr (C::EPI == EPI_DW) {
+                        if (a.accumulate) {   // micro-batch accumulation: add to the stored gq
+                            const float4 old = *reinterpret_cast<const float4*>(o + j);
+                            v.x = old.x + v.x;
+                            v.y = old.y + v.y;
+                            v.z = old.z + v.z;
+                            v.w = old.w + v.w;
+                        }
                     }
                     *reinterpret_cast<float4*>(o + j) = v;
                 }
@@ -452,13 +462,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_body<std::conditional_t<CG == 2, Dw2, Dw1>>(&tmA, &tmB, &tmB, a);
 }
 
-// sgrad[c] = sum over the partial rows in ascending order (deterministic).
-__global__ void tern_sgrad_reduce(const float* __restrict__ partial, int nparts, int N, float* __restrict__ sgrad) {
+// sgrad[c] = sum over the partial rows in ascending order (deterministic); with
+// accumulate, that sum is added to the stored sgrad[c].
+__global__ void tern_sgrad_reduce(const float* __restrict__ partial, int nparts, int N, float* __restrict__ sgrad,
+                                  int accumulate) {
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
     if (c >= N) return;
     float s = 0.0f;
     for (int i = 0; i < nparts; ++i) s += partial[static_cast<int64_t>(i) * N + c];
-    sgrad[c] = s;
+    sgrad[c] = accumulate ? sgrad[c] + s : s;
 }
 
 // ===================================================================== host side
@@ -596,7 +608,7 @@ int run_dx(K kernel, const uint16_t* dY, const uint16_t* whi, const uint16_t* wl
 
 template <class C, class K>
 int run_dw(K kernel, const uint16_t* X, const uint16_t* dY, const float* scale, const uint32_t* packed, float* gq,
-           float* partial, int64_t M, int64_t K_, int64_t N, int num_sms, cudaStream_t s) {
+           float* partial, int accumulate, int64_t M, int64_t K_, int64_t N, int num_sms, cudaStream_t s) {
     CUtensorMap mA, mB;
     if (int st = map_operand<C>(&mA, X, K_, M, C::A_MN, kBM)) return st;
     if (int st = map_operand<C>(&mB, dY, N, M, C::B_MN, C::B_ROWS)) return st;
@@ -605,6 +617,7 @@ int run_dw(K kernel, const uint16_t* X, const uint16_t* dY, const float* scale, 
     a.scale = scale;
     a.packed = packed;
     a.partial = partial;
+    a.accumulate = accumulate;
     return launch<C>(kernel, a, num_sms, s, mA, mB);
 }
 
@@ -643,9 +656,11 @@ extern "C" size_t tern_linear_bwd_workspace(int64_t M, int64_t K, int64_t N) {
     return static_cast<size_t>(tiles_r * 4 * N) * sizeof(float);
 }
 
-extern "C" int tern_linear_bwd(const uint16_t* X, const uint16_t* dY, const tern_tiles* W, const float* scale,
-                               float* dX, float* gq, float* sgrad, void* workspace, size_t ws_bytes, int64_t M,
-                               int64_t K, int64_t N, void* stream) {
+extern "C" int tern_linear_bwd_ex(const uint16_t* X, const uint16_t* dY, const tern_tiles* W, const float* scale,
+                                  float* dX, float* gq, float* sgrad, void* workspace, size_t ws_bytes, int64_t M,
+                                  int64_t K, int64_t N, unsigned flags, void* stream) {
+    if (flags & ~static_cast<unsigned>(TERN_BWD_ACCUMULATE)) return TERN_ERR_ARG;
+    const int accumulate = (flags & TERN_BWD_ACCUMULATE) ? 1 : 0;
     if (!X || !dY || !W || !scale) return TERN_ERR_ARG;
     if (dX && (!W->whi_bf16 || !W->wlo_bf16)) return TERN_ERR_ARG;
     if (sgrad && !W->packed) return TERN_ERR_ARG;
@@ -669,18 +684,25 @@ extern "C" int tern_linear_bwd(const uint16_t* X, const uint16_t* dY, const tern
     }
     if (gq || sgrad) {
         float* partial = sgrad ? static_cast<float*>(workspace) : nullptr;
-        const int st = use_pair(K) ? run_dw<Dw2>(tern_dw_gemm<2>, X, dY, scale, W->packed, gq, partial, M, K, N,
-                                                 num_sms, s)
-                                   : run_dw<Dw1>(tern_dw_gemm<1>, X, dY, scale, W->packed, gq, partial, M, K, N,
-                                                 num_sms, s);
+        const int st = use_pair(K) ? run_dw<Dw2>(tern_dw_gemm<2>, X, dY, scale, W->packed, gq, partial, accumulate,
+                                                 M, K, N, num_sms, s)
+                                   : run_dw<Dw1>(tern_dw_gemm<1>, X, dY, scale, W->packed, gq, partial, accumulate,
+                                                 M, K, N, num_sms, s);
         if (st) return st;
         if (!sgrad) return TERN_OK;
         const int nparts = static_cast<int>((K + kBM - 1) / kBM) * 4;
         tern_sgrad_reduce<<<static_cast<unsigned>((N + 255) / 256), 256, 0, s>>>(partial, nparts,
-                                                                                 static_cast<int>(N), sgrad);
+                                                                                 static_cast<int>(N), sgrad,
+                                                                                 accumulate);
         TERN_CUDA_TRY(cudaGetLastError());
     }
     return TERN_OK;
+}
+
+extern "C" int tern_linear_bwd(const uint16_t* X, const uint16_t* dY, const tern_tiles* W, const float* scale,
+                               float* dX, float* gq, float* sgrad, void* workspace, size_t ws_bytes, int64_t M,
+                               int64_t K, int64_t N, void* stream) {
+    return tern_linear_bwd_ex(X, dY, W, scale, dX, gq, sgrad, workspace, ws_bytes, M, K, N, 0u, stream);
 }
 
 // ===================================================================== backward without a workspace

@@ -169,3 +169,134 @@ extern "C" int tern_sr4_step(int8_t* q, const float* gq, int64_t numel, float in
     TERN_CUDA_TRY(cudaGetLastError());
     return TERN_OK;
 }
+
+// ===================================================================== SR4 health panel
+//
+// Counts over the post-step accumulator of one weight (page "train_gpu.cu",
+// sr4_panel_compute): ternary -1 / 0 / +1, rail (|q| == clamp), dead (|q| <
+// theta) and churn (ternary differs from the previous 2-bit tiles), plus the
+// scale's min / mean / max.  The page copies q and scale to the host and loops
+// there; here one streaming pass over q (and the previous packed tiles) counts
+// with byte-SIMD compares, warp sums and one integer atomic per warp and
+// counter (integer sums, so the result does not depend on the order), and one
+// CTA reduces the scale in a fixed order.
+
+namespace tern {
+namespace {
+
+struct PanelArgs {
+    const int8_t* q;
+    const uint32_t* prev;        // [K*N/16] previous packed tiles, or null
+    const float* scale;
+    int64_t groups;
+    int64_t N;
+    uint32_t th_pos, th_neg, cl;   // theta, -theta, clamp in every byte
+    unsigned long long* counts;  // [6]
+    double* sstats;              // [3]
+};
+
+}  // namespace
+
+__global__ void __launch_bounds__(256) tern_panel_counts(const PanelArgs a) {
+    unsigned long long c[6] = {0, 0, 0, 0, 0, 0};
+    const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t gi = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; gi < a.groups; gi += nth) {
+        const int4 raw = __ldcs(reinterpret_cast<const int4*>(a.q) + gi);
+        const uint32_t w[4] = {static_cast<uint32_t>(raw.x), static_cast<uint32_t>(raw.y),
+                               static_cast<uint32_t>(raw.z), static_cast<uint32_t>(raw.w)};
+        uint32_t code = 0;
+        int npos = 0, nneg = 0, nrail = 0, ndead = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t pos = __vcmpges4(w[k], a.th_pos);
+            const uint32_t neg = __vcmples4(w[k], a.th_neg);
+            const uint32_t mag = __vabs4(w[k]);             // |q| per byte (-128 stays 0x80, i.e. 128)
+            npos += __popc(pos & 0x01010101u);
+            nneg += __popc(neg & 0x01010101u);
+            nrail += __popc(__vcmpeq4(mag, a.cl) & 0x01010101u);
+            ndead += __popc(__vcmpltu4(mag, a.th_pos) & 0x01010101u);
+            uint32_t x = (pos & 0x01010101u) | (neg & 0x03030303u);
+            x = (x | (x >> 6) | (x >> 12) | (x >> 18)) & 0xFFu;
+            code |= x << (8 * k);
+        }
+        c[0] += nneg;
+        c[1] += 16 - npos - nneg;
+        c[2] += npos;
+        c[3] += nrail;
+        c[4] += ndead;
+        if (a.prev) {
+            const uint32_t d = code ^ __ldcs(a.prev + gi);
+            c[5] += __popc((d | (d >> 1)) & 0x55555555u);    // 2-bit fields that differ
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 6; ++k) {
+        unsigned long long v = c[k];
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if ((threadIdx.x & 31) == 0 && v) atomicAdd(a.counts + k, v);
+    }
+}
+
+__global__ void __launch_bounds__(256) tern_panel_scale(const PanelArgs a) {
+    __shared__ double smin[256], smax[256], ssum[256];
+    double mn = 0.0, mx = 0.0, sm = 0.0;
+    bool any = false;
+    for (int64_t c = threadIdx.x; c < a.N; c += blockDim.x) {
+        const double s = a.scale[c];
+        mn = any ? fmin(mn, s) : s;
+        mx = any ? fmax(mx, s) : s;
+        sm += s;
+        any = true;
+    }
+    smin[threadIdx.x] = any ? mn : INFINITY;
+    smax[threadIdx.x] = any ? mx : -INFINITY;
+    ssum[threadIdx.x] = sm;
+    __syncthreads();
+    for (int w = 128; w > 0; w >>= 1) {
+        if (threadIdx.x < w) {
+            smin[threadIdx.x] = fmin(smin[threadIdx.x], smin[threadIdx.x + w]);
+            smax[threadIdx.x] = fmax(smax[threadIdx.x], smax[threadIdx.x + w]);
+            ssum[threadIdx.x] += ssum[threadIdx.x + w];
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        a.sstats[0] = smin[0];
+        a.sstats[1] = ssum[0] / static_cast<double>(a.N);
+        a.sstats[2] = smax[0];
+    }
+}
+
+}  // namespace tern
+
+extern "C" int tern_sr4_panel(const int8_t* q, const uint32_t* packed_prev, const float* scale, int64_t K,
+                              int64_t N, int theta, int q_clamp, unsigned long long* counts, double* scale_stats,
+                              void* stream) {
+    if (!q || !scale || !counts || !scale_stats) return TERN_ERR_ARG;
+    if (K < 1 || N < 16 || K * N >= (1ll << 40) || theta < 1 || q_clamp < theta || q_clamp > 127)
+        return TERN_ERR_ARG;
+    if (N % 16) return TERN_ERR_ALIGN;
+    if (!aligned16(q) || (packed_prev && !aligned16(packed_prev)) || !aligned16(counts)) return TERN_ERR_ALIGN;
+    int num_sms = 0;
+    if (int st = check_device(&num_sms)) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    PanelArgs a;
+    a.q = q;
+    a.prev = packed_prev;
+    a.scale = scale;
+    a.groups = K * N / 16;
+    a.N = N;
+    a.th_pos = static_cast<uint32_t>(static_cast<uint8_t>(theta)) * 0x01010101u;
+    a.th_neg = static_cast<uint32_t>(static_cast<uint8_t>(-theta)) * 0x01010101u;
+    a.cl = static_cast<uint32_t>(static_cast<uint8_t>(q_clamp)) * 0x01010101u;
+    a.counts = counts;
+    a.sstats = scale_stats;
+    TERN_CUDA_TRY(cudaMemsetAsync(counts, 0, 6 * sizeof(unsigned long long), s));
+    const int64_t want = (a.groups + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    tern_panel_counts<<<static_cast<unsigned>(want < cap ? want : cap), 256, 0, s>>>(a);
+    TERN_CUDA_TRY(cudaGetLastError());
+    tern_panel_scale<<<1, 256, 0, s>>>(a);
+    TERN_CUDA_TRY(cudaGetLastError());
+    return TERN_OK;
+}

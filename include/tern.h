@@ -122,6 +122,19 @@ int tern_linear_bwd(const uint16_t* X, const uint16_t* dY, const tern_tiles* W, 
                     int64_t K, int64_t N, void* stream);
 
 /*
+ * tern_linear_bwd with flags.  TERN_BWD_ACCUMULATE adds this call's gq and sgrad
+ * to the values already stored (dX is still overwritten): the gradient of B
+ * micro-batches is the sum of B calls, the first without the flag (page
+ * "train_gpu.cu": the B > 1 path accumulates every gradient over micro-batches
+ * before the optimizer step and scales by 1/B; here the 1/B goes into
+ * tern_sr4_step's inv_bs and AdamW's gmul).  Unknown flag bits: TERN_ERR_ARG.
+ */
+#define TERN_BWD_ACCUMULATE 1u
+int tern_linear_bwd_ex(const uint16_t* X, const uint16_t* dY, const tern_tiles* W, const float* scale,
+                       float* dX, float* gq, float* sgrad, void* workspace, size_t ws_bytes, int64_t M,
+                       int64_t K, int64_t N, unsigned flags, void* stream);
+
+/*
  * tern_linear_bwd for callers that cannot allocate device memory.  The paper
  * has no counterpart of this call; it is a convenience of this library.
  *
@@ -216,6 +229,20 @@ size_t tern_sr4_workspace(int64_t numel);
 int tern_sr4_step(int8_t* q, const float* gq, int64_t numel, float inv_bs, float target_step, uint64_t seed,
                   int64_t idx_base, uint64_t counter, int q_clamp, int use_dither, float* s_out,
                   void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * SR4 health panel of one weight (page "train_gpu.cu", sr4_panel_compute), from
+ * the post-step q [K][N] and scale [N]:
+ *   counts[0..5] = #ternary -1, #ternary 0, #ternary +1, #|q| == q_clamp (rail),
+ *                  #|q| < theta (dead), #ternary differing from packed_prev (churn)
+ *   scale_stats[0..2] = min, mean, max of scale (fp64)
+ *   packed_prev: the previous 2-bit tiles [K][N/16] (from tern_materialize), or
+ *   NULL (churn 0).  counts (device, 6 x u64, 16-byte aligned) is overwritten;
+ *   scale_stats: device, 3 doubles.  Integer counts: the result is exact and
+ *   does not depend on the launch.  Same shape rules as tern_materialize.
+ */
+int tern_sr4_panel(const int8_t* q, const uint32_t* packed_prev, const float* scale, int64_t K, int64_t N,
+                   int theta, int q_clamp, unsigned long long* counts, double* scale_stats, void* stream);
 
 /* Text of a status code (static storage). */
 const char* tern_strerror(int status);

@@ -63,6 +63,7 @@ def _L():
             "or_sumsq": ([vp, i64], dbl),
             "or_clip_factor": ([dbl, dbl], dbl),
             "or_mix64": ([ctypes.c_uint64], ctypes.c_uint64),
+            "or_sr4_panel": ([vp, vp, vp, i64, i64, ci, ci, vp, vp], None),
             "or_sr4_uniform": ([ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64], flt),
             "or_sr4_scale": ([vp, i64, flt, flt], flt),
             "or_sr4_update": ([vp, vp, i64, flt, flt, ctypes.c_uint64, i64, ctypes.c_uint64, ci, ci, vp, vp],
@@ -233,3 +234,14 @@ def sr4_update(q, gq, s, inv_bs=1.0, seed=42, idx_base=0, counter=0, q_clamp=SR4
     _L().or_sr4_update(_p(q), _p(gq), q.size, float(inv_bs), float(s), int(seed), int(idx_base), int(counter),
                        int(q_clamp), 1 if dither else 0, _p(out), _p(y))
     return out, y
+
+
+def sr4_panel(q, scale, q_prev=None, theta=SR4_THETA, q_clamp=SR4_Q_CLAMP):
+    """(counts [neg, zero, pos, rail, dead, churn] uint64, scale [min, mean, max] fp64)."""
+    q = _c(q, np.int8)
+    K, N = q.shape
+    qp = None if q_prev is None else _c(q_prev, np.int8)
+    counts = np.zeros(6, np.uint64)
+    st = np.zeros(3, np.float64)
+    _L().or_sr4_panel(_p(q), _p(qp), _p(_c(scale, np.float32)), K, N, int(theta), int(q_clamp), _p(counts), _p(st))
+    return counts, st

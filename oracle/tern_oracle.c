@@ -501,3 +501,36 @@ double or_clip_factor(double sumsq, double max_norm) {
     if (max_norm > 0.0 && norm > max_norm) return max_norm / norm;
     return 1.0;
 }
+
+/* ------------------------------------------------------------ SR4 health panel */
+
+/*
+ * The SR4 health panel of one weight (page "train_gpu.cu", sr4_panel_compute,
+ * computed from the post-step q and scale):
+ *   counts[0..5] = #ternary -1, #ternary 0, #ternary +1, #|q| == clamp (rail),
+ *                  #|q| < theta (dead), #ternary differing from the previous
+ *                  ternary (churn; 0 when q_prev is NULL)
+ *   sstats[0..2] = min, mean, max of scale over the N columns (mean in fp64).
+ */
+void or_sr4_panel(const int8_t* q, const int8_t* q_prev, const float* scale, int64_t K, int64_t N, int theta,
+                  int clamp, uint64_t* counts, double* sstats) {
+    for (int k = 0; k < 6; ++k) counts[k] = 0;
+    for (int64_t i = 0; i < K * N; ++i) {
+        int w = or_ternary(q[i], theta);
+        int a = q[i] < 0 ? -q[i] : q[i];
+        counts[w + 1] += 1;
+        if (a == clamp) counts[3] += 1;
+        if (a < theta) counts[4] += 1;
+        if (q_prev && or_ternary(q_prev[i], theta) != w) counts[5] += 1;
+    }
+    double mn = 0.0, mx = 0.0, sum = 0.0;
+    for (int64_t c = 0; c < N; ++c) {
+        double s = (double)scale[c];
+        if (c == 0 || s < mn) mn = s;
+        if (c == 0 || s > mx) mx = s;
+        sum += s;
+    }
+    sstats[0] = mn;
+    sstats[1] = N > 0 ? sum / (double)N : 0.0;
+    sstats[2] = mx;
+}

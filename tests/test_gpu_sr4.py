@@ -81,3 +81,26 @@ def test_sr4_zero_gradient_leaves_q(cuda_lib):
     torch.cuda.synchronize()
     np.testing.assert_array_equal(q.cpu().numpy(), q0)
     assert s.item() == 0.0
+
+
+@pytest.mark.parametrize("K,N,theta,clamp", [(64, 48, 2, 7), (1000, 1008, 2, 7), (300, 512, 3, 127)])
+def test_panel_matches_oracle(cuda_lib, K, N, theta, clamp):
+    bl = cuda_lib
+    q_prev = syn.int8_uniform(12, syn.TID_Q, K * N, -128, 127).reshape(K, N)
+    q = syn.int8_uniform(13, syn.TID_Q, K * N, -128, 127).reshape(K, N)
+    q[: K // 2] = q_prev[: K // 2]                     # half the rows unchanged
+    scale = syn.uniform_f32(12, syn.TID_SCALE, N, -0.05, 0.1)
+    prev_tiles = bl.Tiles(K, N, packed=torch.empty((K, N // 16), dtype=torch.int32, device="cuda"))
+    bl.tern_materialize(dev(q_prev), None, prev_tiles, theta, clamp)
+    counts = torch.full((6,), -1, dtype=torch.int64, device="cuda")
+    stats = torch.zeros(3, dtype=torch.float64, device="cuda")
+    bl.tern_sr4_panel(dev(q), dev(scale), counts, stats, packed_prev=prev_tiles.packed, theta=theta, q_clamp=clamp)
+    torch.cuda.synchronize()
+    ref_c, ref_s = oracle.sr4_panel(q, scale, q_prev, theta, clamp)
+    np.testing.assert_array_equal(counts.cpu().numpy().astype(np.uint64), ref_c)
+    got = stats.cpu().numpy()
+    assert got[0] == ref_s[0] and got[2] == ref_s[2]
+    assert abs(got[1] - ref_s[1]) <= 1e-12 * abs(ref_s[1]) + 1e-18
+    bl.tern_sr4_panel(dev(q), dev(scale), counts, stats, theta=theta, q_clamp=clamp)   # no previous tiles
+    torch.cuda.synchronize()
+    assert counts[5].item() == 0

@@ -423,3 +423,16 @@ def test_non_finite_gradient_skips_every_tensor():
     assert skipped
     np.testing.assert_array_equal(out[0][0], w1)
     np.testing.assert_array_equal(out[1][0], w2)
+
+
+def test_g_of_a_concatenated_batch_is_the_sum_over_micro_batches():
+    # the identity behind micro-batch accumulation: G = X^T dY sums over tokens
+    parts = [syn.linear_inputs(m, 24, 32, seed=60 + i) for i, m in enumerate((5, 9, 3))]
+    q, scale = parts[0].q, parts[0].scale
+    X = np.concatenate([p.X for p in parts])
+    dY = np.concatenate([p.dY for p in parts])
+    g, ga, s, sa = oracle.dw(X, dY, q, scale)
+    gsum = sum(oracle.dw(p.X, p.dY, q, scale)[0] for p in parts)
+    ssum = sum(oracle.dw(p.X, p.dY, q, scale)[2] for p in parts)
+    assert np.all(np.abs(gsum - g) <= 1e-12 * ga + 1e-18)
+    assert np.all(np.abs(ssum - s) <= 1e-12 * sa + 1e-18)

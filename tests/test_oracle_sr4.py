@@ -101,3 +101,26 @@ def test_counter_and_seed_change_the_draws_deterministically():
     d, _ = oracle.sr4_update(q, gq, s=1.0, seed=43, counter=1)
     np.testing.assert_array_equal(a, b)
     assert (a != c).mean() > 0.3 and (a != d).mean() > 0.3
+
+
+def test_panel_on_a_hand_built_weight():
+    # one row per accumulator value -7..7, N = 16
+    q = np.repeat(np.arange(-7, 8, dtype=np.int8)[:, None], 16, axis=1)
+    scale = np.linspace(0.5, 2.0, 16).astype(np.float32)
+    counts, st = oracle.sr4_panel(q, scale)
+    # ternary at theta 2: -7..-2 -> -1 (6 rows), -1..1 -> 0 (3 rows), 2..7 -> +1 (6 rows)
+    assert list(counts) == [6 * 16, 3 * 16, 6 * 16, 2 * 16, 3 * 16, 0]
+    assert st[0] == np.float32(0.5) and st[2] == np.float32(2.0)
+    assert abs(st[1] - scale.astype(np.float64).mean()) < 1e-15
+
+
+def test_panel_churn_counts_changed_ternaries():
+    q_prev = syn.int8_uniform(8, syn.TID_Q, 64 * 48, -7, 7).reshape(64, 48)
+    q = q_prev.copy()
+    q[3, 5] = -q[3, 5] if abs(q[3, 5]) >= 2 else 5     # changes the ternary
+    q[10, 0] = 0 if abs(q[10, 0]) >= 2 else -7          # changes the ternary
+    q[20, 7] = q[20, 7] + (1 if q[20, 7] >= 2 and q[20, 7] < 7 else 0)   # same ternary
+    counts, _ = oracle.sr4_panel(q, np.ones(48, np.float32), q_prev)
+    assert counts[5] == 2
+    assert counts[0] + counts[1] + counts[2] == q.size
+    assert counts[4] == counts[1]          # dead (|q| < theta) is ternary zero
