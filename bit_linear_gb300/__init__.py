@@ -38,7 +38,8 @@ TERN_ADAM_MAX_TENSORS = 128
 TERN_BWD_ACCUMULATE = 1
 
 # the C ABI's exported symbols (tests check the library exports every one)
-ABI_SYMBOLS = ("tern_tiles_bytes", "tern_materialize", "tern_linear_fwd", "tern_linear_bwd_workspace",
+ABI_SYMBOLS = ("tern_tiles_bytes", "tern_materialize", "tern_linear_fwd", "tern_linear_bwd_workspace_min",
+               "tern_linear_bwd_workspace",
                "tern_linear_bwd", "tern_linear_bwd_ex", "tern_linear_bwd_noalloc", "adamw_step", "tern_grad_sumsq_workspace",
                "tern_grad_sumsq", "adamw_step_multi", "tern_sr4_workspace", "tern_sr4_step", "tern_sr4_panel", "tern_strerror",
                "tern_device_status")
@@ -65,6 +66,7 @@ def _load():
         "tern_tiles_bytes": ([i64, i64, ci], sz),
         "tern_materialize": ([vp, vp, vp, i64, i64, ci, ci, tp, vp], ci),
         "tern_linear_fwd": ([vp, tp, vp, vp, i64, i64, i64, vp], ci),
+        "tern_linear_bwd_workspace_min": ([i64, i64, i64], sz),
         "tern_linear_bwd_workspace": ([i64, i64, i64], sz),
         "tern_linear_bwd": ([vp, vp, tp, vp, vp, vp, vp, vp, sz, i64, i64, i64, vp], ci),
         "tern_linear_bwd_ex": ([vp, vp, tp, vp, vp, vp, vp, vp, sz, i64, i64, i64, ctypes.c_uint, vp], ci),
@@ -179,6 +181,10 @@ def tern_linear_fwd(X, tiles: Tiles, scale, Y, stream=None):
 
 def tern_linear_bwd_workspace(M, K, N) -> int:
     return int(lib.tern_linear_bwd_workspace(int(M), int(K), int(N)))
+
+
+def tern_linear_bwd_workspace_min(M, K, N) -> int:
+    return int(lib.tern_linear_bwd_workspace_min(int(M), int(K), int(N)))
 
 
 def tern_linear_bwd(X, dY, tiles: Tiles, scale, dX, gq, sgrad, workspace, stream=None, accumulate=False):

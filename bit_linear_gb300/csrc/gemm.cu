@@ -57,6 +57,11 @@ struct GemmArgs {
     const uint32_t* packed;   // [Mg][Ng/16] 2-bit ternary codes (EPI_DW)
     float* partial;           // [ceil(Mg/128)*4][Ng] per-lane-quarter sgrad partials (EPI_DW)
     int accumulate;           // EPI_DW: gq += G*scale instead of gq = G*scale
+    // Work units of this launch: unit u is tile tile_begin + u / split, k-blocks
+    // [(u % split) * kb_per, ...).  With split > 1 (EPI_DW only) each unit writes
+    // its raw partial tile to partial_g[u] and tern_dw_split_reduce finishes it.
+    int tile_begin, num_units, split, kb_per;
+    float* partial_g;
 };
 
 // CG CTAs (1, or a 2-CTA cluster) share one MMA of M = 128*CG rows by N = BN columns.
@@ -129,7 +134,7 @@ __device__ __forceinline__ uint64_t op_desc(uint32_t base, int kk) {
 // Grouped raster: runs of GM m-tiles share an n-tile, so neighbouring CTAs reuse
 // the same B panel and A panels stay resident in L2.
 template <int GM>
-__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int& mt, int& nt) {
+__host__ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int& mt, int& nt) {
     const int group = tile / (GM * tiles_n);
     const int first_m = group * GM;
     const int gm = min(GM, tiles_m - first_m);
@@ -289,12 +294,13 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        for (int tile = unit; ok && tile < a.num_tiles; tile += units) {
+        for (int u = unit; ok && u < a.num_units; u += units) {
             int mt, nt;
-            tile_coords<16 / CG>(tile, a.tiles_m, a.tiles_n, mt, nt);
+            tile_coords<16 / CG>(a.tile_begin + u / a.split, a.tiles_m, a.tiles_n, mt, nt);
             const int arow = mt * C::TILE_M + static_cast<int>(rank) * kBM;
             const int brow = nt * C::BN + static_cast<int>(rank) * C::B_ROWS;
-            for (int kb = 0; kb < a.num_kb; ++kb) {
+            const int kb0 = (u % a.split) * a.kb_per, kb1 = min(a.num_kb, kb0 + a.kb_per);
+            for (int kb = kb0; kb < kb1; ++kb) {
                 if (!wait_bounded(EMPTY0 + 8u * stage, phase ^ 1u, abort_flag, true)) {
                     ok = false;
                     break;
@@ -350,13 +356,14 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
         uint32_t phase = 0;
         bool ok = true;
         int local = 0;
-        for (int tile = unit; ok && tile < a.num_tiles; tile += units, ++local) {
+        for (int u = unit; ok && u < a.num_units; u += units, ++local) {
             const int acc = local & 1;
             const uint32_t acc_parity = (local >> 1) & 1;
             if (!wait_bounded(TEMPTY0 + 8u * acc, acc_parity ^ 1u, abort_flag, true)) break;
             ptx::tc_fence_after();
             const uint32_t d_tmem = tmem_base + acc * C::BN;
-            for (int kb = 0; kb < a.num_kb; ++kb) {
+            const int kb0 = (u % a.split) * a.kb_per, kb1 = min(a.num_kb, kb0 + a.kb_per);
+            for (int kb = kb0; kb < kb1; ++kb) {
                 if (!wait_bounded(FULL0 + 8u * stage, phase, abort_flag, true)) {
                     ok = false;
                     break;
@@ -367,7 +374,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
 #pragma unroll
                 for (int kk = 0; kk < C::BK / 16; ++kk) {
                     const uint64_t da = op_desc<C::A_MN, C::BK>(sA, kk);
-                    mma(d_tmem, da, op_desc<C::B_MN, C::BK>(sB0, kk), (kb | kk) != 0);
+                    mma(d_tmem, da, op_desc<C::B_MN, C::BK>(sB0, kk), (kb != kb0 || kk != 0) ? 1u : 0u);
                     if constexpr (C::NB == 2) mma(d_tmem, da, op_desc<C::B_MN, C::BK>(sB0 + C::B_BYTES, kk), 1u);
                 }
                 commit_all(EMPTY0 + 8u * stage);   // frees the stage once these MMAs are done
@@ -387,18 +394,33 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
         const int quad = warp & 3;   // a warp may touch TMEM lanes 32*(warp%4) .. +31
         const uint32_t tempty_leader = CG == 2 ? ptx::mapa_shared(TEMPTY0, 0) : TEMPTY0;
         int local = 0;
-        for (int tile = unit; tile < a.num_tiles; tile += units, ++local) {
+        for (int u = unit; u < a.num_units; u += units, ++local) {
             const int acc = local & 1;
             const uint32_t acc_parity = (local >> 1) & 1;
             if (!wait_bounded(TFULL0 + 8u * acc, acc_parity, abort_flag, true)) break;
             ptx::tc_fence_after();
             int mt, nt;
-            tile_coords<16 / CG>(tile, a.tiles_m, a.tiles_n, mt, nt);
+            tile_coords<16 / CG>(a.tile_begin + u / a.split, a.tiles_m, a.tiles_n, mt, nt);
             const int row0 = mt * C::TILE_M + static_cast<int>(rank) * kBM;
-            if (row0 < a.Mg) {   // a pair's second half may lie wholly past the last row
+            const uint32_t trow = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * C::BN;
+            if (C::EPI == EPI_DW && a.partial_g != nullptr) {
+                // split unit: the raw partial tile, row-major TILE_M x BN, for the reduce kernel
+                float* pg = a.partial_g + static_cast<int64_t>(u) * C::TILE_M * C::BN +
+                            static_cast<int64_t>(static_cast<int>(rank) * kBM + quad * 32 + lane) * C::BN;
+#pragma unroll 1
+                for (int j = 0; j < C::BN / 32; ++j) {
+                    uint32_t r[32];
+                    ptx::tmem_ld_32x32b_x32(trow + j * 32, r);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        *reinterpret_cast<float4*>(pg + j * 32 + 4 * q) =
+                            make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                        __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+                }
+            } else if (row0 < a.Mg) {   // a pair's second half may lie wholly past the last row
                 const int tile128 = mt * CG + static_cast<int>(rank);
                 const int row = row0 + quad * 32 + lane;
-                const uint32_t trow = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * C::BN;
 #pragma unroll 1
                 for (int j = 0; j < C::BN / 32; ++j) {
                     const int c0 = nt * C::BN + j * 32;
@@ -473,6 +495,44 @@ __global__ void tern_sgrad_reduce(const float* __restrict__ partial, int nparts,
     sgrad[c] = accumulate ? sgrad[c] + s : s;
 }
 
+// Finish the split G tiles: G = sum over the tile's slices in slice order, then
+// the same epilogue as the G kernel (gq = G*scale[c], or += with accumulate,
+// and the sgrad partial of each 32-row group).  One CTA per 32-row group of a
+// tile, one thread per column.
+__global__ void __launch_bounds__(256) tern_dw_split_reduce(const GemmArgs a, int tile_m, int tile_n) {
+    const int groups_per_tile = tile_m / 32;
+    const int j = blockIdx.x / groups_per_tile;           // tail tile
+    const int rg = blockIdx.x % groups_per_tile;          // 32-row group within the tile
+    int tm, tn;
+    if (tile_m == 2 * kBM) tile_coords<8>(a.tile_begin + j, a.tiles_m, a.tiles_n, tm, tn);
+    else tile_coords<16>(a.tile_begin + j, a.tiles_m, a.tiles_n, tm, tn);
+    const int c_in = threadIdx.x;                 // column within the tile (blockDim = tile_n)
+    const int col = tn * tile_n + c_in;
+    const int r_base = tm * tile_m + rg * 32;
+    if (r_base >= a.Mg) return;
+    const bool col_ok = col < a.Ng;
+    float colsum = 0.0f;
+    for (int r = 0; r < 32; ++r) {
+        const int row = r_base + r;
+        float g = 0.0f;
+        for (int sl = 0; sl < a.split; ++sl)
+            g += a.partial_g[(static_cast<int64_t>(j) * a.split + sl) * tile_m * tile_n +
+                             static_cast<int64_t>(rg * 32 + r) * tile_n + c_in];
+        if (row < a.Mg && col_ok) {
+            if (a.out) {
+                float v = g * a.scale[col];
+                float* o = a.out + static_cast<int64_t>(row) * a.Ng + col;
+                *o = a.accumulate ? *o + v : v;
+            }
+            if (a.partial) {
+                const uint32_t code = (a.packed[static_cast<int64_t>(row) * (a.Ng / 16) + col / 16] >> (2 * (col % 16))) & 3u;
+                colsum += (code & 1u) ? ((code & 2u) ? -g : g) : 0.0f;
+            }
+        }
+    }
+    if (a.partial && col_ok) a.partial[static_cast<int64_t>(r_base / 32) * a.Ng + col] = colsum;
+}
+
 // ===================================================================== host side
 
 namespace {
@@ -528,10 +588,15 @@ GemmArgs make_args(int64_t Mg, int64_t Ng, int64_t Kg) {
     a.tiles_n = static_cast<int>((Ng + C::BN - 1) / C::BN);
     a.num_tiles = a.tiles_m * a.tiles_n;
     a.num_kb = static_cast<int>((Kg + C::BK - 1) / C::BK);
+    a.tile_begin = 0;
+    a.num_units = a.num_tiles;
+    a.split = 1;
+    a.kb_per = a.num_kb;
+    a.partial_g = nullptr;
     return a;
 }
 
-// Persistent launch: one CTA (or CTA pair) per SM (pair of SMs), at most one per tile.
+// Persistent launch: one CTA (or CTA pair) per SM (pair of SMs), at most one per work unit.
 template <class C, class K, class... Maps>
 int launch(K kernel, const GemmArgs& a, int num_sms, cudaStream_t s, const Maps&... maps) {
     // once per kernel and device: later calls, e.g. under stream capture, only
@@ -564,11 +629,13 @@ int launch(K kernel, const GemmArgs& a, int num_sms, cudaStream_t s, const Maps&
             TERN_CUDA_TRY(cudaOccupancyMaxActiveClusters(&n, kernel, &cfg));
             max_clusters[dev] = n > 0 ? n : 1;
         }
-        cfg.gridDim = dim3(2 * std::min(a.num_tiles, max_clusters[dev]));
+        if (a.num_tiles < 0) return max_clusters[dev];   // query: persistent units of this kernel
+        cfg.gridDim = dim3(2 * std::min(a.num_units, max_clusters[dev]));
     } else {
+        if (a.num_tiles < 0) return num_sms;
         cfg.attrs = nullptr;
         cfg.numAttrs = 0;
-        cfg.gridDim = dim3(std::min(a.num_tiles, num_sms));
+        cfg.gridDim = dim3(std::min(a.num_units, num_sms));
     }
     TERN_CUDA_TRY(cudaLaunchKernelEx(&cfg, kernel, maps..., a));
     return TERN_OK;
@@ -606,9 +673,24 @@ int run_dx(K kernel, const uint16_t* dY, const uint16_t* whi, const uint16_t* wl
     return launch<C>(kernel, a, num_sms, s, mA, mHi, mLo);
 }
 
+// Largest number of split units the tail of a G launch may use (bounds the workspace).
+constexpr int kMaxTailUnits = 128;
+
+template <class C>
+int64_t dw_tail_bytes(int64_t M, int64_t K_, int64_t N) {
+    const GemmArgs a = make_args<C>(K_, N, M);
+    const int64_t units = std::min<int64_t>(kMaxTailUnits, static_cast<int64_t>(a.num_tiles) * a.num_kb);
+    return units * C::TILE_M * C::BN * static_cast<int64_t>(sizeof(float));
+}
+
+// G = X^T dY with the fused gq / sgrad epilogue.  Whole waves of tiles run as
+// they are; when the last wave would leave units idle and `tail` has room, the
+// remaining tiles are split along the token axis over the idle units and
+// finished by tern_dw_split_reduce.
 template <class C, class K>
 int run_dw(K kernel, const uint16_t* X, const uint16_t* dY, const float* scale, const uint32_t* packed, float* gq,
-           float* partial, int accumulate, int64_t M, int64_t K_, int64_t N, int num_sms, cudaStream_t s) {
+           float* partial, int accumulate, float* tail, int64_t tail_bytes, int64_t M, int64_t K_, int64_t N,
+           int num_sms, cudaStream_t s) {
     CUtensorMap mA, mB;
     if (int st = map_operand<C>(&mA, X, K_, M, C::A_MN, kBM)) return st;
     if (int st = map_operand<C>(&mB, dY, N, M, C::B_MN, C::B_ROWS)) return st;
@@ -618,6 +700,36 @@ int run_dw(K kernel, const uint16_t* X, const uint16_t* dY, const float* scale, 
     a.packed = packed;
     a.partial = partial;
     a.accumulate = accumulate;
+    if (tail) {
+        GemmArgs q = a;
+        q.num_tiles = -1;
+        const int units = launch<C>(kernel, q, num_sms, s, mA, mB);   // persistent units (no launch)
+        const int T = a.num_tiles, T0 = units > 0 ? (T / units) * units : T, R = T - T0;
+        int split = R > 0 ? std::min(units / R, a.num_kb) : 1;
+        if (split >= 2) {
+            const int kb_per = (a.num_kb + split - 1) / split;
+            split = (a.num_kb + kb_per - 1) / kb_per;   // every slice non-empty
+            const int64_t need = static_cast<int64_t>(R) * split * C::TILE_M * C::BN * sizeof(float);
+            if (need <= tail_bytes) {
+                if (T0 > 0) {
+                    GemmArgs m = a;
+                    m.num_units = T0;
+                    if (int st = launch<C>(kernel, m, num_sms, s, mA, mB)) return st;
+                }
+                GemmArgs t = a;
+                t.tile_begin = T0;
+                t.num_units = R * split;
+                t.split = split;
+                t.kb_per = kb_per;
+                t.partial_g = tail;
+                if (int st = launch<C>(kernel, t, num_sms, s, mA, mB)) return st;
+                tern_dw_split_reduce<<<static_cast<unsigned>(R * (C::TILE_M / 32)), C::BN, 0, s>>>(t, C::TILE_M,
+                                                                                                  C::BN);
+                TERN_CUDA_TRY(cudaGetLastError());
+                return TERN_OK;
+            }
+        }
+    }
     return launch<C>(kernel, a, num_sms, s, mA, mB);
 }
 
@@ -650,10 +762,22 @@ extern "C" int tern_linear_fwd(const uint16_t* X, const tern_tiles* W, const flo
     return run_fwd<Fwd1>(tern_fwd_gemm<1>, X, W->t_bf16, scale, Y, M, K, N, num_sms, s);
 }
 
-extern "C" size_t tern_linear_bwd_workspace(int64_t M, int64_t K, int64_t N) {
+// sgrad partials: one row per 32-row group of K, rounded up to 256 bytes.
+static int64_t bwd_partials_bytes(int64_t K, int64_t N) {
+    const int64_t tiles_r = (K + kBM - 1) / kBM;
+    return (tiles_r * 4 * N * static_cast<int64_t>(sizeof(float)) + 255) / 256 * 256;
+}
+
+extern "C" size_t tern_linear_bwd_workspace_min(int64_t M, int64_t K, int64_t N) {
     if (!dims_ok(M, K, N)) return 0;
     const int64_t tiles_r = (K + kBM - 1) / kBM;
     return static_cast<size_t>(tiles_r * 4 * N) * sizeof(float);
+}
+
+extern "C" size_t tern_linear_bwd_workspace(int64_t M, int64_t K, int64_t N) {
+    if (!dims_ok(M, K, N)) return 0;
+    const int64_t tail = use_pair(K) ? dw_tail_bytes<Dw2>(M, K, N) : dw_tail_bytes<Dw1>(M, K, N);
+    return static_cast<size_t>(bwd_partials_bytes(K, N) + tail);
 }
 
 extern "C" int tern_linear_bwd_ex(const uint16_t* X, const uint16_t* dY, const tern_tiles* W, const float* scale,
@@ -671,7 +795,7 @@ extern "C" int tern_linear_bwd_ex(const uint16_t* X, const uint16_t* dY, const t
     if (sgrad && (!aligned16(sgrad) || !aligned16(W->packed) || !aligned16(workspace))) return TERN_ERR_ALIGN;
     if (gq && !aligned16(gq)) return TERN_ERR_ALIGN;
     if (dX && (!aligned16(dX) || !aligned16(W->whi_bf16) || !aligned16(W->wlo_bf16))) return TERN_ERR_ALIGN;
-    if (sgrad && (!workspace || ws_bytes < tern_linear_bwd_workspace(M, K, N))) return TERN_ERR_WORKSPACE;
+    if (sgrad && (!workspace || ws_bytes < tern_linear_bwd_workspace_min(M, K, N))) return TERN_ERR_WORKSPACE;
     int num_sms = 0;
     if (int st = check_device(&num_sms)) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -684,10 +808,18 @@ extern "C" int tern_linear_bwd_ex(const uint16_t* X, const uint16_t* dY, const t
     }
     if (gq || sgrad) {
         float* partial = sgrad ? static_cast<float*>(workspace) : nullptr;
+        // a workspace past the partials (16-byte aligned, 256-byte rounded) holds split G tiles
+        const int64_t pb = sgrad ? bwd_partials_bytes(K, N) : 0;
+        float* tail = nullptr;
+        int64_t tail_bytes = 0;
+        if (workspace && aligned16(workspace) && static_cast<int64_t>(ws_bytes) > pb) {
+            tail = reinterpret_cast<float*>(static_cast<char*>(workspace) + pb);
+            tail_bytes = static_cast<int64_t>(ws_bytes) - pb;
+        }
         const int st = use_pair(K) ? run_dw<Dw2>(tern_dw_gemm<2>, X, dY, scale, W->packed, gq, partial, accumulate,
-                                                 M, K, N, num_sms, s)
+                                                 tail, tail_bytes, M, K, N, num_sms, s)
                                    : run_dw<Dw1>(tern_dw_gemm<1>, X, dY, scale, W->packed, gq, partial, accumulate,
-                                                 M, K, N, num_sms, s);
+                                                 tail, tail_bytes, M, K, N, num_sms, s);
         if (st) return st;
         if (!sgrad) return TERN_OK;
         const int nparts = static_cast<int>((K + kBM - 1) / kBM) * 4;
@@ -757,7 +889,7 @@ int noalloc_scratch(void** out) {
 extern "C" int tern_linear_bwd_noalloc(const uint16_t* X, const uint16_t* dY, const tern_tiles* W,
                                        const float* scale, float* dX, float* gq, float* sgrad, int64_t M,
                                        int64_t K, int64_t N, void* stream) {
-    if (sgrad && tern_linear_bwd_workspace(M, K, N) > TERN_NOALLOC_SCRATCH_BYTES) return TERN_ERR_SCRATCH_LIMIT;
+    if (sgrad && tern_linear_bwd_workspace_min(M, K, N) > TERN_NOALLOC_SCRATCH_BYTES) return TERN_ERR_SCRATCH_LIMIT;
     void* scratch = nullptr;
     if (int st = noalloc_scratch(&scratch)) return st;
     return tern_linear_bwd(X, dY, W, scale, dX, gq, sgrad, scratch, TERN_NOALLOC_SCRATCH_BYTES, M, K, N, stream);

@@ -96,7 +96,17 @@ int tern_materialize(const int8_t* q, int8_t* q_clamped, const float* scale, int
 int tern_linear_fwd(const uint16_t* X, const tern_tiles* W, const float* scale, float* Y, int64_t M,
                     int64_t K, int64_t N, void* stream);
 
-/* Bytes of device workspace tern_linear_bwd needs for sgrad's per-tile partials. */
+/*
+ * Device workspace of tern_linear_bwd, in bytes.
+ *   tern_linear_bwd_workspace_min: the sgrad partials, the least a call computing
+ *     sgrad accepts (ceil(K/128)*4*N floats).
+ *   tern_linear_bwd_workspace: the partials plus room for the split tail of the G
+ *     GEMM (at most 128 partial tiles of 256 x 256 fp32): when the last wave of G
+ *     tiles would leave SMs idle, or a small K x N has too few tiles, the
+ *     remaining tiles are split along the token axis and reduced in a fixed
+ *     order.  A workspace between the two sizes runs without the split.
+ */
+size_t tern_linear_bwd_workspace_min(int64_t M, int64_t K, int64_t N);
 size_t tern_linear_bwd_workspace(int64_t M, int64_t K, int64_t N);
 
 /*
@@ -112,9 +122,9 @@ size_t tern_linear_bwd_workspace(int64_t M, int64_t K, int64_t N);
  * At least one of dX, gq, sgrad must be given; with gq and sgrad both NULL the
  * G GEMM is not run, with dX NULL the dX GEMM is not run.
  *   X [M][K] bf16, dY [M][N] bf16, scale [N] fp32: device, read.
- *   workspace: device, >= tern_linear_bwd_workspace(M,K,N) bytes when sgrad is
- *   requested (else unused, may be NULL), 16-byte aligned, contents ignored and
- *   overwritten.
+ *   workspace: device, 16-byte aligned, contents ignored and overwritten; at least
+ *   tern_linear_bwd_workspace_min(M,K,N) bytes when sgrad is requested (else may
+ *   be NULL); tern_linear_bwd_workspace(M,K,N) bytes enable the split G tail.
  * Same shape rules as the forward.
  */
 int tern_linear_bwd(const uint16_t* X, const uint16_t* dY, const tern_tiles* W, const float* scale,
@@ -144,7 +154,7 @@ int tern_linear_bwd_ex(const uint16_t* X, const uint16_t* dY, const tern_tiles* 
  * device-wide synchronisation), so they cannot provide one.  This entry point
  * keeps the sgrad partials in a fixed array inside the library's device image
  * instead; it allocates nothing.
- *   Limit: tern_linear_bwd_workspace(M, K, N) <= TERN_NOALLOC_SCRATCH_BYTES
+ *   Limit: tern_linear_bwd_workspace_min(M, K, N) <= TERN_NOALLOC_SCRATCH_BYTES
  *   (8 MiB: ceil(K/128)*4*N <= 2^21, e.g. K = 4096 with N <= 16384) when sgrad
  *   is requested, else TERN_ERR_SCRATCH_LIMIT and nothing is enqueued.
  *   Every GPU that loads the library holds the 8 MiB until the process exits.

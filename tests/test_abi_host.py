@@ -47,8 +47,13 @@ def test_sizes(lib):
     assert lib.tern_tiles_bytes(4096, 12288, lib.TERN_TILE_T) == 4096 * 12288 * 2
     assert lib.tern_tiles_bytes(7, 24, lib.TERN_TILE_T) == 0           # N not a multiple of 16
     assert lib.tern_tiles_bytes(7, 32, 9) == 0
-    assert lib.tern_linear_bwd_workspace(32768, 4096, 12288) == 32 * 4 * 12288 * 4
-    assert lib.tern_linear_bwd_workspace(64, 129, 16) == 2 * 4 * 16 * 4
+    assert lib.tern_linear_bwd_workspace_min(32768, 4096, 12288) == 32 * 4 * 12288 * 4
+    assert lib.tern_linear_bwd_workspace_min(64, 129, 16) == 2 * 4 * 16 * 4
+    assert lib.tern_linear_bwd_workspace_min(0, 16, 16) == 0
+    # plus at most 128 split tiles of 256 x 256 fp32 (pairs) for the G tail
+    assert lib.tern_linear_bwd_workspace(32768, 4096, 12288) == 32 * 4 * 12288 * 4 + 128 * 256 * 256 * 4
+    # K <= 128: single-CTA tiles (128 x 256), 1 tile x 1 k-block -> one split tile at most
+    assert lib.tern_linear_bwd_workspace(64, 128, 16) == 256 * (-(-(1 * 4 * 16 * 4) // 256)) + 128 * 256 * 4
     assert lib.tern_linear_bwd_workspace(0, 16, 16) == 0
 
 
@@ -78,7 +83,7 @@ def test_backward_argument_checks(lib):
     t = _tiles(lib)
     args = lambda dX, ws, n: (P(0x20000), P(0x21000), ctypes.byref(t), P(0x30000), dX, P(0x50000),  # noqa
                               P(0x60000), ws, n, 64, 128, 128, None)
-    need = lib.tern_linear_bwd_workspace(64, 128, 128)
+    need = lib.tern_linear_bwd_workspace_min(64, 128, 128)
     assert f(*args(P(0x40000), P(0x70000), need - 4)) == lib.TERN_ERR_WORKSPACE
     assert f(*args(P(0x40000), None, need)) == lib.TERN_ERR_WORKSPACE
     nohl = lib._Tiles(P(0x10000), P(0x11000), None, None)           # dX asked without W_hi/W_lo
