@@ -228,6 +228,67 @@ def traffic_from_profiles(kernel, src_files):
     return None
 
 
+def rwkv_block(bl, dev, stream, steps):
+    import torch
+    M = 8192
+    shapes = syn.RWKV_SHAPES
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    layers = []
+    for i, (K, N) in enumerate(shapes):
+        inp = syn.linear_inputs(M, K, N, seed=1, scale_lo=0.01, scale_hi=0.1,
+                                tids=(10 * i + 1, 10 * i + 2, 10 * i + 3, 10 * i + 4))
+        L = dict(K=K, N=N, X=bf(inp.X), dY=bf(inp.dY), q=torch.from_numpy(inp.q).to(dev),
+                 scale=torch.from_numpy(inp.scale).to(dev), tiles=bl.Tiles.empty(K, N, device=dev),
+                 Y=torch.empty(M, N, device=dev), dX=torch.empty(M, K, device=dev),
+                 gq=torch.empty(K, N, device=dev), sgrad=torch.empty(N, device=dev),
+                 ws=bl.workspace_for(M, K, N, device=dev), m=torch.zeros(N, device=dev),
+                 v=torch.zeros(N, device=dev))
+        layers.append(L)
+
+    def block():
+        for L in layers:
+            bl.tern_materialize(L["q"], L["scale"], L["tiles"], 2, 7)
+            bl.tern_linear_fwd(L["X"], L["tiles"], L["scale"], L["Y"])
+            bl.tern_linear_bwd(L["X"], L["dY"], L["tiles"], L["scale"], L["dX"], L["gq"], L["sgrad"], L["ws"])
+            bl.adamw_step(L["scale"], L["sgrad"], L["m"], L["v"], 1, **ADAM_HP)
+
+    flops = 6.0 * M * sum(K * N for K, N in shapes)
+    reps = max(20, min(steps, 200))
+    for _ in range(5):
+        block()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(reps):
+        block()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    eager_ms = e0.elapsed_time(e1) / reps
+    g = torch.cuda.CUDAGraph()
+    s2 = torch.cuda.Stream()
+    s2.wait_stream(stream)
+    with torch.cuda.graph(g, stream=s2):
+        block()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    graph_ms = e0.elapsed_time(e1) / reps
+    launches = sum(1 + 1 + 4 + 1 for _ in shapes)   # materialise, fwd, dX + G (+ split reduce) + sgrad, AdamW
+    return {"M": M, "shapes": [list(x) for x in shapes], "flops_per_step": flops,
+            "eager": {"ms": eager_ms, "tflops": flops / (eager_ms * 1e-3) / 1e12},
+            "graph": {"ms": graph_ms, "tflops": flops / (graph_ms * 1e-3) / 1e12},
+            "launches_per_step_approx": launches}
+
+
 def run_ours(args):
     import torch
 
@@ -381,6 +442,11 @@ def run_ours(args):
         extra["ternarise_sweep"] = sweep
         torch.cuda.empty_cache()
         Y = torch.empty(M, N, device=dev)
+
+    # ---- the RWKV-style block (M = 8192 tokens; 4 x 512x512, 512x2048, 2048x512):
+    #      the same step over its six projections, eager and replayed as one CUDA graph
+    if not args.skip_bandwidth and args.workload == "large_single_projection":
+        extra["rwkv_block"] = rwkv_block(bl, dev, stream, args.steps)
 
     # ---- end to end through the C ABI: every step's inputs X and dY copied from
     #      pinned host memory and the step's result (updated scales and their

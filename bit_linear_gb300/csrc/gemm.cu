@@ -509,7 +509,9 @@ __global__ void __launch_bounds__(256) tern_dw_split_reduce(const GemmArgs a, in
     const int c_in = threadIdx.x;                 // column within the tile (blockDim = tile_n)
     const int col = tn * tile_n + c_in;
     const int r_base = tm * tile_m + rg * 32;
-    if (r_base >= a.Mg) return;
+    // partial rows exist for every 32-row group of the 128-row blocks that hold rows;
+    // a group wholly past the last row still writes its (zero) partial
+    if (r_base >= ((a.Mg + kBM - 1) / kBM) * kBM) return;
     const bool col_ok = col < a.Ng;
     float colsum = 0.0f;
     for (int r = 0; r < 32; ++r) {
