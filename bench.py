@@ -67,6 +67,22 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(value, device=None):
+    """The largest `value` over all ranks (the slowest replica sets the job time)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_step, ms_per_step_max, world_size):
+    """Whole-job TFLOP/s: every replica's work over the slowest replica's time."""
+    return flops_per_step * world_size / (ms_per_step_max * 1e-3) / 1e12
+
+
 # --------------------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -372,13 +388,10 @@ def run_ours(args):
         raise RuntimeError(f"device status: {bl.strerror(st)}")
     total_ms = evs[0][0].elapsed_time(evs[-1][5])
     per = {n: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j, n in enumerate(names)}
-    if ws > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dev)
     ms_step = total_ms / args.steps
     flops = 6.0 * M * K * N
-    value = flops * ws / (ms_step * 1e-3) / 1e12
+    value = job_throughput(flops, ms_step, ws)
 
     # kernel rooflines: credited flops per launch / average launch time
     credited = {"fwd": 2.0 * M * K * N, "dx": 2.0 * M * K * N, "dw": 2.0 * M * K * N}

@@ -1,0 +1,60 @@
+"""bench.py's multi-rank plumbing on CPU: two gloo ranks, the job time is the
+slowest rank's, the job throughput counts every rank's work, and the
+reference arm runs on rank 0 only."""
+import os
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _worker(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    sys.path.insert(0, ROOT)
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ms = bench.max_over_ranks(3.0 + 2.0 * rank)
+        q.put((rank, ms, bench.job_throughput(6e12, ms, world)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 29500 + os.getpid() % 1000
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    out = sorted(q.get(timeout=5) for _ in range(2))
+    assert [o[1] for o in out] == [5.0, 5.0]             # both ranks see the slowest rank's time
+    assert abs(out[0][2] - 6e12 * 2 / 5e-3 / 1e12) < 1e-9  # whole-job TFLOP/s
+
+
+def test_single_process_max_is_identity():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(7.5) == 7.5
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    env = dict(os.environ, WORLD_SIZE="2", RANK="1", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+                        "--steps", "1", "--warmup", "3"], env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0
+    assert r.stdout.strip() == ""
+
+
+@pytest.mark.parametrize("bad", [["--warmup", "2"]])
+def test_bench_rejects_too_few_warmups(bad):
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", *bad],
+                       capture_output=True, text=True, timeout=60)
+    assert r.returncode != 0
