@@ -47,6 +47,8 @@ WORKLOADS = {
     # the large projection's weight with a quarter of its tokens: a profiling case whose
     # operands still exceed L2 (dY 201 MB) while the device holds under 1 GB
     "profile_quarter_tokens": dict(M=8192, K=4096, N=12288, scale_lo=0.005, scale_hi=0.05, zero_prob=0.0),
+    # not a layer: the HBM-bound kernels alone (AdamW, ternarise, materialise, SR4, panel)
+    "hbm_kernels": None,
 }
 ADAM_HP = dict(lr=1e-3, b1=0.9, b2=0.95, eps=1e-8, wd=0.1)
 
@@ -305,6 +307,59 @@ def rwkv_block(bl, dev, stream, steps):
             "launches_per_step_approx": launches}
 
 
+def hbm_kernels(args):
+    """The HBM-bound kernels alone at profiling sizes (each input over L2, a few GB in
+    all): AdamW on 1e8 elements, packed ternarisation of 1e9 weights, the full
+    materialise, the SR4 step and the panel of the large projection's weight.
+    Prints one line of GB/s per kernel; a case for ncu, not a bench line."""
+    import torch
+    torch.cuda.set_device(0)
+    import __graft_entry__
+    __graft_entry__._builder().build()
+    import bit_linear_gb300 as bl
+    dev = torch.device("cuda")
+    pk = peaks()
+    stream = torch.cuda.current_stream()
+
+    def loop(fn, nbytes, reps):
+        for _ in range(args.warmup):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        return {"ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9, "frac": nbytes / (ms * 1e-3) / 1e9 / pk["hbm"]}
+
+    out = {}
+    n = 100_000_000
+    w, g = torch.empty(n, device=dev).normal_(0, 0.02), torch.empty(n, device=dev).normal_(0, 1e-3)
+    m, v = torch.zeros(n, device=dev), torch.zeros(n, device=dev)
+    out["adamw_1e8"] = loop(lambda: bl.adamw_step(w, g, m, v, 1, **ADAM_HP), 28 * n, args.steps)
+    del w, g, m, v
+    Kt, Nt = 65536, 15264
+    qt = torch.randint(-7, 8, (Kt, Nt), dtype=torch.int8, device=dev)
+    tt = bl.Tiles(Kt, Nt, packed=torch.empty((Kt, Nt // 16), dtype=torch.int32, device=dev))
+    out["ternarise_1e9"] = loop(lambda: bl.tern_materialize(qt, None, tt, 2, 7), 1.25 * Kt * Nt, args.steps)
+    del qt, tt
+    K, N = 4096, 12288
+    q = torch.randint(-7, 8, (K, N), dtype=torch.int8, device=dev)
+    scale = torch.empty(N, device=dev).uniform_(0.005, 0.05)
+    tiles = bl.Tiles.empty(K, N)
+    out["materialise_all_planes"] = loop(lambda: bl.tern_materialize(q, scale, tiles, 2, 7), 7.25 * K * N, args.steps)
+    gq = torch.empty(K, N, device=dev).normal_(0, 1e-3)
+    ws = torch.empty(bl.tern_sr4_workspace(K * N) // 4 + 4, device=dev)
+    out["sr4_step"] = loop(lambda: bl.tern_sr4_step(q, gq, ws, target_step=0.003), 10.0 * K * N, args.steps)
+    counts = torch.zeros(6, dtype=torch.int64, device=dev)
+    stats = torch.zeros(3, dtype=torch.float64, device=dev)
+    out["sr4_panel"] = loop(lambda: bl.tern_sr4_panel(q, scale, counts, stats, packed_prev=tiles.packed),
+                            1.25 * K * N, args.steps)
+    print(json.dumps({"hbm_kernels": out, "peak_hbm_gbs": pk["hbm"]}), flush=True)
+    return 0
+
+
 def run_ours(args):
     import torch
 
@@ -547,6 +602,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.workload == "hbm_kernels":
+        return hbm_kernels(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

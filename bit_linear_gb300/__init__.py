@@ -42,7 +42,7 @@ ABI_SYMBOLS = ("tern_tiles_bytes", "tern_materialize", "tern_linear_fwd", "tern_
                "tern_linear_bwd_workspace",
                "tern_linear_bwd", "tern_linear_bwd_ex", "tern_linear_bwd_noalloc", "adamw_step", "tern_grad_sumsq_workspace",
                "tern_grad_sumsq", "adamw_step_multi", "tern_sr4_workspace", "tern_sr4_step", "tern_sr4_panel", "tern_strerror",
-               "tern_device_status")
+               "tern_device_status", "tern_selftest_wait_timeout")
 
 
 class TernError(RuntimeError):
@@ -81,6 +81,7 @@ def _load():
         "tern_sr4_panel": ([vp, vp, vp, i64, i64, ci, ci, vp, vp, vp], ci),
         "tern_strerror": ([ci], ctypes.c_char_p),
         "tern_device_status": ([vp, ci], ci),
+        "tern_selftest_wait_timeout": ([ctypes.c_uint, vp], ci),
     }
     for name, (args, res) in sigs.items():
         f = getattr(lib, name)

@@ -146,14 +146,14 @@ __host__ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int 
 // Bounded wait on an mbarrier phase.  Returns false on timeout (after recording
 // it) or, when `watch_abort`, once another role has raised the abort flag.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                             bool watch_abort) {
+                                             bool watch_abort, uint64_t limit_ns = kWaitLimitNs) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (ptx::mbar_try_wait(bar, parity)) return true;
         if ((it & 63u) == 0) {
             if (watch_abort && *abort_flag) return false;
-            if (ptx::globaltimer() - t0 > kWaitLimitNs) {
+            if (ptx::globaltimer() - t0 > limit_ns) {
                 *abort_flag = 1;
                 atomicExch(&g_gemm_status, 1);
                 return false;
@@ -482,6 +482,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     tern_dw_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const GemmArgs a) {
     gemm_body<std::conditional_t<CG == 2, Dw2, Dw1>>(&tmA, &tmB, &tmB, a);
+}
+
+// Self-test of the bounded wait: one warp waits on an mbarrier that nothing
+// arrives on, with the GEMMs' wait routine and a short limit; it must give up,
+// record TERN_ERR_TIMEOUT and return.
+__global__ void tern_wait_selftest(uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(ptx::smem_u32(&bar), 1);
+        abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) wait_bounded(ptx::smem_u32(&bar), 0, &abort_flag, false, limit_ns);
 }
 
 // sgrad[c] = sum over the partial rows in ascending order (deterministic); with
@@ -895,4 +910,13 @@ extern "C" int tern_linear_bwd_noalloc(const uint16_t* X, const uint16_t* dY, co
     void* scratch = nullptr;
     if (int st = noalloc_scratch(&scratch)) return st;
     return tern_linear_bwd(X, dY, W, scale, dX, gq, sgrad, scratch, TERN_NOALLOC_SCRATCH_BYTES, M, K, N, stream);
+}
+
+extern "C" int tern_selftest_wait_timeout(unsigned limit_us, void* stream) {
+    if (limit_us < 1 || limit_us > 2000000) return TERN_ERR_ARG;
+    int num_sms = 0;
+    if (int st = check_device(&num_sms)) return st;
+    tern_wait_selftest<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<uint64_t>(limit_us) * 1000ull);
+    TERN_CUDA_TRY(cudaGetLastError());
+    return TERN_OK;
 }

@@ -264,6 +264,15 @@ const char* tern_strerror(int status);
  */
 int tern_device_status(void* stream, int clear);
 
+/*
+ * Self-test of failure detection (no counterpart in the paper): enqueue one
+ * kernel that waits, with the GEMMs' bounded-wait routine and a limit of
+ * limit_us microseconds (1..2e6), on an mbarrier nothing arrives on.  It gives
+ * up, records TERN_ERR_TIMEOUT in the device status word (see
+ * tern_device_status) and returns; the context stays usable.
+ */
+int tern_selftest_wait_timeout(unsigned limit_us, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
