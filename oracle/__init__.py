@@ -43,38 +43,48 @@ def _L():
     global _lib
     if _lib is None:
         build()
-        lib = ctypes.CDLL(_LIB)
-        vp, i64, ci, dbl, flt = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double,
-                                 ctypes.c_float)
-        sig = {
-            "or_ternary": ([ci, ci], ci),
-            "or_clamp": ([ci, ci], ci),
-            "or_bf16_value": ([ctypes.c_uint16], dbl),
-            "or_bf16_round": ([dbl], ctypes.c_uint16),
-            "or_materialize": ([vp, vp, i64, i64, ci, ci, vp, vp, vp, vp, vp], None),
-            "or_fwd": ([vp, vp, vp, i64, i64, i64, ci, vp, vp, ci], None),
-            "or_dx": ([vp, vp, vp, i64, i64, i64, ci, vp, vp, ci], None),
-            "or_dw": ([vp, vp, vp, vp, i64, i64, i64, ci, vp, vp, vp, vp, ci], None),
-            "or_fwd_at": ([vp, vp, flt, i64, ci, vp, vp], None),
-            "or_dx_at": ([vp, vp, vp, i64, ci, vp, vp], None),
-            "or_gq_at": ([vp, vp, flt, i64, vp, vp], None),
-            "or_sgrad_at": ([vp, vp, vp, i64, i64, ci, vp, vp, ci], None),
-            "or_adamw": ([vp, vp, vp, vp, i64, ci, dbl, dbl, dbl, dbl, dbl, dbl, ci, vp, vp, vp], None),
-            "or_sumsq": ([vp, i64], dbl),
-            "or_clip_factor": ([dbl, dbl], dbl),
-            "or_mix64": ([ctypes.c_uint64], ctypes.c_uint64),
-            "or_sr4_panel": ([vp, vp, vp, i64, i64, ci, ci, vp, vp], None),
-            "or_sr4_uniform": ([ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64], flt),
-            "or_sr4_scale": ([vp, i64, flt, flt], flt),
-            "or_sr4_update": ([vp, vp, i64, flt, flt, ctypes.c_uint64, i64, ctypes.c_uint64, ci, ci, vp, vp],
-                              None),
-        }
-        for name, (args, res) in sig.items():
-            f = getattr(lib, name)
-            f.argtypes = args
-            f.restype = res
-        _lib = lib
+        _lib = _bind(ctypes.CDLL(_LIB))
     return _lib
+
+
+def use_library(path=None):
+    """Point the oracle at another build of tern_oracle.c (the mutation tests plant
+    mistakes in copies of the source); None restores the default build."""
+    global _lib
+    _lib = None if path is None else _bind(ctypes.CDLL(path))
+
+
+def _bind(lib):
+    vp, i64, ci, dbl, flt = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double,
+                             ctypes.c_float)
+    sig = {
+        "or_ternary": ([ci, ci], ci),
+        "or_clamp": ([ci, ci], ci),
+        "or_bf16_value": ([ctypes.c_uint16], dbl),
+        "or_bf16_round": ([dbl], ctypes.c_uint16),
+        "or_materialize": ([vp, vp, i64, i64, ci, ci, vp, vp, vp, vp, vp], None),
+        "or_fwd": ([vp, vp, vp, i64, i64, i64, ci, vp, vp, ci], None),
+        "or_dx": ([vp, vp, vp, i64, i64, i64, ci, vp, vp, ci], None),
+        "or_dw": ([vp, vp, vp, vp, i64, i64, i64, ci, vp, vp, vp, vp, ci], None),
+        "or_fwd_at": ([vp, vp, flt, i64, ci, vp, vp], None),
+        "or_dx_at": ([vp, vp, vp, i64, ci, vp, vp], None),
+        "or_gq_at": ([vp, vp, flt, i64, vp, vp], None),
+        "or_sgrad_at": ([vp, vp, vp, i64, i64, ci, vp, vp, ci], None),
+        "or_adamw": ([vp, vp, vp, vp, i64, ci, dbl, dbl, dbl, dbl, dbl, dbl, ci, vp, vp, vp], None),
+        "or_sumsq": ([vp, i64], dbl),
+        "or_clip_factor": ([dbl, dbl], dbl),
+        "or_mix64": ([ctypes.c_uint64], ctypes.c_uint64),
+        "or_sr4_panel": ([vp, vp, vp, i64, i64, ci, ci, vp, vp], None),
+        "or_sr4_uniform": ([ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64], flt),
+        "or_sr4_scale": ([vp, i64, flt, flt], flt),
+        "or_sr4_update": ([vp, vp, i64, flt, flt, ctypes.c_uint64, i64, ctypes.c_uint64, ci, ci, vp, vp],
+                          None),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    return lib
 
 
 def _p(a):

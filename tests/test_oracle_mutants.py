@@ -1,0 +1,92 @@
+"""The pins catch plausible mistakes in the oracle.
+
+Each case plants one mistake in a copy of oracle/tern_oracle.c (a dropped
+factor, a wrong index, a flipped sign, eps under the root, truncation instead
+of round-to-nearest, ...), builds it on the CPU, points the oracle at it and
+runs the pins that cover that function: at least one of them must fail.  The
+unmutated oracle passes the same pins (test_oracle_pins.py, test_oracle_sr4.py).
+"""
+import os
+import subprocess
+import tempfile
+
+import pytest
+
+import oracle
+import test_oracle_pins as P
+import test_oracle_sr4 as S
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "tern_oracle.c")
+
+# (name, text to find, replacement, occurrence (0-based), pins that must catch it)
+MUTANTS = [
+    ("ternary threshold off by one", "if (q >= theta) return 1;", "if (q > theta) return 1;", 0,
+     [P.test_ternary_truth_table_theta2, lambda: P.test_ternary_exhaustive_int8(2)]),
+    ("clamp rail one short", "if (q > clamp) return clamp;", "if (q > clamp) return clamp - 1;", 0,
+     [lambda: P.test_clamp_exhaustive(7)]),
+    ("bf16 rounding truncates", "double r = nearbyint(ldexp(m, 8));", "double r = floor(ldexp(m, 8));", 0,
+     [P.test_bf16_round_matches_torch_rne, P.test_bf16_golden_values]),
+    ("-1 packed as 10", "uint32_t code = w == 1 ? 1u : (w == -1 ? 3u : 0u);",
+     "uint32_t code = w == 1 ? 1u : (w == -1 ? 2u : 0u);", 0, [P.test_pack_golden_words]),
+    ("forward drops the scale", "a->out[m * a->N + c] = s * acc[c];", "a->out[m * a->N + c] = acc[c];", 0,
+     [P.test_fwd_matches_library_matmul, P.test_fwd_all_positive_is_scaled_rowsum]),
+    ("forward reads X transposed-ish", "double x = or_bf16_value(a->X[m * a->K + r]);",
+     "double x = or_bf16_value(a->X[m * a->K + (a->K - 1 - r)]);", 0,
+     [P.test_fwd_signed_permutation_is_exact, P.test_fwd_identity_weight_returns_x]),
+    ("dX uses the wrong scale index", "double term = dy[c] * (double)a->scale[c] * (double)or_ternary(qrow[c], a->theta);",
+     "double term = dy[c] * (double)a->scale[r % a->N] * (double)or_ternary(qrow[c], a->theta);", 0,
+     [lambda: P.test_dx_is_the_gradient_of_the_loss((4, 8, 16))]),
+    ("G reads the wrong X column", "double x = or_bf16_value(a->X[m * a->K + r]);",
+     "double x = or_bf16_value(a->X[m * a->K + (a->K - 1 - r)]);", 1,
+     [lambda: P.test_gq_is_the_straight_through_gradient((8, 16, 16)), P.test_gq_at_unit_scale_is_xt_dy]),
+    ("gq drops the scale", "if (gq) gq[r * N + c] = G[r * N + c] * s;", "if (gq) gq[r * N + c] = G[r * N + c];", 0,
+     [lambda: P.test_gq_is_the_straight_through_gradient((4, 8, 16))]),
+    ("sgrad loses the sign of T", "s += G[r * N + c] * (double)w;", "s += G[r * N + c] * (double)abs(w);", 0,
+     [lambda: P.test_sgrad_is_the_gradient_in_the_scale((4, 8, 16)), P.test_sgrad_through_the_forward]),
+    ("AdamW eps under the root", "double step = lr * (mi / bc1) / (sqrt(vi / bc2) + eps);",
+     "double step = lr * (mi / bc1) / sqrt(vi / bc2 + eps);", 0, [P.test_adamw_eps_sits_outside_the_root]),
+    ("AdamW decay without lr", "double decay = decoupled ? lr * wd * wi : 0.0;",
+     "double decay = decoupled ? wd * wi : 0.0;", 0,
+     [P.test_adamw_first_step_closed_form, P.test_adamw_constant_gradient_closed_form]),
+    ("AdamW bias correction of v uses beta1", "double bc2 = 1.0 - pow(b2, (double)t);",
+     "double bc2 = 1.0 - pow(b1, (double)t);", 0,
+     [P.test_adamw_first_step_closed_form, P.test_adamw_constant_gradient_closed_form]),
+    ("SR4 steps up the gradient", "v = or_clamp(v - (int)d, clamp);", "v = or_clamp(v + (int)d, clamp);", 0,
+     [S.test_round_half_up_without_dither, lambda: S.test_stochastic_rounding_is_unbiased(0.3)]),
+    ("SR4 scale multiplies", "return target_step / mean;", "return target_step * mean;", 0,
+     [S.test_scale_sets_the_mean_step]),
+    ("clip inverted", "if (max_norm > 0.0 && norm > max_norm) return max_norm / norm;",
+     "if (max_norm > 0.0 && norm > max_norm) return norm / max_norm;", 0,
+     [P.test_sumsq_and_norm, P.test_clipped_gradient_has_the_clip_norm]),
+]
+
+
+def _mutant_lib(tmp, find, repl, occurrence):
+    src = open(SRC).read()
+    pos = -1
+    for _ in range(occurrence + 1):
+        pos = src.index(find, pos + 1)
+    mutated = src[:pos] + repl + src[pos + len(find):]
+    c = os.path.join(tmp, "mutant.c")
+    so = os.path.join(tmp, "libmutant.so")
+    open(c, "w").write(mutated)
+    subprocess.check_call(["gcc", "-O1", "-shared", "-fPIC", "-std=c11", "-fno-fast-math", "-ffp-contract=off",
+                           "-o", so, c, "-lm", "-lpthread"])
+    return so
+
+
+@pytest.mark.parametrize("name,find,repl,occ,pins", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_the_mutant(name, find, repl, occ, pins):
+    with tempfile.TemporaryDirectory() as tmp:
+        so = _mutant_lib(tmp, find, repl, occ)
+        oracle.use_library(so)
+        try:
+            caught = 0
+            for pin in pins:
+                try:
+                    pin()
+                except (AssertionError, ValueError):
+                    caught += 1
+            assert caught >= 1, f"no pin caught the mutant: {name}"
+        finally:
+            oracle.use_library(None)
