@@ -232,3 +232,21 @@ def test_misaligned_and_bad_arguments_are_rejected(cuda_lib):
         bl.tern_materialize(layer.q, layer.scale, layer.tiles, theta=3, q_clamp=2)
     assert e.value.status == bl.TERN_ERR_ARG
     assert bl.tern_device_status() == bl.TERN_OK
+
+
+@pytest.mark.parametrize("theta,clamp", [(1, 7), (3, 7), (5, 127)])
+def test_layer_other_thresholds(cuda_lib, theta, clamp):
+    inp = syn.linear_inputs(300, 272, 400, seed=theta * 10 + clamp)
+    inp.q = syn.int8_uniform(theta, syn.TID_Q, 272 * 400, -128, 127).reshape(272, 400)   # full int8 range
+    layer = Layer(inp, theta=theta, q_clamp=clamp).run()
+    full_oracle_check(layer)
+
+
+def test_layer_with_negative_and_zero_scales(cuda_lib):
+    inp = syn.linear_inputs(257, 400, 304, seed=77)
+    sc = syn.uniform_f32(77, syn.TID_SCALE, 304, -0.1, 0.1)
+    sc[::13] = 0.0
+    sc[5::17] = -1.0             # exact in bf16: s_lo = 0
+    inp.scale = sc
+    layer = Layer(inp).run()
+    full_oracle_check(layer)
