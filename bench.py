@@ -307,6 +307,30 @@ def rwkv_block(bl, dev, stream, steps):
             "launches_per_step_approx": launches}
 
 
+def graph_bw(torch, fn, nbytes, reps, warm, stream, peak_gbs):
+    """Device time per call of `fn` over `reps` calls captured in one CUDA graph."""
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.graph(g, stream=side):
+        for _ in range(reps):
+            fn()
+    torch.cuda.synchronize()
+    g.replay()                     # warm replay
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"ms": ms, "gbs": gbs, "frac": gbs / peak_gbs, "timing": f"{reps} calls in one CUDA graph"}
+
+
 def hbm_kernels(args):
     """The HBM-bound kernels alone at profiling sizes (each input over L2, a few GB in
     all): AdamW on 1e8 elements, packed ternarisation of 1e9 weights, the full
@@ -322,16 +346,7 @@ def hbm_kernels(args):
     stream = torch.cuda.current_stream()
 
     def loop(fn, nbytes, reps):
-        for _ in range(args.warmup):
-            fn()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(reps):
-            fn()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / reps
-        return {"ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9, "frac": nbytes / (ms * 1e-3) / 1e9 / pk["hbm"]}
+        return graph_bw(torch, fn, nbytes, reps, args.warmup, stream, pk["hbm"])
 
     out = {}
     n = 100_000_000
@@ -472,16 +487,9 @@ def run_ours(args):
 
     # ---- AdamW and ternarise bandwidth at their large sizes (separate timed loops)
     def bw_loop(fn, nbytes, reps=10, warm=3):
-        for _ in range(warm):
-            fn()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(reps):
-            fn()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ms_ = e0.elapsed_time(e1) / reps
-        return {"ms": ms_, "gbs": nbytes / (ms_ * 1e-3) / 1e9, "frac": nbytes / (ms_ * 1e-3) / 1e9 / pk["hbm"]}
+        # the reps run as one captured CUDA graph: a short kernel (tens of microseconds)
+        # would otherwise wait on the host's launch rate between reps
+        return graph_bw(torch, fn, nbytes, reps, warm, stream, pk["hbm"])
 
     extra = {}
     if not args.skip_bandwidth and args.workload == "large_single_projection":
