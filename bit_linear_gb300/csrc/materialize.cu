@@ -9,10 +9,11 @@
 //           scale[c]*T used by the dX GEMM (s_hi = bf16(scale), s_lo =
 //           bf16(scale - s_hi)); a zero weight is +0 in every plane
 //   qc      the clamped accumulator
-// The kernel is HBM-bound.  Each thread takes four 16-weight groups (one packed
-// word each) per iteration, issues their four 16-byte loads before using any,
-// and works on four weights at a time with byte-SIMD compares; every output is
-// written with 16-byte (packed: 4-byte) coalesced streaming stores.
+// The kernel is HBM-bound.  Each thread issues eight loads before using any and
+// works on four weights at a time with byte-SIMD compares.  Packed-only launches
+// take 16-weight groups (one packed word, a 16-byte q load); launches that write
+// the bf16 planes take 8-weight halves, so every plane store is one 16-byte
+// store per thread and a warp covers 512 contiguous bytes.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -128,25 +129,112 @@ __device__ __forceinline__ void encode_group(const MatArgs& a, int4 raw, int64_t
     }
 }
 
+// Eight weights (half a packed word) per thread and call, for the launches that
+// write the bf16 planes: each plane then takes one 16-byte store per thread, so
+// a warp's store covers 512 contiguous bytes; the codes go out as 16-bit halves.
+template <bool QC, bool PK, bool TT, bool HL>
+__device__ __forceinline__ void encode_half(const MatArgs& a, int2 raw, int64_t h) {
+    const uint32_t w[2] = {static_cast<uint32_t>(raw.x), static_cast<uint32_t>(raw.y)};
+    uint32_t pos[2], neg[2];
+    uint32_t code = 0;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        pos[k] = __vcmpges4(w[k], a.th_pos);
+        neg[k] = __vcmples4(w[k], a.th_neg);
+        uint32_t x = (pos[k] & 0x01010101u) | (neg[k] & 0x03030303u);
+        x = (x | (x >> 6) | (x >> 12) | (x >> 18)) & 0xFFu;
+        code |= x << (8 * k);
+    }
+    const int64_t e0 = h * 8;
+    if constexpr (QC) {
+        int2 c;
+        c.x = static_cast<int>(__vmaxs4(__vmins4(w[0], a.cl_pos), a.cl_neg));
+        c.y = static_cast<int>(__vmaxs4(__vmins4(w[1], a.cl_pos), a.cl_neg));
+        __stcs(reinterpret_cast<int2*>(a.qc + e0), c);
+    }
+    if constexpr (PK) __stcs(reinterpret_cast<unsigned short*>(a.packed) + h, static_cast<unsigned short>(code));
+    uint32_t nz[4], ng[4];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        nz[2 * k] = lanes16(pos[k] | neg[k], 0x1100u);
+        nz[2 * k + 1] = lanes16(pos[k] | neg[k], 0x3322u);
+        ng[2 * k] = lanes16(neg[k], 0x1100u);
+        ng[2 * k + 1] = lanes16(neg[k], 0x3322u);
+    }
+    if constexpr (TT) {
+        uint32_t p[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) p[i] = (nz[i] & 0x3F803F80u) | (ng[i] & 0x80008000u);
+        __stcs(reinterpret_cast<int4*>(a.t + e0), make_int4(p[0], p[1], p[2], p[3]));
+    }
+    if constexpr (HL) {
+        const uint32_t cg = static_cast<uint32_t>(h % (2 * static_cast<int64_t>(a.ngroups_row)));   // 8-column group
+        const float4* sp = reinterpret_cast<const float4*>(a.scale + static_cast<int64_t>(cg) * 8);
+        uint32_t hi2[4], lo2[4];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float4 s4 = __ldg(sp + i);
+            const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
+            uint32_t hb[4], lb[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                hb[k] = bf16_bits(sv[k]);
+                lb[k] = bf16_bits(sv[k] - __uint_as_float(hb[k] << 16));   // exact difference in fp32
+            }
+            hi2[2 * i] = hb[0] | (hb[1] << 16);
+            hi2[2 * i + 1] = hb[2] | (hb[3] << 16);
+            lo2[2 * i] = lb[0] | (lb[1] << 16);
+            lo2[2 * i + 1] = lb[2] | (lb[3] << 16);
+        }
+        // a zero weight is +0; a negative weight flips the sign bit of s_hi / s_lo
+        if (a.whi) {
+            uint32_t p[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) p[i] = (hi2[i] & nz[i]) ^ (ng[i] & 0x80008000u);
+            __stcs(reinterpret_cast<int4*>(a.whi + e0), make_int4(p[0], p[1], p[2], p[3]));
+        }
+        if (a.wlo) {
+            uint32_t p[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) p[i] = (lo2[i] & nz[i]) ^ (ng[i] & 0x80008000u);
+            __stcs(reinterpret_cast<int4*>(a.wlo + e0), make_int4(p[0], p[1], p[2], p[3]));
+        }
+    }
+}
+
 }  // namespace
 
 // Which encodings a launch writes is a template choice, so the packed-only
-// ternarisation carries no registers for the bf16 planes and keeps eight 16-byte
-// loads in flight per thread.
+// ternarisation carries no registers for the bf16 planes.
 template <bool QC, bool PK, bool TT, bool HL>
 __global__ void __launch_bounds__(256) tern_materialize_kernel(const MatArgs a) {
-    constexpr int U = (TT || HL) ? 4 : 8;
+    constexpr int U = 8;
     const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    int64_t gi = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int4* q4 = reinterpret_cast<const int4*>(a.q);
-    for (; gi + (U - 1) * nth < a.groups; gi += U * nth) {
-        int4 r[U];
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if constexpr (TT || HL) {
+        const int64_t halves = a.groups * 2;
+        const int2* q2 = reinterpret_cast<const int2*>(a.q);
+        int64_t h = tid;
+        for (; h + (U - 1) * nth < halves; h += U * nth) {
+            int2 r[U];
 #pragma unroll
-        for (int j = 0; j < U; ++j) r[j] = __ldcs(q4 + gi + j * nth);
+            for (int j = 0; j < U; ++j) r[j] = __ldcs(q2 + h + j * nth);
 #pragma unroll
-        for (int j = 0; j < U; ++j) encode_group<QC, PK, TT, HL>(a, r[j], gi + j * nth);
+            for (int j = 0; j < U; ++j) encode_half<QC, PK, TT, HL>(a, r[j], h + j * nth);
+        }
+        for (; h < halves; h += nth) encode_half<QC, PK, TT, HL>(a, __ldcs(q2 + h), h);
+    } else {
+        const int4* q4 = reinterpret_cast<const int4*>(a.q);
+        int64_t gi = tid;
+        for (; gi + (U - 1) * nth < a.groups; gi += U * nth) {
+            int4 r[U];
+#pragma unroll
+            for (int j = 0; j < U; ++j) r[j] = __ldcs(q4 + gi + j * nth);
+#pragma unroll
+            for (int j = 0; j < U; ++j) encode_group<QC, PK, TT, HL>(a, r[j], gi + j * nth);
+        }
+        for (; gi < a.groups; gi += nth) encode_group<QC, PK, TT, HL>(a, __ldcs(q4 + gi), gi);
     }
-    for (; gi < a.groups; gi += nth) encode_group<QC, PK, TT, HL>(a, __ldcs(q4 + gi), gi);
 }
 
 namespace {
@@ -160,7 +248,8 @@ int launch_materialize(const MatArgs& a, int num_sms, cudaStream_t s) {
         TERN_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, 256, 0));
         per_sm = b > 0 ? b : 1;
     }
-    const int64_t want = (a.groups + 255) / 256;
+    const int64_t items = (TT || HL) ? 2 * a.groups : a.groups;   // eight- or sixteen-weight items
+    const int64_t want = (items + 255) / 256;
     const int64_t cap = static_cast<int64_t>(num_sms) * per_sm;
     const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
     kernel<<<grid, 256, 0, s>>>(a);
