@@ -49,6 +49,8 @@ WORKLOADS = {
     "profile_quarter_tokens": dict(M=8192, K=4096, N=12288, scale_lo=0.005, scale_hi=0.05, zero_prob=0.0),
     # not a layer: the HBM-bound kernels alone (AdamW, ternarise, materialise, SR4, panel)
     "hbm_kernels": None,
+    # the six projections of the RWKV-style block, M = 8192 (extra line, not the headline)
+    "rwkv_block": None,
 }
 ADAM_HP = dict(lr=1e-3, b1=0.9, b2=0.95, eps=1e-8, wd=0.1)
 
@@ -616,6 +618,15 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.workload == "hbm_kernels":
         return hbm_kernels(args)
+    if args.workload == "rwkv_block":
+        import torch
+        torch.cuda.set_device(0)
+        import __graft_entry__
+        __graft_entry__._builder().build()
+        import bit_linear_gb300 as bl
+        out = rwkv_block(bl, torch.device("cuda"), torch.cuda.current_stream(), args.steps)
+        print(json.dumps({"rwkv_block": out}), flush=True)
+        return 0
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

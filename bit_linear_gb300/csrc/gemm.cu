@@ -512,16 +512,20 @@ __global__ void tern_sgrad_reduce(const float* __restrict__ partial, int nparts,
 
 // Finish the split G tiles: G = sum over the tile's slices in slice order, then
 // the same epilogue as the G kernel (gq = G*scale[c], or += with accumulate,
-// and the sgrad partial of each 32-row group).  One CTA per 32-row group of a
-// tile, one thread per column.
+// and the sgrad partial of each 32-row group).  One CTA per 32 x 32 block of a
+// tile: warp w takes rows 4w..4w+3 of the block, lane l column l; the eight
+// warps' column sums are added in warp order through shared memory.
 __global__ void __launch_bounds__(256) tern_dw_split_reduce(const GemmArgs a, int tile_m, int tile_n) {
-    const int groups_per_tile = tile_m / 32;
-    const int j = blockIdx.x / groups_per_tile;           // tail tile
-    const int rg = blockIdx.x % groups_per_tile;          // 32-row group within the tile
+    const int row_groups = tile_m / 32, col_groups = tile_n / 32;
+    const int per_tile = row_groups * col_groups;
+    const int j = blockIdx.x / per_tile;                   // tail tile
+    const int rg = (blockIdx.x % per_tile) / col_groups;   // 32-row group within the tile
+    const int cgi = blockIdx.x % col_groups;               // 32-column group within the tile
     int tm, tn;
     if (tile_m == 2 * kBM) tile_coords<8>(a.tile_begin + j, a.tiles_m, a.tiles_n, tm, tn);
     else tile_coords<16>(a.tile_begin + j, a.tiles_m, a.tiles_n, tm, tn);
-    const int c_in = threadIdx.x;                 // column within the tile (blockDim = tile_n)
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c_in = cgi * 32 + lane;                      // column within the tile
     const int col = tn * tile_n + c_in;
     const int r_base = tm * tile_m + rg * 32;
     // partial rows exist for every 32-row group of the 128-row blocks that hold rows;
@@ -529,25 +533,37 @@ __global__ void __launch_bounds__(256) tern_dw_split_reduce(const GemmArgs a, in
     if (r_base >= ((a.Mg + kBM - 1) / kBM) * kBM) return;
     const bool col_ok = col < a.Ng;
     float colsum = 0.0f;
-    for (int r = 0; r < 32; ++r) {
-        const int row = r_base + r;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r_in = rg * 32 + warp * 4 + i;           // row within the tile
+        const int row = tm * tile_m + r_in;
+        const float* p = a.partial_g + static_cast<int64_t>(j) * a.split * tile_m * tile_n +
+                         static_cast<int64_t>(r_in) * tile_n + c_in;
         float g = 0.0f;
-        for (int sl = 0; sl < a.split; ++sl)
-            g += a.partial_g[(static_cast<int64_t>(j) * a.split + sl) * tile_m * tile_n +
-                             static_cast<int64_t>(rg * 32 + r) * tile_n + c_in];
+        for (int sl = 0; sl < a.split; ++sl) g += p[static_cast<int64_t>(sl) * tile_m * tile_n];
         if (row < a.Mg && col_ok) {
             if (a.out) {
-                float v = g * a.scale[col];
+                const float v = g * a.scale[col];
                 float* o = a.out + static_cast<int64_t>(row) * a.Ng + col;
                 *o = a.accumulate ? *o + v : v;
             }
             if (a.partial) {
-                const uint32_t code = (a.packed[static_cast<int64_t>(row) * (a.Ng / 16) + col / 16] >> (2 * (col % 16))) & 3u;
+                const uint32_t code =
+                    (a.packed[static_cast<int64_t>(row) * (a.Ng / 16) + col / 16] >> (2 * (col % 16))) & 3u;
                 colsum += (code & 1u) ? ((code & 2u) ? -g : g) : 0.0f;
             }
         }
     }
-    if (a.partial && col_ok) a.partial[static_cast<int64_t>(r_base / 32) * a.Ng + col] = colsum;
+    if (a.partial == nullptr) return;
+    __shared__ float red[8][32];
+    red[warp][lane] = colsum;
+    __syncthreads();
+    if (warp == 0 && col_ok) {
+        float s = 0.0f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) s += red[w][lane];
+        a.partial[static_cast<int64_t>(r_base / 32) * a.Ng + col] = s;
+    }
 }
 
 // ===================================================================== host side
@@ -740,8 +756,8 @@ int run_dw(K kernel, const uint16_t* X, const uint16_t* dY, const float* scale, 
                 t.kb_per = kb_per;
                 t.partial_g = tail;
                 if (int st = launch<C>(kernel, t, num_sms, s, mA, mB)) return st;
-                tern_dw_split_reduce<<<static_cast<unsigned>(R * (C::TILE_M / 32)), C::BN, 0, s>>>(t, C::TILE_M,
-                                                                                                  C::BN);
+                tern_dw_split_reduce<<<static_cast<unsigned>(R * (C::TILE_M / 32) * (C::BN / 32)), 256, 0, s>>>(
+                    t, C::TILE_M, C::BN);
                 TERN_CUDA_TRY(cudaGetLastError());
                 return TERN_OK;
             }
