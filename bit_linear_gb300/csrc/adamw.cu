@@ -40,6 +40,8 @@ __device__ __forceinline__ void adam_one(const AdamArgs& a, float& w, float g, f
 }  // namespace
 
 __global__ void __launch_bounds__(256) tern_adamw_kernel(const AdamArgs a) {
+    ptx::pdl_trigger();
+    ptx::pdl_wait();
     const int64_t n4 = a.n >> 2;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -102,9 +104,7 @@ extern "C" int adamw_step(float* w, const float* g, float* m, float* v, int64_t 
     const int64_t want = ((n >> 2) + 255) / 256;
     const int64_t cap = static_cast<int64_t>(num_sms) * 8;
     const unsigned grid = static_cast<unsigned>(want < 1 ? 1 : (want < cap ? want : cap));
-    tern_adamw_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
-    TERN_CUDA_TRY(cudaGetLastError());
-    return TERN_OK;
+    return launch_pdl(tern_adamw_kernel, dim3(grid), dim3(256), 0, static_cast<cudaStream_t>(stream), a);
 }
 
 // ===================================================================== several tensors per launch
@@ -179,6 +179,8 @@ __device__ __forceinline__ void adam_elem(const MultiArgs& a, float lr, float bc
 }  // namespace
 
 __global__ void __launch_bounds__(256) tern_adamw_multi_kernel(const __grid_constant__ MultiArgs a) {
+    ptx::pdl_trigger();
+    ptx::pdl_wait();
     const tern_adam_scalars hp = *a.hp;
     float gmul = hp.gmul;
     if (a.sumsq) {
@@ -227,6 +229,8 @@ __global__ void __launch_bounds__(256) tern_adamw_multi_kernel(const __grid_cons
 // Per-chunk fp64 sums of squares (fixed chunking and order), then one CTA sums
 // the chunk partials in a fixed order.
 __global__ void __launch_bounds__(256) tern_sumsq_chunks(const __grid_constant__ SumArgs a) {
+    ptx::pdl_trigger();
+    ptx::pdl_wait();
     __shared__ double red[256];
     for (int64_t ch = blockIdx.x; ch < a.nchunks; ch += gridDim.x) {
         const int t = chunk_tensor(a, ch);
@@ -251,6 +255,8 @@ __global__ void __launch_bounds__(256) tern_sumsq_chunks(const __grid_constant__
 
 __global__ void __launch_bounds__(256) tern_sumsq_final(const double* __restrict__ partial, int64_t nparts,
                                                         double* __restrict__ out) {
+    ptx::pdl_trigger();
+    ptx::pdl_wait();
     __shared__ double red[256];
     double acc = 0.0;
     for (int64_t i = threadIdx.x; i < nparts; i += blockDim.x) acc += partial[i];
@@ -304,12 +310,9 @@ extern "C" int tern_grad_sumsq(const float* const* g, const int64_t* n, int nten
     a.out = sumsq;
     if (a.nchunks > 0) {
         const int64_t grid = a.nchunks < 8 * num_sms ? a.nchunks : 8 * num_sms;
-        tern_sumsq_chunks<<<static_cast<unsigned>(grid), 256, 0, s>>>(a);
-        TERN_CUDA_TRY(cudaGetLastError());
+        if (int st = launch_pdl(tern_sumsq_chunks, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s, a)) return st;
     }
-    tern_sumsq_final<<<1, 256, 0, s>>>(a.partial, a.nchunks, sumsq);
-    TERN_CUDA_TRY(cudaGetLastError());
-    return TERN_OK;
+    return launch_pdl(tern_sumsq_final, dim3(1), dim3(256), 0, s, static_cast<const double*>(a.partial), a.nchunks, sumsq);
 }
 
 extern "C" int adamw_step_multi(float* const* w, const float* const* g, float* const* m, float* const* v,
@@ -345,7 +348,6 @@ extern "C" int adamw_step_multi(float* const* w, const float* const* g, float* c
     a.max_norm = max_norm;
     a.skipped = skipped;
     const int64_t grid = a.nchunks < 1 ? 1 : (a.nchunks < 8 * num_sms ? a.nchunks : 8 * num_sms);
-    tern_adamw_multi_kernel<<<static_cast<unsigned>(grid), 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
-    TERN_CUDA_TRY(cudaGetLastError());
-    return TERN_OK;
+    return launch_pdl(tern_adamw_multi_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0,
+                      static_cast<cudaStream_t>(stream), a);
 }

@@ -27,12 +27,43 @@ int gemm_status_read(int clear);
 }  // namespace tern
 
 #ifdef __CUDACC__
+#include <utility>
+namespace tern {
+// Every kernel of the library is launched with programmatic stream serialization
+// (programmatic dependent launch): the next kernel on the stream may launch while
+// this one finishes, and each kernel waits for its predecessor (ptx::pdl_wait)
+// before it touches global memory.  Launch latency and prologues (barrier set-up,
+// TMEM allocation) then overlap the previous kernel's tail.
+template <class... KArgs, class... Args>
+int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args) {
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    TERN_CUDA_TRY(cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...));
+    return TERN_OK;
+}
+}  // namespace tern
+#endif
+
+#ifdef __CUDACC__
 namespace tern {
 namespace ptx {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+
+// Programmatic dependent launch: let the next kernel on the stream launch now;
+// wait until the previous kernel has finished and its writes are visible.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ uint64_t globaltimer() {
     uint64_t t;

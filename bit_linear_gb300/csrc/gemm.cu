@@ -252,6 +252,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
     const uint32_t FULL0 = bar0, EMPTY0 = bar0 + 8u * C::STAGES;
     const uint32_t TFULL0 = bar0 + 16u * C::STAGES, TEMPTY0 = TFULL0 + 16u, DRAIN = TFULL0 + 32u;
 
+    ptx::pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = CG == 2 ? ptx::cluster_ctarank() : 0u;   // 0 = leader of the pair
     const int unit = CG == 2 ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
@@ -284,6 +285,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
     if constexpr (CG == 2) ptx::cluster_sync(); else __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    ptx::pdl_wait();   // the set-up above overlapped the previous kernel; global memory from here on
 
     uint32_t issued = 0, issued_parity = 0;   // producer: stages with a copy issued, and its phase
     if (warp == 0 && lane == 0) {
@@ -488,6 +490,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // arrives on, with the GEMMs' wait routine and a short limit; it must give up,
 // record TERN_ERR_TIMEOUT and return.
 __global__ void tern_wait_selftest(uint64_t limit_ns) {
+    ptx::pdl_trigger();
+    ptx::pdl_wait();
     __shared__ uint64_t bar;
     __shared__ int abort_flag;
     if (threadIdx.x == 0) {
@@ -503,6 +507,8 @@ __global__ void tern_wait_selftest(uint64_t limit_ns) {
 // accumulate, that sum is added to the stored sgrad[c].
 __global__ void tern_sgrad_reduce(const float* __restrict__ partial, int nparts, int N, float* __restrict__ sgrad,
                                   int accumulate) {
+    ptx::pdl_trigger();
+    ptx::pdl_wait();
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
     if (c >= N) return;
     float s = 0.0f;
@@ -516,6 +522,8 @@ __global__ void tern_sgrad_reduce(const float* __restrict__ partial, int nparts,
 // tile: warp w takes rows 4w..4w+3 of the block, lane l column l; the eight
 // warps' column sums are added in warp order through shared memory.
 __global__ void __launch_bounds__(256) tern_dw_split_reduce(const GemmArgs a, int tile_m, int tile_n) {
+    ptx::pdl_trigger();
+    ptx::pdl_wait();
     const int row_groups = tile_m / 32, col_groups = tile_n / 32;
     const int per_tile = row_groups * col_groups;
     const int j = blockIdx.x / per_tile;                   // tail tile
@@ -644,10 +652,12 @@ int launch(K kernel, const GemmArgs& a, int num_sms, cudaStream_t s, const Maps&
     });
     TERN_CUDA_TRY(smem_attr[dev]);
     cudaLaunchConfig_t cfg{};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = s;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // programmatic dependent launch
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     if constexpr (C::CG == 2) {
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
@@ -664,10 +674,11 @@ int launch(K kernel, const GemmArgs& a, int num_sms, cudaStream_t s, const Maps&
         }
         if (a.num_tiles < 0) return max_clusters[dev];   // query: persistent units of this kernel
         cfg.gridDim = dim3(2 * std::min(a.num_units, max_clusters[dev]));
+        cfg.numAttrs = 2;
     } else {
         if (a.num_tiles < 0) return num_sms;
-        cfg.attrs = nullptr;
-        cfg.numAttrs = 0;
+        cfg.attrs = attr + 1;
+        cfg.numAttrs = 1;
         cfg.gridDim = dim3(std::min(a.num_units, num_sms));
     }
     TERN_CUDA_TRY(cudaLaunchKernelEx(&cfg, kernel, maps..., a));
@@ -756,10 +767,8 @@ int run_dw(K kernel, const uint16_t* X, const uint16_t* dY, const float* scale, 
                 t.kb_per = kb_per;
                 t.partial_g = tail;
                 if (int st = launch<C>(kernel, t, num_sms, s, mA, mB)) return st;
-                tern_dw_split_reduce<<<static_cast<unsigned>(R * (C::TILE_M / 32) * (C::BN / 32)), 256, 0, s>>>(
-                    t, C::TILE_M, C::BN);
-                TERN_CUDA_TRY(cudaGetLastError());
-                return TERN_OK;
+                return launch_pdl(tern_dw_split_reduce, dim3(static_cast<unsigned>(R * (C::TILE_M / 32) * (C::BN / 32))),
+                                  dim3(256), 0, s, t, C::TILE_M, C::BN);
             }
         }
     }
@@ -856,10 +865,9 @@ extern "C" int tern_linear_bwd_ex(const uint16_t* X, const uint16_t* dY, const t
         if (st) return st;
         if (!sgrad) return TERN_OK;
         const int nparts = static_cast<int>((K + kBM - 1) / kBM) * 4;
-        tern_sgrad_reduce<<<static_cast<unsigned>((N + 255) / 256), 256, 0, s>>>(partial, nparts,
-                                                                                 static_cast<int>(N), sgrad,
-                                                                                 accumulate);
-        TERN_CUDA_TRY(cudaGetLastError());
+        if (int st = launch_pdl(tern_sgrad_reduce, dim3(static_cast<unsigned>((N + 255) / 256)), dim3(256), 0, s,
+                                static_cast<const float*>(partial), nparts, static_cast<int>(N), sgrad, accumulate))
+            return st;
     }
     return TERN_OK;
 }
@@ -932,7 +940,6 @@ extern "C" int tern_selftest_wait_timeout(unsigned limit_us, void* stream) {
     if (limit_us < 1 || limit_us > 2000000) return TERN_ERR_ARG;
     int num_sms = 0;
     if (int st = check_device(&num_sms)) return st;
-    tern_wait_selftest<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<uint64_t>(limit_us) * 1000ull);
-    TERN_CUDA_TRY(cudaGetLastError());
-    return TERN_OK;
+    return launch_pdl(tern_wait_selftest, dim3(1), dim3(32), 0, static_cast<cudaStream_t>(stream),
+                      static_cast<uint64_t>(limit_us) * 1000ull);
 }

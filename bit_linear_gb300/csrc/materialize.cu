@@ -208,6 +208,8 @@ __device__ __forceinline__ void encode_half(const MatArgs& a, int2 raw, int64_t 
 // ternarisation carries no registers for the bf16 planes.
 template <bool QC, bool PK, bool TT, bool HL>
 __global__ void __launch_bounds__(256) tern_materialize_kernel(const MatArgs a) {
+    ptx::pdl_trigger();
+    ptx::pdl_wait();
     constexpr int U = 8;
     const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -252,9 +254,7 @@ int launch_materialize(const MatArgs& a, int num_sms, cudaStream_t s) {
     const int64_t want = (items + 255) / 256;
     const int64_t cap = static_cast<int64_t>(num_sms) * per_sm;
     const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
-    kernel<<<grid, 256, 0, s>>>(a);
-    TERN_CUDA_TRY(cudaGetLastError());
-    return TERN_OK;
+    return launch_pdl(kernel, dim3(grid), dim3(256), 0, s, a);
 }
 
 template <bool QC, bool PK, bool TT>

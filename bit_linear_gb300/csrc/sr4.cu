@@ -64,6 +64,8 @@ __device__ __forceinline__ int8_t sr4_one(const Sr4Args& a, int8_t q, float g, f
 }  // namespace
 
 __global__ void __launch_bounds__(256) tern_sr4_absum(const Sr4Args a) {
+    ptx::pdl_trigger();
+    ptx::pdl_wait();
     // block b owns the contiguous slice [b*n/B, (b+1)*n/B)
     const int64_t lo = a.n * blockIdx.x / gridDim.x, hi = a.n * (blockIdx.x + 1) / gridDim.x;
     double acc = 0.0;
@@ -80,6 +82,8 @@ __global__ void __launch_bounds__(256) tern_sr4_absum(const Sr4Args a) {
 }
 
 __global__ void __launch_bounds__(256) tern_sr4_finalize(const Sr4Args a, int nparts) {
+    ptx::pdl_trigger();
+    ptx::pdl_wait();
     __shared__ double red[256];
     double acc = 0.0;
     for (int i = threadIdx.x; i < nparts; i += blockDim.x) acc += a.partial[i];
@@ -98,6 +102,8 @@ __global__ void __launch_bounds__(256) tern_sr4_finalize(const Sr4Args a, int np
 }
 
 __global__ void __launch_bounds__(256) tern_sr4_update(const Sr4Args a) {
+    ptx::pdl_trigger();
+    ptx::pdl_wait();
     const float s = *a.s;
     const int64_t groups = a.n / 16;
     const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -158,16 +164,12 @@ extern "C" int tern_sr4_step(int8_t* q, const float* gq, int64_t numel, float in
     a.s = reinterpret_cast<float*>(static_cast<char*>(workspace) + kAbsumBlocks * sizeof(double));
     a.s_out = s_out;
     const int nparts = static_cast<int>(numel < kAbsumBlocks ? numel : kAbsumBlocks);
-    tern_sr4_absum<<<nparts, 256, 0, s>>>(a);
-    TERN_CUDA_TRY(cudaGetLastError());
-    tern_sr4_finalize<<<1, 256, 0, s>>>(a, nparts);
-    TERN_CUDA_TRY(cudaGetLastError());
+    if (int st = launch_pdl(tern_sr4_absum, dim3(nparts), dim3(256), 0, s, a)) return st;
+    if (int st = launch_pdl(tern_sr4_finalize, dim3(1), dim3(256), 0, s, a, nparts)) return st;
     const int64_t want = (numel / 16 + 255) / 256;
     const int64_t cap = static_cast<int64_t>(num_sms) * 8;
     const unsigned grid = static_cast<unsigned>(want < 1 ? 1 : (want < cap ? want : cap));
-    tern_sr4_update<<<grid, 256, 0, s>>>(a);
-    TERN_CUDA_TRY(cudaGetLastError());
-    return TERN_OK;
+    return launch_pdl(tern_sr4_update, dim3(grid), dim3(256), 0, s, a);
 }
 
 // ===================================================================== SR4 health panel
@@ -198,6 +200,8 @@ struct PanelArgs {
 }  // namespace
 
 __global__ void __launch_bounds__(256) tern_panel_counts(const PanelArgs a) {
+    ptx::pdl_trigger();
+    ptx::pdl_wait();
     unsigned long long c[6] = {0, 0, 0, 0, 0, 0};
     const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t gi = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; gi < a.groups; gi += nth) {
@@ -238,6 +242,8 @@ __global__ void __launch_bounds__(256) tern_panel_counts(const PanelArgs a) {
 }
 
 __global__ void __launch_bounds__(256) tern_panel_scale(const PanelArgs a) {
+    ptx::pdl_trigger();
+    ptx::pdl_wait();
     __shared__ double smin[256], smax[256], ssum[256];
     double mn = 0.0, mx = 0.0, sm = 0.0;
     bool any = false;
@@ -294,9 +300,7 @@ extern "C" int tern_sr4_panel(const int8_t* q, const uint32_t* packed_prev, cons
     TERN_CUDA_TRY(cudaMemsetAsync(counts, 0, 6 * sizeof(unsigned long long), s));
     const int64_t want = (a.groups + 255) / 256;
     const int64_t cap = static_cast<int64_t>(num_sms) * 8;
-    tern_panel_counts<<<static_cast<unsigned>(want < cap ? want : cap), 256, 0, s>>>(a);
-    TERN_CUDA_TRY(cudaGetLastError());
-    tern_panel_scale<<<1, 256, 0, s>>>(a);
-    TERN_CUDA_TRY(cudaGetLastError());
-    return TERN_OK;
+    if (int st = launch_pdl(tern_panel_counts, dim3(static_cast<unsigned>(want < cap ? want : cap)), dim3(256), 0, s, a))
+        return st;
+    return launch_pdl(tern_panel_scale, dim3(1), dim3(256), 0, s, a);
 }
