@@ -55,6 +55,14 @@ WORKLOADS = {
 ADAM_HP = dict(lr=1e-3, b1=0.9, b2=0.95, eps=1e-8, wd=0.1)
 
 
+_T0 = time.perf_counter()
+
+
+def progress(msg):
+    """One line per bench phase on stderr (the JSON line alone goes to stdout)."""
+    print(f"[bench {time.perf_counter() - _T0:7.1f} s] {msg}", file=sys.stderr, flush=True)
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -275,37 +283,74 @@ def rwkv_block(bl, dev, stream, steps):
             bl.tern_linear_bwd(L["X"], L["dY"], L["tiles"], L["scale"], L["dX"], L["gq"], L["sgrad"], L["ws"])
             bl.adamw_step(L["scale"], L["sgrad"], L["m"], L["v"], 1, **ADAM_HP)
 
+    # Grouped calls in a block's dependency order: the r, k, v projections read one
+    # input and run as one group; the output projection and the two channel-mixing
+    # layers each wait for the one before.  AdamW of all six scales in one launch.
+    fwd_groups = [[0, 1, 2], [3], [4], [5]]
+    bwd_groups = [[5], [4], [3], [0, 1, 2]]
+    gws = {tuple(gr): torch.empty(bl.tern_linear_bwd_grouped_workspace([(M, layers[i]["K"], layers[i]["N"])
+                                                                        for i in gr]) // 4, device=dev)
+           for gr in bwd_groups}
+    adam_scalars = torch.tensor([ADAM_HP["lr"], 1 - ADAM_HP["b1"], 1 - ADAM_HP["b2"], 1.0], device=dev)
+
+    def block_grouped():
+        for L in layers:
+            bl.tern_materialize(L["q"], L["scale"], L["tiles"], 2, 7)
+        for gr in fwd_groups:
+            bl.tern_linear_fwd_grouped([dict(X=layers[i]["X"], tiles=layers[i]["tiles"], scale=layers[i]["scale"],
+                                             Y=layers[i]["Y"]) for i in gr])
+        for gr in bwd_groups:
+            bl.tern_linear_bwd_grouped([dict(X=layers[i]["X"], dY=layers[i]["dY"], tiles=layers[i]["tiles"],
+                                             scale=layers[i]["scale"], dX=layers[i]["dX"], gq=layers[i]["gq"],
+                                             sgrad=layers[i]["sgrad"]) for i in gr], gws[tuple(gr)])
+        bl.adamw_step_multi([L["scale"] for L in layers], [L["sgrad"] for L in layers], [L["m"] for L in layers],
+                            [L["v"] for L in layers], adam_scalars, ADAM_HP["b1"], ADAM_HP["b2"], ADAM_HP["eps"],
+                            ADAM_HP["wd"])
+
     flops = 6.0 * M * sum(K * N for K, N in shapes)
     reps = max(20, min(steps, 200))
-    for _ in range(5):
-        block()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(reps):
-        block()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    eager_ms = e0.elapsed_time(e1) / reps
-    g = torch.cuda.CUDAGraph()
-    s2 = torch.cuda.Stream()
-    s2.wait_stream(stream)
-    with torch.cuda.graph(g, stream=s2):
-        block()
-    torch.cuda.synchronize()
-    for _ in range(3):
-        g.replay()
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(reps):
-        g.replay()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    graph_ms = e0.elapsed_time(e1) / reps
+
+    def eager(fn):
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    def graphed(fn):
+        g = torch.cuda.CUDAGraph()
+        s2 = torch.cuda.Stream()
+        s2.wait_stream(stream)
+        with torch.cuda.graph(g, stream=s2):
+            fn()
+        torch.cuda.synchronize()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    progress("RWKV block: per-layer calls")
+    eager_ms, graph_ms = eager(block), graphed(block)
+    progress("RWKV block: grouped calls")
+    geager_ms, ggraph_ms = eager(block_grouped), graphed(block_grouped)
+
+    def rate(ms):
+        return {"ms": ms, "tflops": flops / (ms * 1e-3) / 1e12}
+
     launches = sum(1 + 1 + 4 + 1 for _ in shapes)   # materialise, fwd, dX + G (+ split reduce) + sgrad, AdamW
     return {"M": M, "shapes": [list(x) for x in shapes], "flops_per_step": flops,
-            "eager": {"ms": eager_ms, "tflops": flops / (eager_ms * 1e-3) / 1e12},
-            "graph": {"ms": graph_ms, "tflops": flops / (graph_ms * 1e-3) / 1e12},
+            "eager": rate(eager_ms), "graph": rate(graph_ms),
+            "grouped_eager": rate(geager_ms), "grouped_graph": rate(ggraph_ms),
             "launches_per_step_approx": launches}
 
 
@@ -392,6 +437,7 @@ def run_ours(args):
     import bit_linear_gb300 as bl
 
     pk = peaks()
+    progress(f"generating inputs ({args.workload})")
     inp = make_inputs(args.workload)
     M, K, N = inp.M, inp.K, inp.N
     dev = torch.device("cuda")
@@ -443,9 +489,11 @@ def run_ours(args):
     g_tiles = ((K + 255) // 256) * ((N + 255) // 256)
     launches_per_step = 6 + (2 if g_tiles % units else 0)
 
+    progress("warm-up steps")
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
+    progress("timed steps")
     if bl.tern_device_status() != bl.TERN_OK:
         raise RuntimeError("a kernel gave up on a bounded wait during warm-up")
 
@@ -495,6 +543,7 @@ def run_ours(args):
 
     extra = {}
     if not args.skip_bandwidth and args.workload == "large_single_projection":
+        progress("AdamW and ternarise bandwidth sweeps")
         del Y
         torch.cuda.empty_cache()
         sweep = []
@@ -528,12 +577,14 @@ def run_ours(args):
     # ---- the RWKV-style block (M = 8192 tokens; 4 x 512x512, 512x2048, 2048x512):
     #      the same step over its six projections, eager and replayed as one CUDA graph
     if not args.skip_bandwidth and args.workload == "large_single_projection":
+        progress("RWKV block")
         extra["rwkv_block"] = rwkv_block(bl, dev, stream, args.steps)
 
     # ---- end to end through the C ABI: every step's inputs X and dY copied from
     #      pinned host memory and the step's result (updated scales and their
     #      gradient) read back.  The upload of step i+1 runs on a copy stream into
     #      the other of two input buffers while step i computes (double buffering).
+    progress("end to end")
     e2e_steps = min(args.steps, 10)
     res_h = torch.empty(2, N, dtype=torch.float32).pin_memory()
     Xb, dYb = [X, torch.empty_like(X)], [dY, torch.empty_like(dY)]
@@ -574,6 +625,7 @@ def run_ours(args):
     if rank == 0:
         cpu = None
         if ws == 1 and not args.skip_cpu:
+            progress("CPU oracle sample")
             v, desc, cores = oracle_sample(inp, args.cpu_budget)
             cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
         csum = clk.summary()

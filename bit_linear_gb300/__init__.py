@@ -40,7 +40,8 @@ TERN_BWD_ACCUMULATE = 1
 # the C ABI's exported symbols (tests check the library exports every one)
 ABI_SYMBOLS = ("tern_tiles_bytes", "tern_materialize", "tern_linear_fwd", "tern_linear_bwd_workspace_min",
                "tern_linear_bwd_workspace",
-               "tern_linear_bwd", "tern_linear_bwd_ex", "tern_linear_bwd_noalloc", "adamw_step", "tern_grad_sumsq_workspace",
+               "tern_linear_bwd", "tern_linear_bwd_ex", "tern_linear_bwd_noalloc", "tern_linear_fwd_grouped",
+               "tern_linear_bwd_grouped_workspace", "tern_linear_bwd_grouped", "adamw_step", "tern_grad_sumsq_workspace",
                "tern_grad_sumsq", "adamw_step_multi", "tern_sr4_workspace", "tern_sr4_step", "tern_sr4_panel", "tern_strerror",
                "tern_device_status", "tern_selftest_wait_timeout")
 
@@ -54,6 +55,13 @@ class TernError(RuntimeError):
 class _Tiles(ctypes.Structure):
     _fields_ = [("packed", ctypes.c_void_p), ("t_bf16", ctypes.c_void_p),
                 ("whi_bf16", ctypes.c_void_p), ("wlo_bf16", ctypes.c_void_p)]
+
+
+class _Layer(ctypes.Structure):
+    _fields_ = [("X", ctypes.c_void_p), ("dY", ctypes.c_void_p), ("W", ctypes.POINTER(_Tiles)),
+                ("scale", ctypes.c_void_p), ("Y", ctypes.c_void_p), ("dX", ctypes.c_void_p),
+                ("gq", ctypes.c_void_p), ("sgrad", ctypes.c_void_p), ("M", ctypes.c_int64),
+                ("K", ctypes.c_int64), ("N", ctypes.c_int64)]
 
 
 def _load():
@@ -71,6 +79,9 @@ def _load():
         "tern_linear_bwd": ([vp, vp, tp, vp, vp, vp, vp, vp, sz, i64, i64, i64, vp], ci),
         "tern_linear_bwd_ex": ([vp, vp, tp, vp, vp, vp, vp, vp, sz, i64, i64, i64, ctypes.c_uint, vp], ci),
         "tern_linear_bwd_noalloc": ([vp, vp, tp, vp, vp, vp, vp, i64, i64, i64, vp], ci),
+        "tern_linear_fwd_grouped": ([ctypes.POINTER(_Layer), ci, vp], ci),
+        "tern_linear_bwd_grouped_workspace": ([ctypes.POINTER(_Layer), ci], sz),
+        "tern_linear_bwd_grouped": ([ctypes.POINTER(_Layer), ci, vp, sz, ctypes.c_uint, vp], ci),
         "adamw_step": ([vp, vp, vp, vp, i64, ci, cf, cf, cf, cf, cf, cf, ci, vp], ci),
         "tern_grad_sumsq_workspace": ([ctypes.POINTER(i64), ci], sz),
         "tern_grad_sumsq": ([ctypes.POINTER(vp), ctypes.POINTER(i64), ci, vp, vp, sz, vp], ci),
@@ -217,6 +228,56 @@ def tern_linear_bwd_noalloc(X, dY, tiles: Tiles, scale, dX, gq, sgrad, stream=No
                                        _ptr(dX, torch.float32, (M, K), "dX"), _ptr(gq, torch.float32, (K, N), "gq"),
                                        _ptr(sgrad, torch.float32, (N,), "sgrad"), M, K, N, _stream(stream)),
            "tern_linear_bwd_noalloc")
+
+
+def _layers(layers, backward):
+    """ctypes array of tern_layer from dicts with keys X, tiles, scale and Y (forward) or
+    X, dY, tiles, scale, dX, gq, sgrad (backward; dX, gq, sgrad may be None).  The
+    second value keeps the tern_tiles structs alive while the array is in use."""
+    arr = (_Layer * len(layers))()
+    keep = []
+    for i, L in enumerate(layers):
+        X, tiles = L["X"], L["tiles"]
+        M, K = X.shape
+        N = tiles.N
+        ct = tiles._c()
+        keep.append(ct)
+        c = arr[i]
+        c.X = _ptr(X, torch.bfloat16, (M, K), "X")
+        c.W = ctypes.pointer(ct)
+        c.scale = _ptr(L["scale"], torch.float32, (N,), "scale")
+        c.M, c.K, c.N = M, K, N
+        if backward:
+            c.dY = _ptr(L["dY"], torch.bfloat16, (M, N), "dY")
+            c.dX = _ptr(L.get("dX"), torch.float32, (M, K), "dX")
+            c.gq = _ptr(L.get("gq"), torch.float32, (K, N), "gq")
+            c.sgrad = _ptr(L.get("sgrad"), torch.float32, (N,), "sgrad")
+        else:
+            c.Y = _ptr(L["Y"], torch.float32, (M, N), "Y")
+    return arr, keep
+
+
+def tern_linear_fwd_grouped(layers, stream=None):
+    """Y = X * W_eff for every layer (dicts with X, tiles, scale, Y), in grouped launches."""
+    arr, _keep = _layers(layers, False)
+    _check(lib.tern_linear_fwd_grouped(arr, len(layers), _stream(stream)), "tern_linear_fwd_grouped")
+
+
+def tern_linear_bwd_grouped_workspace(shapes) -> int:
+    """Workspace bytes of tern_linear_bwd_grouped for layers of these (M, K, N) shapes."""
+    arr = (_Layer * len(shapes))()
+    for i, (M, K, N) in enumerate(shapes):
+        arr[i].M, arr[i].K, arr[i].N = int(M), int(K), int(N)
+    return int(lib.tern_linear_bwd_grouped_workspace(arr, len(shapes)))
+
+
+def tern_linear_bwd_grouped(layers, workspace, stream=None, accumulate=False):
+    """dX, gq and sgrad for every layer (dicts with X, dY, tiles, scale, dX, gq, sgrad)."""
+    arr, _keep = _layers(layers, True)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib.tern_linear_bwd_grouped(arr, len(layers), _ptr(workspace, workspace.dtype, None, "workspace"),
+                                       ws_bytes, TERN_BWD_ACCUMULATE if accumulate else 0, _stream(stream)),
+           "tern_linear_bwd_grouped")
 
 
 def adamw_step(w, g, m, v, t, lr, b1, b2, eps, wd, gmul=1.0, decoupled=True, stream=None):

@@ -31,8 +31,10 @@
 // TERN_ERR_TIMEOUT in g_gemm_status, raises a CTA-wide abort flag, waits (again
 // bounded) for its own TMA copies and MMAs in flight, frees TMEM and returns.
 #include <algorithm>
+#include <cmath>
 #include <mutex>
 #include <type_traits>
+#include <vector>
 
 #include "common.cuh"
 
@@ -63,6 +65,26 @@ struct GemmArgs {
     int tile_begin, num_units, split, kb_per;
     float* partial_g;
 };
+
+// Up to G independent problems in one launch: their work units are concatenated
+// (problem p owns units [unit_begin[p], unit_begin[p+1])) and each carries its
+// own tensor maps and arguments.  A single problem is a group of one.
+template <int G>
+struct GemmGroup {
+    CUtensorMap mA[G];
+    CUtensorMap mB0[G];
+    CUtensorMap mB1[G];
+    GemmArgs args[G];
+    int unit_begin[G + 1];
+    int count;
+};
+
+template <int G>
+__device__ __forceinline__ int group_find(const GemmGroup<G>& g, int unit) {
+    int p = 0;
+    while (p + 1 < g.count && unit >= g.unit_begin[p + 1]) ++p;
+    return p;
+}
 
 // CG CTAs (1, or a 2-CTA cluster) share one MMA of M = 128*CG rows by N = BN columns.
 // Each CTA loads its 128 rows of A and BN/CG rows of B per k-block of BK, and its
@@ -237,10 +259,10 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const uint32_t
     }
 }
 
-template <class C>
-__device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensorMap* tmB0,
-                                          const CUtensorMap* tmB1, const GemmArgs& a) {
+template <class C, int G>
+__device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
     constexpr int CG = C::CG;
+    const int total_units = grp.unit_begin[grp.count];
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -290,13 +312,21 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
     uint32_t issued = 0, issued_parity = 0;   // producer: stages with a copy issued, and its phase
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------------------ TMA producer
-        ptx::tma_prefetch_desc(tmA);
-        ptx::tma_prefetch_desc(tmB0);
-        if (C::NB == 2) ptx::tma_prefetch_desc(tmB1);
+        for (int p = 0; p < grp.count; ++p) {
+            ptx::tma_prefetch_desc(&grp.mA[p]);
+            ptx::tma_prefetch_desc(&grp.mB0[p]);
+            if (C::NB == 2) ptx::tma_prefetch_desc(&grp.mB1[p]);
+        }
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        for (int u = unit; ok && u < a.num_units; u += units) {
+        for (int ug = unit; ok && ug < total_units; ug += units) {
+            const int p = group_find(grp, ug);
+            const GemmArgs& a = grp.args[p];
+            const int u = ug - grp.unit_begin[p];
+            const CUtensorMap* tmA = &grp.mA[p];
+            const CUtensorMap* tmB0 = &grp.mB0[p];
+            const CUtensorMap* tmB1 = &grp.mB1[p];
             int mt, nt;
             tile_coords<16 / CG>(a.tile_begin + u / a.split, a.tiles_m, a.tiles_n, mt, nt);
             const int arow = mt * C::TILE_M + static_cast<int>(rank) * kBM;
@@ -358,7 +388,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
         uint32_t phase = 0;
         bool ok = true;
         int local = 0;
-        for (int u = unit; ok && u < a.num_units; u += units, ++local) {
+        for (int ug = unit; ok && ug < total_units; ug += units, ++local) {
+            const int p = group_find(grp, ug);
+            const GemmArgs& a = grp.args[p];
+            const int u = ug - grp.unit_begin[p];
             const int acc = local & 1;
             const uint32_t acc_parity = (local >> 1) & 1;
             if (!wait_bounded(TEMPTY0 + 8u * acc, acc_parity ^ 1u, abort_flag, true)) break;
@@ -396,7 +429,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
         const int quad = warp & 3;   // a warp may touch TMEM lanes 32*(warp%4) .. +31
         const uint32_t tempty_leader = CG == 2 ? ptx::mapa_shared(TEMPTY0, 0) : TEMPTY0;
         int local = 0;
-        for (int u = unit; u < a.num_units; u += units, ++local) {
+        for (int ug = unit; ug < total_units; ug += units, ++local) {
+            const int p = group_find(grp, ug);
+            const GemmArgs& a = grp.args[p];
+            const int u = ug - grp.unit_begin[p];
             const int acc = local & 1;
             const uint32_t acc_parity = (local >> 1) & 1;
             if (!wait_bounded(TFULL0 + 8u * acc, acc_parity, abort_flag, true)) break;
@@ -465,25 +501,21 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap* tmA, const CUtensor
 
 }  // namespace
 
-template <int CG>
-__global__ void __launch_bounds__(kThreads, 1)
-    tern_fwd_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                  const GemmArgs a) {
-    gemm_body<std::conditional_t<CG == 2, Fwd2, Fwd1>>(&tmA, &tmB, &tmB, a);
+// One launch runs the work units of a group of G problems (G = 1: a single
+// layer); the tensor maps live in the kernel's parameter space.
+template <int CG, int G>
+__global__ void __launch_bounds__(kThreads, 1) tern_fwd_gemm(const __grid_constant__ GemmGroup<G> grp) {
+    gemm_body<std::conditional_t<CG == 2, Fwd2, Fwd1>, G>(grp);
 }
 
-template <int CG>
-__global__ void __launch_bounds__(kThreads, 1)
-    tern_dx_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmBhi,
-                 const __grid_constant__ CUtensorMap tmBlo, const GemmArgs a) {
-    gemm_body<std::conditional_t<CG == 2, Dx2, Dx1>>(&tmA, &tmBhi, &tmBlo, a);
+template <int CG, int G>
+__global__ void __launch_bounds__(kThreads, 1) tern_dx_gemm(const __grid_constant__ GemmGroup<G> grp) {
+    gemm_body<std::conditional_t<CG == 2, Dx2, Dx1>, G>(grp);
 }
 
-template <int CG>
-__global__ void __launch_bounds__(kThreads, 1)
-    tern_dw_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                 const GemmArgs a) {
-    gemm_body<std::conditional_t<CG == 2, Dw2, Dw1>>(&tmA, &tmB, &tmB, a);
+template <int CG, int G>
+__global__ void __launch_bounds__(kThreads, 1) tern_dw_gemm(const __grid_constant__ GemmGroup<G> grp) {
+    gemm_body<std::conditional_t<CG == 2, Dw2, Dw1>, G>(grp);
 }
 
 // Self-test of the bounded wait: one warp waits on an mbarrier that nothing
@@ -521,14 +553,29 @@ __global__ void tern_sgrad_reduce(const float* __restrict__ partial, int nparts,
 // and the sgrad partial of each 32-row group).  One CTA per 32 x 32 block of a
 // tile: warp w takes rows 4w..4w+3 of the block, lane l column l; the eight
 // warps' column sums are added in warp order through shared memory.
-__global__ void __launch_bounds__(256) tern_dw_split_reduce(const GemmArgs a, int tile_m, int tile_n) {
+// The split tiles of up to G problems: problem p owns blocks [block_begin[p], block_begin[p+1]).
+template <int G>
+struct ReduceGroup {
+    GemmArgs args[G];
+    int block_begin[G + 1];
+    int count;
+    int tile_m, tile_n;
+};
+
+template <int G>
+__global__ void __launch_bounds__(256) tern_dw_split_reduce(const __grid_constant__ ReduceGroup<G> grp) {
     ptx::pdl_trigger();
     ptx::pdl_wait();
+    int p = 0;
+    while (p + 1 < grp.count && static_cast<int>(blockIdx.x) >= grp.block_begin[p + 1]) ++p;
+    const GemmArgs& a = grp.args[p];
+    const int block = static_cast<int>(blockIdx.x) - grp.block_begin[p];
+    const int tile_m = grp.tile_m, tile_n = grp.tile_n;
     const int row_groups = tile_m / 32, col_groups = tile_n / 32;
     const int per_tile = row_groups * col_groups;
-    const int j = blockIdx.x / per_tile;                   // tail tile
-    const int rg = (blockIdx.x % per_tile) / col_groups;   // 32-row group within the tile
-    const int cgi = blockIdx.x % col_groups;               // 32-column group within the tile
+    const int j = block / per_tile;                        // split tile
+    const int rg = (block % per_tile) / col_groups;        // 32-row group within the tile
+    const int cgi = block % col_groups;                    // 32-column group within the tile
     int tm, tn;
     if (tile_m == 2 * kBM) tile_coords<8>(a.tile_begin + j, a.tiles_m, a.tiles_n, tm, tn);
     else tile_coords<16>(a.tile_begin + j, a.tiles_m, a.tiles_n, tm, tn);
@@ -637,51 +684,63 @@ GemmArgs make_args(int64_t Mg, int64_t Ng, int64_t Kg) {
     return a;
 }
 
-// Persistent launch: one CTA (or CTA pair) per SM (pair of SMs), at most one per work unit.
-template <class C, class K, class... Maps>
-int launch(K kernel, const GemmArgs& a, int num_sms, cudaStream_t s, const Maps&... maps) {
-    // once per kernel and device: later calls, e.g. under stream capture, only
-    // enqueue the launch
+// Co-resident CTA pairs (or CTAs) of a GEMM kernel: the persistent grid.  Sets
+// the kernel's shared-memory attribute once per device, so later calls (e.g.
+// under stream capture) only enqueue launches.
+template <class C, class K>
+int persistent_units(K kernel, int num_sms, int* units) {
     static std::once_flag once[64];
-    static cudaError_t smem_attr[64];
+    static cudaError_t attr_status[64];
+    static int max_clusters[64];
     int dev = 0;
     TERN_CUDA_TRY(cudaGetDevice(&dev));
     if (dev < 0 || dev >= 64) return TERN_ERR_DEVICE;
     std::call_once(once[dev], [&] {
-        smem_attr[dev] = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        attr_status[dev] = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (attr_status[dev] != cudaSuccess || C::CG == 1) return;
+        cudaLaunchConfig_t cfg{};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2 * (num_sms / 2));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = C::SMEM_BYTES;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        attr_status[dev] = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+        max_clusters[dev] = n > 0 ? n : 1;
     });
-    TERN_CUDA_TRY(smem_attr[dev]);
+    TERN_CUDA_TRY(attr_status[dev]);
+    *units = C::CG == 2 ? max_clusters[dev] : num_sms;
+    return TERN_OK;
+}
+
+// Persistent launch of a problem group: one CTA (or CTA pair) per SM (pair of
+// SMs), at most one per work unit, with programmatic dependent launch.
+template <class C, class K, int G>
+int launch(K kernel, const GemmGroup<G>& grp, int num_sms, cudaStream_t s) {
+    int units = 0;
+    if (int st = persistent_units<C>(kernel, num_sms, &units)) return st;
+    const int total = grp.unit_begin[grp.count];
+    if (total <= 0) return TERN_OK;
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[2];
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = s;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // programmatic dependent launch
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
-    if constexpr (C::CG == 2) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        static int max_clusters[64];   // co-resident CTA pairs of this kernel, per device
-        if (max_clusters[dev] == 0) {
-            cfg.gridDim = dim3(2 * (num_sms / 2));
-            int n = 0;
-            TERN_CUDA_TRY(cudaOccupancyMaxActiveClusters(&n, kernel, &cfg));
-            max_clusters[dev] = n > 0 ? n : 1;
-        }
-        if (a.num_tiles < 0) return max_clusters[dev];   // query: persistent units of this kernel
-        cfg.gridDim = dim3(2 * std::min(a.num_units, max_clusters[dev]));
-        cfg.numAttrs = 2;
-    } else {
-        if (a.num_tiles < 0) return num_sms;
-        cfg.attrs = attr + 1;
-        cfg.numAttrs = 1;
-        cfg.gridDim = dim3(std::min(a.num_units, num_sms));
-    }
-    TERN_CUDA_TRY(cudaLaunchKernelEx(&cfg, kernel, maps..., a));
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = C::CG == 2 ? 2 : 1;
+    cfg.gridDim = dim3(C::CG * std::min(total, units));
+    TERN_CUDA_TRY(cudaLaunchKernelEx(&cfg, kernel, grp));
     return TERN_OK;
 }
 
@@ -693,28 +752,50 @@ bool dims_ok(int64_t M, int64_t K, int64_t N) {
 // A CTA pair per tile once the output has at least two 128-row blocks.
 bool use_pair(int64_t Mg) { return Mg > kBM; }
 
+// Fill problem p of a group with its maps and arguments.
+template <class C, int G>
+int group_set(GemmGroup<G>& g, int p, const void* A, int64_t a_inner, int64_t a_outer, const void* B0,
+              const void* B1, int64_t b_inner, int64_t b_outer, const GemmArgs& a) {
+    if (int st = map_operand<C>(&g.mA[p], A, a_inner, a_outer, C::A_MN, kBM)) return st;
+    if (int st = map_operand<C>(&g.mB0[p], B0, b_inner, b_outer, C::B_MN, C::B_ROWS)) return st;
+    if (B1) {
+        if (int st = map_operand<C>(&g.mB1[p], B1, b_inner, b_outer, C::B_MN, C::B_ROWS)) return st;
+    } else {
+        g.mB1[p] = g.mB0[p];
+    }
+    g.args[p] = a;
+    return TERN_OK;
+}
+
+// Unit ranges of the first `count` problems, from their num_units.
+template <int G>
+void group_close(GemmGroup<G>& g, int count) {
+    g.count = count;
+    g.unit_begin[0] = 0;
+    for (int p = 0; p < count; ++p) g.unit_begin[p + 1] = g.unit_begin[p] + g.args[p].num_units;
+}
+
 template <class C, class K>
 int run_fwd(K kernel, const uint16_t* X, const uint16_t* T, const float* scale, float* Y, int64_t M, int64_t K_,
             int64_t N, int num_sms, cudaStream_t s) {
-    CUtensorMap mA, mB;
-    if (int st = map_operand<C>(&mA, X, K_, M, C::A_MN, kBM)) return st;
-    if (int st = map_operand<C>(&mB, T, N, K_, C::B_MN, C::B_ROWS)) return st;
+    GemmGroup<1> g;
     GemmArgs a = make_args<C>(M, N, K_);
     a.out = Y;
     a.scale = scale;
-    return launch<C>(kernel, a, num_sms, s, mA, mB);
+    if (int st = group_set<C>(g, 0, X, K_, M, T, nullptr, N, K_, a)) return st;
+    group_close(g, 1);
+    return launch<C>(kernel, g, num_sms, s);
 }
 
 template <class C, class K>
 int run_dx(K kernel, const uint16_t* dY, const uint16_t* whi, const uint16_t* wlo, float* dX, int64_t M,
            int64_t K_, int64_t N, int num_sms, cudaStream_t s) {
-    CUtensorMap mA, mHi, mLo;
-    if (int st = map_operand<C>(&mA, dY, N, M, C::A_MN, kBM)) return st;
-    if (int st = map_operand<C>(&mHi, whi, N, K_, C::B_MN, C::B_ROWS)) return st;
-    if (int st = map_operand<C>(&mLo, wlo, N, K_, C::B_MN, C::B_ROWS)) return st;
+    GemmGroup<1> g;
     GemmArgs a = make_args<C>(M, K_, N);
     a.out = dX;
-    return launch<C>(kernel, a, num_sms, s, mA, mHi, mLo);
+    if (int st = group_set<C>(g, 0, dY, N, M, whi, wlo, N, K_, a)) return st;
+    group_close(g, 1);
+    return launch<C>(kernel, g, num_sms, s);
 }
 
 // Largest number of split units the tail of a G launch may use (bounds the workspace).
@@ -731,24 +812,32 @@ int64_t dw_tail_bytes(int64_t M, int64_t K_, int64_t N) {
 // they are; when the last wave would leave units idle and `tail` has room, the
 // remaining tiles are split along the token axis over the idle units and
 // finished by tern_dw_split_reduce.
+template <class C, int G>
+int launch_split_reduce(const ReduceGroup<G>& r, cudaStream_t s) {
+    return launch_pdl(tern_dw_split_reduce<G>, dim3(static_cast<unsigned>(r.block_begin[r.count])), dim3(256), 0, s,
+                      r);
+}
+
+// G = X^T dY with the fused gq / sgrad epilogue.  Whole waves of tiles run as
+// they are; when the last wave would leave units idle and `tail` has room, the
+// remaining tiles are split along the token axis over the idle units and
+// finished by tern_dw_split_reduce.
 template <class C, class K>
 int run_dw(K kernel, const uint16_t* X, const uint16_t* dY, const float* scale, const uint32_t* packed, float* gq,
            float* partial, int accumulate, float* tail, int64_t tail_bytes, int64_t M, int64_t K_, int64_t N,
            int num_sms, cudaStream_t s) {
-    CUtensorMap mA, mB;
-    if (int st = map_operand<C>(&mA, X, K_, M, C::A_MN, kBM)) return st;
-    if (int st = map_operand<C>(&mB, dY, N, M, C::B_MN, C::B_ROWS)) return st;
+    GemmGroup<1> g;
     GemmArgs a = make_args<C>(K_, N, M);
     a.out = gq;
     a.scale = scale;
     a.packed = packed;
     a.partial = partial;
     a.accumulate = accumulate;
+    if (int st = group_set<C>(g, 0, X, K_, M, dY, nullptr, N, M, a)) return st;
     if (tail) {
-        GemmArgs q = a;
-        q.num_tiles = -1;
-        const int units = launch<C>(kernel, q, num_sms, s, mA, mB);   // persistent units (no launch)
-        const int T = a.num_tiles, T0 = units > 0 ? (T / units) * units : T, R = T - T0;
+        int units = 0;
+        if (int st = persistent_units<C>(kernel, num_sms, &units)) return st;
+        const int T = a.num_tiles, T0 = (T / units) * units, R = T - T0;
         int split = R > 0 ? std::min(units / R, a.num_kb) : 1;
         if (split >= 2) {
             const int kb_per = (a.num_kb + split - 1) / split;
@@ -756,23 +845,31 @@ int run_dw(K kernel, const uint16_t* X, const uint16_t* dY, const float* scale, 
             const int64_t need = static_cast<int64_t>(R) * split * C::TILE_M * C::BN * sizeof(float);
             if (need <= tail_bytes) {
                 if (T0 > 0) {
-                    GemmArgs m = a;
-                    m.num_units = T0;
-                    if (int st = launch<C>(kernel, m, num_sms, s, mA, mB)) return st;
+                    g.args[0].num_units = T0;
+                    group_close(g, 1);
+                    if (int st = launch<C>(kernel, g, num_sms, s)) return st;
                 }
-                GemmArgs t = a;
+                GemmArgs& t = g.args[0];
                 t.tile_begin = T0;
                 t.num_units = R * split;
                 t.split = split;
                 t.kb_per = kb_per;
                 t.partial_g = tail;
-                if (int st = launch<C>(kernel, t, num_sms, s, mA, mB)) return st;
-                return launch_pdl(tern_dw_split_reduce, dim3(static_cast<unsigned>(R * (C::TILE_M / 32) * (C::BN / 32))),
-                                  dim3(256), 0, s, t, C::TILE_M, C::BN);
+                group_close(g, 1);
+                if (int st = launch<C>(kernel, g, num_sms, s)) return st;
+                ReduceGroup<1> r;
+                r.args[0] = t;
+                r.count = 1;
+                r.tile_m = C::TILE_M;
+                r.tile_n = C::BN;
+                r.block_begin[0] = 0;
+                r.block_begin[1] = R * (C::TILE_M / 32) * (C::BN / 32);
+                return launch_split_reduce<C>(r, s);
             }
         }
     }
-    return launch<C>(kernel, a, num_sms, s, mA, mB);
+    group_close(g, 1);
+    return launch<C>(kernel, g, num_sms, s);
 }
 
 }  // namespace
@@ -800,8 +897,8 @@ extern "C" int tern_linear_fwd(const uint16_t* X, const tern_tiles* W, const flo
     int num_sms = 0;
     if (int st = check_device(&num_sms)) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (use_pair(M)) return run_fwd<Fwd2>(tern_fwd_gemm<2>, X, W->t_bf16, scale, Y, M, K, N, num_sms, s);
-    return run_fwd<Fwd1>(tern_fwd_gemm<1>, X, W->t_bf16, scale, Y, M, K, N, num_sms, s);
+    if (use_pair(M)) return run_fwd<Fwd2>(tern_fwd_gemm<2, 1>, X, W->t_bf16, scale, Y, M, K, N, num_sms, s);
+    return run_fwd<Fwd1>(tern_fwd_gemm<1, 1>, X, W->t_bf16, scale, Y, M, K, N, num_sms, s);
 }
 
 // sgrad partials: one row per 32-row group of K, rounded up to 256 bytes.
@@ -844,8 +941,8 @@ extern "C" int tern_linear_bwd_ex(const uint16_t* X, const uint16_t* dY, const t
 
     if (dX) {
         const int st = use_pair(M)
-                           ? run_dx<Dx2>(tern_dx_gemm<2>, dY, W->whi_bf16, W->wlo_bf16, dX, M, K, N, num_sms, s)
-                           : run_dx<Dx1>(tern_dx_gemm<1>, dY, W->whi_bf16, W->wlo_bf16, dX, M, K, N, num_sms, s);
+                           ? run_dx<Dx2>(tern_dx_gemm<2, 1>, dY, W->whi_bf16, W->wlo_bf16, dX, M, K, N, num_sms, s)
+                           : run_dx<Dx1>(tern_dx_gemm<1, 1>, dY, W->whi_bf16, W->wlo_bf16, dX, M, K, N, num_sms, s);
         if (st) return st;
     }
     if (gq || sgrad) {
@@ -858,9 +955,9 @@ extern "C" int tern_linear_bwd_ex(const uint16_t* X, const uint16_t* dY, const t
             tail = reinterpret_cast<float*>(static_cast<char*>(workspace) + pb);
             tail_bytes = static_cast<int64_t>(ws_bytes) - pb;
         }
-        const int st = use_pair(K) ? run_dw<Dw2>(tern_dw_gemm<2>, X, dY, scale, W->packed, gq, partial, accumulate,
+        const int st = use_pair(K) ? run_dw<Dw2>(tern_dw_gemm<2, 1>, X, dY, scale, W->packed, gq, partial, accumulate,
                                                  tail, tail_bytes, M, K, N, num_sms, s)
-                                   : run_dw<Dw1>(tern_dw_gemm<1>, X, dY, scale, W->packed, gq, partial, accumulate,
+                                   : run_dw<Dw1>(tern_dw_gemm<1, 1>, X, dY, scale, W->packed, gq, partial, accumulate,
                                                  tail, tail_bytes, M, K, N, num_sms, s);
         if (st) return st;
         if (!sgrad) return TERN_OK;
@@ -876,6 +973,291 @@ extern "C" int tern_linear_bwd(const uint16_t* X, const uint16_t* dY, const tern
                                float* dX, float* gq, float* sgrad, void* workspace, size_t ws_bytes, int64_t M,
                                int64_t K, int64_t N, void* stream) {
     return tern_linear_bwd_ex(X, dY, W, scale, dX, gq, sgrad, workspace, ws_bytes, M, K, N, 0u, stream);
+}
+
+// ===================================================================== grouped calls
+//
+// Several independent layers per call (e.g. the projections of one block): up
+// to kGroup problems share one persistent GEMM launch, so the tiles of small
+// layers fill the GPU together and one layer's epilogue overlaps another's main
+// loop.  Results equal the single-layer calls' up to the order of fp32 sums in
+// the G tiles that are split along the token axis.
+
+namespace tern {
+namespace {
+
+constexpr int kGroup = 8;
+
+int layer_align(const tern_layer& L) {
+    if (L.K % 16 || L.N % 16) return TERN_ERR_ALIGN;
+    const void* ps[] = {L.X, L.dY, L.scale, L.Y, L.dX, L.gq, L.sgrad};
+    for (const void* p : ps)
+        if (p && !aligned16(p)) return TERN_ERR_ALIGN;
+    const void* ws[] = {L.W->packed, L.W->t_bf16, L.W->whi_bf16, L.W->wlo_bf16};
+    for (const void* p : ws)
+        if (p && !aligned16(p)) return TERN_ERR_ALIGN;
+    return TERN_OK;
+}
+
+// Calls fn(idx, n) for the layers selected by `pick`, in order, kGroup at a time,
+// separately for layers whose rows (rows_of) need a CTA pair and those that do not.
+template <class Pick, class Rows, class Fn>
+int for_groups(const tern_layer* L, int count, Pick pick, Rows rows_of, Fn fn) {
+    for (int pair = 1; pair >= 0; --pair) {
+        int idx[kGroup], n = 0;
+        for (int i = 0; i <= count; ++i) {
+            if (i < count && pick(L[i]) && use_pair(rows_of(L[i])) == (pair == 1)) idx[n++] = i;
+            if (n == kGroup || (i == count && n > 0)) {
+                if (int st = fn(pair == 1, idx, n)) return st;
+                n = 0;
+            }
+        }
+    }
+    return TERN_OK;
+}
+
+template <class C, class K>
+int fwd_group(K kernel, const tern_layer* L, const int* idx, int n, int num_sms, cudaStream_t s) {
+    GemmGroup<kGroup> g;
+    for (int i = 0; i < n; ++i) {
+        const tern_layer& l = L[idx[i]];
+        GemmArgs a = make_args<C>(l.M, l.N, l.K);
+        a.out = l.Y;
+        a.scale = l.scale;
+        if (int st = group_set<C>(g, i, l.X, l.K, l.M, l.W->t_bf16, nullptr, l.N, l.K, a)) return st;
+    }
+    group_close(g, n);
+    return launch<C>(kernel, g, num_sms, s);
+}
+
+template <class C, class K>
+int dx_group(K kernel, const tern_layer* L, const int* idx, int n, int num_sms, cudaStream_t s) {
+    GemmGroup<kGroup> g;
+    for (int i = 0; i < n; ++i) {
+        const tern_layer& l = L[idx[i]];
+        GemmArgs a = make_args<C>(l.M, l.K, l.N);
+        a.out = l.dX;
+        if (int st = group_set<C>(g, i, l.dY, l.N, l.M, l.W->whi_bf16, l.W->wlo_bf16, l.N, l.K, a)) return st;
+    }
+    group_close(g, n);
+    return launch<C>(kernel, g, num_sms, s);
+}
+
+// Split factor for a group of G problems with `tiles` tiles in all: the one
+// that minimises waves per slice, every problem keeping at least one k-block
+// per slice and the split units within kMaxTailUnits.
+int group_split(int tiles, int min_kb, int units) {
+    int best = 1;
+    double best_cost = std::ceil(static_cast<double>(tiles) / units);
+    for (int sp = 2; sp <= min_kb && tiles * sp <= kMaxTailUnits; ++sp) {
+        const double cost = std::ceil(static_cast<double>(tiles) * sp / units) / sp;
+        if (cost < best_cost - 1e-9) {
+            best = sp;
+            best_cost = cost;
+        }
+    }
+    return best;
+}
+
+template <class C>
+int64_t group_tail_bytes(const tern_layer* L, const int* idx, int n) {
+    int64_t units = 0;
+    for (int i = 0; i < n; ++i) {
+        const GemmArgs a = make_args<C>(L[idx[i]].K, L[idx[i]].N, L[idx[i]].M);
+        units += static_cast<int64_t>(a.num_tiles) * a.num_kb;
+    }
+    return std::min<int64_t>(kMaxTailUnits, units) * C::TILE_M * C::BN * static_cast<int64_t>(sizeof(float));
+}
+
+// The G GEMMs of a group with the fused gq / sgrad epilogue.  When the group's
+// tiles leave persistent units idle and the workspace has room, every tile is
+// split along the token axis by one factor and the grouped reduce finishes them.
+template <class C, class K>
+int dw_group(K kernel, const tern_layer* L, const int* idx, int n, float* const* partial, float* tail,
+             int64_t tail_bytes, int accumulate, int num_sms, cudaStream_t s) {
+    GemmGroup<kGroup> g;
+    int tiles = 0, min_kb = 1 << 30;
+    for (int i = 0; i < n; ++i) {
+        const tern_layer& l = L[idx[i]];
+        GemmArgs a = make_args<C>(l.K, l.N, l.M);
+        a.out = l.gq;
+        a.scale = l.scale;
+        a.packed = l.W->packed;
+        a.partial = partial[i];
+        a.accumulate = accumulate;
+        if (int st = group_set<C>(g, i, l.X, l.K, l.M, l.dY, nullptr, l.N, l.M, a)) return st;
+        tiles += a.num_tiles;
+        min_kb = std::min(min_kb, a.num_kb);
+    }
+    int units = 0;
+    if (int st = persistent_units<C>(kernel, num_sms, &units)) return st;
+    int split = group_split(tiles, min_kb, units);
+    const int64_t tile_bytes = static_cast<int64_t>(C::TILE_M) * C::BN * static_cast<int64_t>(sizeof(float));
+    if (split >= 2 && static_cast<int64_t>(tiles) * split * tile_bytes > tail_bytes) split = 1;
+    if (split == 1) {
+        group_close(g, n);
+        return launch<C>(kernel, g, num_sms, s);
+    }
+    ReduceGroup<kGroup> r;
+    r.count = n;
+    r.tile_m = C::TILE_M;
+    r.tile_n = C::BN;
+    r.block_begin[0] = 0;
+    int64_t off = 0;
+    for (int i = 0; i < n; ++i) {
+        GemmArgs& a = g.args[i];
+        const int kb_per = (a.num_kb + split - 1) / split;
+        a.split = (a.num_kb + kb_per - 1) / kb_per;   // every slice non-empty
+        a.kb_per = kb_per;
+        a.num_units = a.num_tiles * a.split;
+        a.partial_g = tail + off;
+        off += static_cast<int64_t>(a.num_units) * C::TILE_M * C::BN;
+        r.args[i] = a;
+        r.block_begin[i + 1] = r.block_begin[i] + a.num_tiles * (C::TILE_M / 32) * (C::BN / 32);
+    }
+    group_close(g, n);
+    if (int st = launch<C>(kernel, g, num_sms, s)) return st;
+    return launch_split_reduce<C>(r, s);
+}
+
+// sgrad of up to kGroup layers: each column sums its layer's partial rows in order.
+struct SgradGroup {
+    const float* partial[kGroup];
+    float* sgrad[kGroup];
+    int nparts[kGroup], N[kGroup];
+    int block_begin[kGroup + 1];
+    int count, accumulate;
+};
+
+}  // namespace
+
+__global__ void __launch_bounds__(256) tern_sgrad_reduce_group(const __grid_constant__ SgradGroup g) {
+    ptx::pdl_trigger();
+    ptx::pdl_wait();
+    int p = 0;
+    while (p + 1 < g.count && static_cast<int>(blockIdx.x) >= g.block_begin[p + 1]) ++p;
+    const int c = (static_cast<int>(blockIdx.x) - g.block_begin[p]) * blockDim.x + threadIdx.x;
+    if (c >= g.N[p]) return;
+    float s = 0.0f;
+    for (int i = 0; i < g.nparts[p]; ++i) s += g.partial[p][static_cast<int64_t>(i) * g.N[p] + c];
+    g.sgrad[p][c] = g.accumulate ? g.sgrad[p][c] + s : s;
+}
+
+}  // namespace tern
+
+extern "C" int tern_linear_fwd_grouped(const tern_layer* layers, int count, void* stream) {
+    if (!layers || count < 1) return TERN_ERR_ARG;
+    for (int i = 0; i < count; ++i) {
+        const tern_layer& l = layers[i];
+        if (!l.X || !l.W || !l.W->t_bf16 || !l.scale || !l.Y || !dims_ok(l.M, l.K, l.N)) return TERN_ERR_ARG;
+        if (int st = layer_align(l)) return st;
+    }
+    int num_sms = 0;
+    if (int st = check_device(&num_sms)) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return for_groups(
+        layers, count, [](const tern_layer&) { return true; }, [](const tern_layer& l) { return l.M; },
+        [&](bool pair, const int* idx, int n) {
+            return pair ? fwd_group<Fwd2>(tern_fwd_gemm<2, kGroup>, layers, idx, n, num_sms, s)
+                        : fwd_group<Fwd1>(tern_fwd_gemm<1, kGroup>, layers, idx, n, num_sms, s);
+        });
+}
+
+// Workspace of a grouped backward: every layer's sgrad partials (256-byte
+// rounded, in layer order), then room for the split G tiles of the largest group.
+extern "C" size_t tern_linear_bwd_grouped_workspace(const tern_layer* layers, int count) {
+    if (!layers || count < 1) return 0;
+    int64_t bytes = 0, tail = 0;
+    for (int i = 0; i < count; ++i) {
+        if (!dims_ok(layers[i].M, layers[i].K, layers[i].N)) return 0;
+        bytes += bwd_partials_bytes(layers[i].K, layers[i].N);
+    }
+    for_groups(
+        layers, count, [](const tern_layer&) { return true; }, [](const tern_layer& l) { return l.K; },
+        [&](bool pair, const int* idx, int n) {
+            tail = std::max(tail, pair ? group_tail_bytes<Dw2>(layers, idx, n) : group_tail_bytes<Dw1>(layers, idx, n));
+            return TERN_OK;
+        });
+    return static_cast<size_t>(bytes + tail);
+}
+
+extern "C" int tern_linear_bwd_grouped(const tern_layer* layers, int count, void* workspace, size_t ws_bytes,
+                                       unsigned flags, void* stream) {
+    if (!layers || count < 1) return TERN_ERR_ARG;
+    if (flags & ~static_cast<unsigned>(TERN_BWD_ACCUMULATE)) return TERN_ERR_ARG;
+    const int accumulate = (flags & TERN_BWD_ACCUMULATE) ? 1 : 0;
+    int64_t need = 0;
+    for (int i = 0; i < count; ++i) {
+        const tern_layer& l = layers[i];
+        if (!l.X || !l.dY || !l.W || !l.scale || (!l.dX && !l.gq && !l.sgrad)) return TERN_ERR_ARG;
+        if (l.dX && (!l.W->whi_bf16 || !l.W->wlo_bf16)) return TERN_ERR_ARG;
+        if (l.sgrad && !l.W->packed) return TERN_ERR_ARG;
+        if (!dims_ok(l.M, l.K, l.N)) return TERN_ERR_ARG;
+        if (int st = layer_align(l)) return st;
+        need += bwd_partials_bytes(l.K, l.N);
+    }
+    if (!workspace) return TERN_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return TERN_ERR_ALIGN;
+    if (static_cast<int64_t>(ws_bytes) < need) return TERN_ERR_WORKSPACE;
+    int num_sms = 0;
+    if (int st = check_device(&num_sms)) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* ws = static_cast<char*>(workspace);
+    float* tail = reinterpret_cast<float*>(ws + need);
+    const int64_t tail_bytes = static_cast<int64_t>(ws_bytes) - need;
+
+    // dX of every layer that asks for it
+    if (int st = for_groups(
+            layers, count, [](const tern_layer& l) { return l.dX != nullptr; },
+            [](const tern_layer& l) { return l.M; },
+            [&](bool pair, const int* idx, int n) {
+                return pair ? dx_group<Dx2>(tern_dx_gemm<2, kGroup>, layers, idx, n, num_sms, s)
+                            : dx_group<Dx1>(tern_dx_gemm<1, kGroup>, layers, idx, n, num_sms, s);
+            }))
+        return st;
+
+    // G with the fused gq / sgrad epilogue
+    std::vector<float*> partial(count, nullptr);
+    int64_t off = 0;
+    for (int i = 0; i < count; ++i) {
+        if (layers[i].sgrad) partial[i] = reinterpret_cast<float*>(ws + off);
+        off += bwd_partials_bytes(layers[i].K, layers[i].N);
+    }
+    if (int st = for_groups(
+            layers, count, [](const tern_layer& l) { return l.gq != nullptr || l.sgrad != nullptr; },
+            [](const tern_layer& l) { return l.K; },
+            [&](bool pair, const int* idx, int n) {
+                float* parts[kGroup];
+                for (int k = 0; k < n; ++k) parts[k] = partial[idx[k]];
+                return pair ? dw_group<Dw2>(tern_dw_gemm<2, kGroup>, layers, idx, n, parts, tail, tail_bytes,
+                                            accumulate, num_sms, s)
+                            : dw_group<Dw1>(tern_dw_gemm<1, kGroup>, layers, idx, n, parts, tail, tail_bytes,
+                                            accumulate, num_sms, s);
+            }))
+        return st;
+
+    // sgrad sums
+    SgradGroup sg{};
+    sg.accumulate = accumulate;
+    int n = 0;
+    for (int i = 0; i <= count; ++i) {
+        if (i < count && layers[i].sgrad) {
+            sg.partial[n] = partial[i];
+            sg.sgrad[n] = layers[i].sgrad;
+            sg.nparts[n] = static_cast<int>((layers[i].K + kBM - 1) / kBM) * 4;
+            sg.N[n] = static_cast<int>(layers[i].N);
+            sg.block_begin[n + 1] = sg.block_begin[n] + static_cast<int>((layers[i].N + 255) / 256);
+            ++n;
+        }
+        if (n == kGroup || (i == count && n > 0)) {
+            sg.count = n;
+            if (int st = launch_pdl(tern_sgrad_reduce_group, dim3(static_cast<unsigned>(sg.block_begin[n])),
+                                    dim3(256), 0, s, sg))
+                return st;
+            n = 0;
+        }
+    }
+    return TERN_OK;
 }
 
 // ===================================================================== backward without a workspace

@@ -145,6 +145,48 @@ int tern_linear_bwd_ex(const uint16_t* X, const uint16_t* dY, const tern_tiles* 
                        int64_t K, int64_t N, unsigned flags, void* stream);
 
 /*
+ * Grouped calls: several independent layers (for example the four token-mixing
+ * projections of a block, which read the same input) in one call, so that the
+ * tiles of small layers fill the GPU together.  The paper runs each projection
+ * as its own GEMM (page "train_gpu.cu", the per-layer GEMM calls of the
+ * forward and backward); the grouping is this library's.  One layer:
+ */
+typedef struct tern_layer {
+    const uint16_t* X;    /* [M][K] bf16, device */
+    const uint16_t* dY;   /* [M][N] bf16, device (backward only) */
+    const tern_tiles* W;  /* the layer's tiles: host struct of device pointers */
+    const float* scale;   /* [N] fp32, device */
+    float* Y;             /* [M][N] fp32, device (forward only) */
+    float* dX;            /* [M][K] fp32, device (backward; NULL skips it) */
+    float* gq;            /* [K][N] fp32, device (backward; NULL skips it) */
+    float* sgrad;         /* [N] fp32, device (backward; NULL skips it) */
+    int64_t M, K, N;
+} tern_layer;
+
+/*
+ * tern_linear_fwd for every layer of `layers` (host array of count >= 1 layers;
+ * each layer's own shape).  Same rules, errors and results as the single-layer
+ * call, layer by layer; nothing is enqueued if any layer's arguments are bad.
+ * Layers are launched up to eight at a time; a layer's Y must not overlap
+ * another layer's inputs.
+ */
+int tern_linear_fwd_grouped(const tern_layer* layers, int count, void* stream);
+
+/*
+ * tern_linear_bwd_ex for every layer.  One workspace (device, 16-byte aligned,
+ * contents ignored) of at least the sum over layers of the sgrad partials
+ * (each tern_linear_bwd_workspace_min rounded up to 256 bytes) serves all;
+ * tern_linear_bwd_grouped_workspace() bytes (0 on bad shapes) add room for
+ * splitting the G tiles of small layers along the token axis.  dX equals the
+ * single-layer call's; gq and sgrad equal it up to the order of fp32 sums.
+ * flags: 0 or TERN_BWD_ACCUMULATE (every layer).  Errors as tern_linear_bwd_ex;
+ * a NULL workspace is TERN_ERR_WORKSPACE.
+ */
+size_t tern_linear_bwd_grouped_workspace(const tern_layer* layers, int count);
+int tern_linear_bwd_grouped(const tern_layer* layers, int count, void* workspace, size_t ws_bytes,
+                            unsigned flags, void* stream);
+
+/*
  * tern_linear_bwd for callers that cannot allocate device memory.  The paper
  * has no counterpart of this call; it is a convenience of this library.
  *

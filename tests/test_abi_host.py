@@ -129,3 +129,29 @@ def test_noalloc_rejects_sizes_beyond_its_scratch_before_touching_the_device(lib
     assert f(P(0x20000), P(0x21000), ctypes.byref(t), P(0x30000), None, None, P(0x60000),
              1, 4096, 16400, None) == lib.TERN_ERR_SCRATCH_LIMIT
     assert lib.strerror(lib.TERN_ERR_SCRATCH_LIMIT) != "unknown status"
+
+
+def test_grouped_workspace_and_argument_checks(lib):
+    shapes = [(1024, 512, 512)] * 4
+    # sgrad partials of each layer (4 x 128-row blocks x 4 quarters x 512 columns), then
+    # 128 split tiles of 256 x 256 fp32 (the group has 4 x 4 tiles x 16 k-blocks to split)
+    assert lib.tern_linear_bwd_grouped_workspace(shapes) == 4 * (4 * 4 * 512 * 4) + 128 * 256 * 256 * 4
+    assert lib.tern_linear_bwd_grouped_workspace([(0, 512, 512)]) == 0
+    t = _tiles(lib)
+    arr = (lib._Layer * 2)()
+    for i in range(2):
+        arr[i] = lib._Layer(P(0x20000), P(0x21000), ctypes.pointer(t), P(0x30000), P(0x40000), P(0x41000),
+                            P(0x50000), P(0x60000), 64, 128, 128)
+    f, b = lib.lib.tern_linear_fwd_grouped, lib.lib.tern_linear_bwd_grouped
+    assert f(arr, 0, None) == lib.TERN_ERR_ARG
+    assert f(None, 1, None) == lib.TERN_ERR_ARG
+    arr[1].X = P(0x20002)
+    assert f(arr, 2, None) == lib.TERN_ERR_ALIGN
+    assert b(arr, 2, P(0x70000), 1 << 20, 0, None) == lib.TERN_ERR_ALIGN
+    arr[1].X = P(0x20000)
+    arr[1].K = 8
+    assert f(arr, 2, None) == lib.TERN_ERR_ARG
+    arr[1].K = 128
+    assert b(arr, 2, None, 0, 0, None) == lib.TERN_ERR_WORKSPACE
+    assert b(arr, 2, P(0x70000), 100, 0, None) == lib.TERN_ERR_WORKSPACE
+    assert b(arr, 2, P(0x70000), 1 << 20, 4, None) == lib.TERN_ERR_ARG     # unknown flag

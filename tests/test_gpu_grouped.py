@@ -1,0 +1,133 @@
+"""Grouped forward/backward (several independent layers per call) against the
+oracle, layer by layer; Y and dX also bit-equal to the single-layer calls (the
+same tiles, k-order and epilogue), gq and sgrad within the oracle tolerance
+(their split G tiles may sum in another order)."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import tern_synth as syn
+from _parity import Layer, full_oracle_check
+
+pytestmark = pytest.mark.gpu
+
+# (M, K, N): single-CTA and CTA-pair tiles in both GEMM orientations, ragged edges
+MIXED = [(300, 256, 384), (64, 144, 272), (1000, 512, 512), (257, 128, 1008), (8, 64, 48), (777, 128, 512),
+         (129, 384, 256), (100, 256, 384), (513, 1024, 160), (2, 2048, 64)]
+
+
+def _layers(shapes, seed0):
+    out = []
+    for i, (M, K, N) in enumerate(shapes):
+        L = Layer(syn.linear_inputs(M, K, N, seed=seed0 + i))
+        L.bl.tern_materialize(L.q, L.scale, L.tiles, 2, 7)
+        out.append(L)
+    return out
+
+
+def _fwd_dicts(layers):
+    return [dict(X=L.X, tiles=L.tiles, scale=L.scale, Y=L.Y) for L in layers]
+
+
+def _bwd_dicts(layers):
+    return [dict(X=L.X, dY=L.dY, tiles=L.tiles, scale=L.scale, dX=L.dX, gq=L.gq, sgrad=L.sgrad) for L in layers]
+
+
+def _workspace(bl, layers, full=True):
+    shapes = [(L.M, L.K, L.N) for L in layers]
+    if full:
+        nbytes = bl.tern_linear_bwd_grouped_workspace(shapes)
+    else:   # the sgrad partials alone: no room to split G tiles
+        nbytes = sum((bl.tern_linear_bwd_workspace_min(*s) + 255) // 256 * 256 for s in shapes)
+    assert nbytes > 0
+    return torch.full((nbytes // 4,), float("nan"), device="cuda")
+
+
+@pytest.mark.parametrize("full_ws", [True, False])
+def test_grouped_matches_oracle_and_single_calls(cuda_lib, full_ws):
+    bl = cuda_lib
+    layers = _layers(MIXED, 200)
+    bl.tern_linear_fwd_grouped(_fwd_dicts(layers))
+    bl.tern_linear_bwd_grouped(_bwd_dicts(layers), _workspace(bl, layers, full_ws))
+    assert bl.tern_device_status() == bl.TERN_OK
+    for L in layers:
+        full_oracle_check(L)
+    for L in layers:   # the single-layer calls give the same Y and dX bits
+        Y1 = torch.empty_like(L.Y)
+        dX1 = torch.empty_like(L.dX)
+        bl.tern_linear_fwd(L.X, L.tiles, L.scale, Y1)
+        bl.tern_linear_bwd(L.X, L.dY, L.tiles, L.scale, dX1, None, None, None)
+        torch.cuda.synchronize()
+        assert torch.equal(Y1, L.Y), (L.M, L.K, L.N)
+        assert torch.equal(dX1, L.dX), (L.M, L.K, L.N)
+
+
+def test_block_projections(cuda_lib):
+    """Four square projections of one block's width and its two channel-mixing
+    layers, as one grouped call each way, at 1024 tokens."""
+    bl = cuda_lib
+    layers = _layers([(1024, K, N) for K, N in syn.RWKV_SHAPES], 300)
+    bl.tern_linear_fwd_grouped(_fwd_dicts(layers))
+    bl.tern_linear_bwd_grouped(_bwd_dicts(layers), _workspace(bl, layers))
+    assert bl.tern_device_status() == bl.TERN_OK
+    for L in layers:
+        full_oracle_check(L)
+
+
+def test_grouped_accumulate_and_skipped_outputs(cuda_lib):
+    """Two grouped calls with TERN_BWD_ACCUMULATE on the second double gq and
+    sgrad; layers without dX, gq or sgrad leave those buffers untouched."""
+    bl = cuda_lib
+    layers = _layers([(300, 256, 384), (1000, 512, 512), (64, 144, 272)], 400)
+    ref = _layers([(300, 256, 384), (1000, 512, 512), (64, 144, 272)], 400)
+    ws = _workspace(bl, layers)
+    d = _bwd_dicts(layers)
+    bl.tern_linear_bwd_grouped(d, ws)
+    bl.tern_linear_bwd_grouped(d, ws, accumulate=True)
+    bl.tern_linear_bwd_grouped(_bwd_dicts(ref), _workspace(bl, ref))
+    torch.cuda.synchronize()
+    for L, R in zip(layers, ref):
+        torch.testing.assert_close(L.gq, 2 * R.gq, rtol=1e-6, atol=1e-7)
+        torch.testing.assert_close(L.sgrad, 2 * R.sgrad, rtol=1e-5, atol=1e-6)
+    marker = float("nan")
+    for L in layers:
+        L.dX.fill_(marker)
+        L.gq.fill_(marker)
+        L.sgrad.fill_(marker)
+    d = _bwd_dicts(layers)
+    d[0]["dX"] = None
+    d[1]["gq"] = None
+    d[2]["sgrad"] = None
+    bl.tern_linear_bwd_grouped(d, ws)
+    torch.cuda.synchronize()
+    assert torch.isnan(layers[0].dX).all() and torch.isnan(layers[1].gq).all() and torch.isnan(layers[2].sgrad).all()
+    torch.testing.assert_close(layers[0].gq, ref[0].gq, rtol=1e-6, atol=1e-7)
+    torch.testing.assert_close(layers[1].sgrad, ref[1].sgrad, rtol=1e-5, atol=1e-6)
+    torch.testing.assert_close(layers[2].dX, ref[2].dX, rtol=0, atol=0)
+
+
+def test_grouped_argument_errors_enqueue_nothing(cuda_lib):
+    bl = cuda_lib
+    layers = _layers([(64, 64, 64), (96, 128, 64)], 500)
+    for L in layers:
+        L.Y.fill_(7.0)
+    arr, keep = bl._layers(_fwd_dicts(layers), False)
+    arr[1].X = ctypes.c_void_p(layers[1].X.data_ptr() + 2)        # misaligned input in the second layer
+    assert bl.lib.tern_linear_fwd_grouped(arr, 2, None) == bl.TERN_ERR_ALIGN
+    arr[1].X = ctypes.c_void_p(layers[1].X.data_ptr())
+    arr[1].N = 40                                                  # not a multiple of 16
+    assert bl.lib.tern_linear_fwd_grouped(arr, 2, None) == bl.TERN_ERR_ALIGN
+    assert bl.lib.tern_linear_fwd_grouped(arr, 0, None) == bl.TERN_ERR_ARG
+    torch.cuda.synchronize()
+    assert (layers[0].Y == 7.0).all() and (layers[1].Y == 7.0).all()
+    barr, keep2 = bl._layers(_bwd_dicts(layers), True)
+    assert bl.lib.tern_linear_bwd_grouped(barr, 2, None, 0, 0, None) == bl.TERN_ERR_WORKSPACE
+    ws = _workspace(bl, layers, full=False)
+    nb = ws.numel() * 4
+    assert bl.lib.tern_linear_bwd_grouped(barr, 2, ctypes.c_void_p(ws.data_ptr()), nb - 256, 0, None) == \
+        bl.TERN_ERR_WORKSPACE
+    assert bl.lib.tern_linear_bwd_grouped(barr, 2, ctypes.c_void_p(ws.data_ptr()), nb, 2, None) == bl.TERN_ERR_ARG
+    assert bl.lib.tern_linear_bwd_grouped(barr, 2, ctypes.c_void_p(ws.data_ptr()), nb, 0, None) == bl.TERN_OK
+    assert bl.tern_device_status() == bl.TERN_OK
