@@ -51,6 +51,9 @@ WORKLOADS = {
     "hbm_kernels": None,
     # the six projections of the RWKV-style block, M = 8192 (extra line, not the headline)
     "rwkv_block": None,
+    # the two-layer ternary FFN chain, M = 16384: 2048 -> 6144 -> 2048, layer 1's output
+    # rounded to bf16 as layer 2's input (extra line, not the headline)
+    "wide_ffn_chain": None,
 }
 ADAM_HP = dict(lr=1e-3, b1=0.9, b2=0.95, eps=1e-8, wd=0.1)
 
@@ -311,8 +314,15 @@ def rwkv_block(bl, dev, stream, steps):
     reps = max(20, min(steps, 200))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
+    def checked(fn, what):
+        fn()
+        st = bl.tern_device_status()
+        if st != bl.TERN_OK:
+            raise RuntimeError(f"RWKV block, {what}: {bl.strerror(st)}")
+
     def eager(fn):
-        for _ in range(5):
+        checked(fn, "first eager step")
+        for _ in range(4):
             fn()
         torch.cuda.synchronize()
         e0.record(stream)
@@ -329,7 +339,8 @@ def rwkv_block(bl, dev, stream, steps):
         with torch.cuda.graph(g, stream=s2):
             fn()
         torch.cuda.synchronize()
-        for _ in range(3):
+        checked(g.replay, "first graph replay")
+        for _ in range(2):
             g.replay()
         torch.cuda.synchronize()
         e0.record(stream)
@@ -339,10 +350,17 @@ def rwkv_block(bl, dev, stream, steps):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / reps
 
-    progress("RWKV block: per-layer calls")
-    eager_ms, graph_ms = eager(block), graphed(block)
-    progress("RWKV block: grouped calls")
-    geager_ms, ggraph_ms = eager(block_grouped), graphed(block_grouped)
+    progress("RWKV block: per-layer calls, eager")
+    eager_ms = eager(block)
+    progress("RWKV block: per-layer calls, graph")
+    graph_ms = graphed(block)
+    progress("RWKV block: grouped calls, eager")
+    geager_ms = eager(block_grouped)
+    progress("RWKV block: grouped calls, graph")
+    ggraph_ms = graphed(block_grouped)
+    st = bl.tern_device_status()
+    if st != bl.TERN_OK:
+        raise RuntimeError(f"RWKV block: {bl.strerror(st)}")
 
     def rate(ms):
         return {"ms": ms, "tflops": flops / (ms * 1e-3) / 1e12}
@@ -352,6 +370,80 @@ def rwkv_block(bl, dev, stream, steps):
             "eager": rate(eager_ms), "graph": rate(graph_ms),
             "grouped_eager": rate(geager_ms), "grouped_graph": rate(ggraph_ms),
             "launches_per_step_approx": launches}
+
+
+def wide_chain(bl, dev, stream, steps):
+    """Two chained projections, (M, K1, N1) = (16384, 2048, 6144) then (16384, 6144, 2048),
+    40% of q forced to zero: materialise both, fwd 1 writes its output in bf16 only
+    (layer 2's input), fwd 2, bwd 2 writes its input gradient in bf16 only (layer 1's
+    dY), bwd 1, then AdamW of both scales in one launch."""
+    import torch
+    c = syn.WIDE
+    M, K1, N1 = c["M"], c["K"], c["N"]
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    a = syn.linear_inputs(M, K1, N1, seed=3, scale_lo=c["scale_lo"], scale_hi=c["scale_hi"],
+                          zero_prob=c["zero_prob"], tids=(31, 33, 34, 32))
+    b = syn.linear_inputs(M, N1, K1, seed=3, scale_lo=c["scale_lo"], scale_hi=c["scale_hi"],
+                          zero_prob=c["zero_prob"], tids=(41, 43, 44, 42))
+    X = bf(a.X)
+    dY2 = bf(b.dY)
+    q1, q2 = torch.from_numpy(a.q).to(dev), torch.from_numpy(b.q).to(dev)
+    s1, s2 = torch.from_numpy(a.scale).to(dev), torch.from_numpy(b.scale).to(dev)
+    t1, t2 = bl.Tiles.empty(K1, N1, device=dev), bl.Tiles.empty(N1, K1, device=dev)
+    X2 = torch.empty(M, N1, dtype=torch.bfloat16, device=dev)
+    Y2 = torch.empty(M, K1, device=dev)
+    dY1 = torch.empty(M, N1, dtype=torch.bfloat16, device=dev)
+    dX1 = torch.empty(M, K1, device=dev)
+    gq1, gq2 = torch.empty(K1, N1, device=dev), torch.empty(N1, K1, device=dev)
+    sg1, sg2 = torch.empty(N1, device=dev), torch.empty(K1, device=dev)
+    m1, v1, m2, v2 = (torch.zeros(n, device=dev) for n in (N1, N1, K1, K1))
+    ws1 = torch.empty(bl.tern_linear_bwd_grouped_workspace([(M, K1, N1)]) // 4, device=dev)
+    ws2 = torch.empty(bl.tern_linear_bwd_grouped_workspace([(M, N1, K1)]) // 4, device=dev)
+    adam_scalars = torch.tensor([ADAM_HP["lr"], 1 - ADAM_HP["b1"], 1 - ADAM_HP["b2"], 1.0], device=dev)
+    names = ["materialize", "fwd1", "fwd2", "bwd2", "bwd1", "adamw"]
+
+    def step(ev=None):
+        def mark(i):
+            if ev is not None:
+                ev[i].record(stream)
+        mark(0)
+        bl.tern_materialize(q1, s1, t1, 2, 7)
+        bl.tern_materialize(q2, s2, t2, 2, 7)
+        mark(1)
+        bl.tern_linear_fwd_grouped([dict(X=X, tiles=t1, scale=s1, Y_bf16=X2)])
+        mark(2)
+        bl.tern_linear_fwd_grouped([dict(X=X2, tiles=t2, scale=s2, Y=Y2)])
+        mark(3)
+        bl.tern_linear_bwd_grouped([dict(X=X2, dY=dY2, tiles=t2, scale=s2, dX_bf16=dY1, gq=gq2, sgrad=sg2)], ws2)
+        mark(4)
+        bl.tern_linear_bwd_grouped([dict(X=X, dY=dY1, tiles=t1, scale=s1, dX=dX1, gq=gq1, sgrad=sg1)], ws1)
+        mark(5)
+        bl.adamw_step_multi([s1, s2], [sg1, sg2], [m1, m2], [v1, v2], adam_scalars, ADAM_HP["b1"], ADAM_HP["b2"],
+                            ADAM_HP["eps"], ADAM_HP["wd"])
+        mark(6)
+
+    flops = 6.0 * M * (K1 * N1 + N1 * K1)
+    reps = max(10, min(steps, 100))
+    for _ in range(5):
+        step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(reps)]
+    for i in range(reps):
+        step(evs[i])
+    torch.cuda.synchronize()
+    if bl.tern_device_status() != bl.TERN_OK:
+        raise RuntimeError("a kernel gave up on a bounded wait in the FFN chain")
+    ms = evs[0][0].elapsed_time(evs[-1][6]) / reps
+    per = {n: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j, n in enumerate(names)}
+    gemm_flops = {"fwd1": 2.0 * M * K1 * N1, "fwd2": 2.0 * M * K1 * N1, "bwd2": 4.0 * M * K1 * N1,
+                  "bwd1": 4.0 * M * K1 * N1}
+    return {"M": M, "layers": [[K1, N1], [N1, K1]], "q_zero_fraction": c["zero_prob"], "flops_per_step": flops,
+            "ms": ms, "tflops": flops / (ms * 1e-3) / 1e12,
+            "parts_ms": per, "parts_tflops": {n: f / (per[n] * 1e-3) / 1e12 for n, f in gemm_flops.items()},
+            "timing": f"{reps} eager steps, CUDA events on the launching stream"}
 
 
 def graph_bw(torch, fn, nbytes, reps, warm, stream, peak_gbs):
@@ -579,13 +671,15 @@ def run_ours(args):
     if not args.skip_bandwidth and args.workload == "large_single_projection":
         progress("RWKV block")
         extra["rwkv_block"] = rwkv_block(bl, dev, stream, args.steps)
+        progress("wide FFN chain")
+        extra["wide_ffn_chain"] = wide_chain(bl, dev, stream, args.steps)
 
     # ---- end to end through the C ABI: every step's inputs X and dY copied from
     #      pinned host memory and the step's result (updated scales and their
     #      gradient) read back.  The upload of step i+1 runs on a copy stream into
     #      the other of two input buffers while step i computes (double buffering).
     progress("end to end")
-    e2e_steps = min(args.steps, 10)
+    e2e_steps = min(args.steps, 50)
     res_h = torch.empty(2, N, dtype=torch.float32).pin_memory()
     Xb, dYb = [X, torch.empty_like(X)], [dY, torch.empty_like(dY)]
     copy_streams = [torch.cuda.Stream(), torch.cuda.Stream()]   # X and dY on separate copy engines
@@ -671,14 +765,15 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.workload == "hbm_kernels":
         return hbm_kernels(args)
-    if args.workload == "rwkv_block":
+    if args.workload in ("rwkv_block", "wide_ffn_chain"):
         import torch
         torch.cuda.set_device(0)
         import __graft_entry__
         __graft_entry__._builder().build()
         import bit_linear_gb300 as bl
-        out = rwkv_block(bl, torch.device("cuda"), torch.cuda.current_stream(), args.steps)
-        print(json.dumps({"rwkv_block": out}), flush=True)
+        fn = rwkv_block if args.workload == "rwkv_block" else wide_chain
+        out = fn(bl, torch.device("cuda"), torch.cuda.current_stream(), args.steps)
+        print(json.dumps({args.workload: out}), flush=True)
         return 0
     if args.impl == "reference":
         return run_reference(args)

@@ -61,7 +61,8 @@ class _Layer(ctypes.Structure):
     _fields_ = [("X", ctypes.c_void_p), ("dY", ctypes.c_void_p), ("W", ctypes.POINTER(_Tiles)),
                 ("scale", ctypes.c_void_p), ("Y", ctypes.c_void_p), ("dX", ctypes.c_void_p),
                 ("gq", ctypes.c_void_p), ("sgrad", ctypes.c_void_p), ("M", ctypes.c_int64),
-                ("K", ctypes.c_int64), ("N", ctypes.c_int64)]
+                ("K", ctypes.c_int64), ("N", ctypes.c_int64), ("Y_bf16", ctypes.c_void_p),
+                ("dX_bf16", ctypes.c_void_p)]
 
 
 def _load():
@@ -231,9 +232,10 @@ def tern_linear_bwd_noalloc(X, dY, tiles: Tiles, scale, dX, gq, sgrad, stream=No
 
 
 def _layers(layers, backward):
-    """ctypes array of tern_layer from dicts with keys X, tiles, scale and Y (forward) or
-    X, dY, tiles, scale, dX, gq, sgrad (backward; dX, gq, sgrad may be None).  The
-    second value keeps the tern_tiles structs alive while the array is in use."""
+    """ctypes array of tern_layer from dicts with keys X, tiles, scale and Y and/or Y_bf16
+    (forward) or X, dY, tiles, scale and any of dX, dX_bf16, gq, sgrad (backward); a
+    missing or None output is skipped.  The second value keeps the tern_tiles structs
+    alive while the array is in use."""
     arr = (_Layer * len(layers))()
     keep = []
     for i, L in enumerate(layers):
@@ -250,15 +252,17 @@ def _layers(layers, backward):
         if backward:
             c.dY = _ptr(L["dY"], torch.bfloat16, (M, N), "dY")
             c.dX = _ptr(L.get("dX"), torch.float32, (M, K), "dX")
+            c.dX_bf16 = _ptr(L.get("dX_bf16"), torch.bfloat16, (M, K), "dX_bf16")
             c.gq = _ptr(L.get("gq"), torch.float32, (K, N), "gq")
             c.sgrad = _ptr(L.get("sgrad"), torch.float32, (N,), "sgrad")
         else:
-            c.Y = _ptr(L["Y"], torch.float32, (M, N), "Y")
+            c.Y = _ptr(L.get("Y"), torch.float32, (M, N), "Y")
+            c.Y_bf16 = _ptr(L.get("Y_bf16"), torch.bfloat16, (M, N), "Y_bf16")
     return arr, keep
 
 
 def tern_linear_fwd_grouped(layers, stream=None):
-    """Y = X * W_eff for every layer (dicts with X, tiles, scale, Y), in grouped launches."""
+    """Y = X * W_eff for every layer (dicts with X, tiles, scale, Y and/or Y_bf16), in grouped launches."""
     arr, _keep = _layers(layers, False)
     _check(lib.tern_linear_fwd_grouped(arr, len(layers), _stream(stream)), "tern_linear_fwd_grouped")
 
@@ -272,7 +276,8 @@ def tern_linear_bwd_grouped_workspace(shapes) -> int:
 
 
 def tern_linear_bwd_grouped(layers, workspace, stream=None, accumulate=False):
-    """dX, gq and sgrad for every layer (dicts with X, dY, tiles, scale, dX, gq, sgrad)."""
+    """dX (fp32 and/or bf16), gq and sgrad for every layer (dicts with X, dY, tiles, scale, dX, dX_bf16,
+    gq, sgrad)."""
     arr, _keep = _layers(layers, True)
     ws_bytes = workspace.numel() * workspace.element_size()
     _check(lib.tern_linear_bwd_grouped(arr, len(layers), _ptr(workspace, workspace.dtype, None, "workspace"),

@@ -36,6 +36,8 @@
 #include <type_traits>
 #include <vector>
 
+#include <cuda_bf16.h>
+
 #include "common.cuh"
 
 namespace tern {
@@ -64,6 +66,7 @@ struct GemmArgs {
     // its raw partial tile to partial_g[u] and tern_dw_split_reduce finishes it.
     int tile_begin, num_units, split, kb_per;
     float* partial_g;
+    uint16_t* out_bf16;       // [Mg][Ng] bf16 (RNE) copy of out, or its only output (EPI_FWD, EPI_DX)
 };
 
 // Up to G independent problems in one launch: their work units are concatenated
@@ -207,33 +210,52 @@ template <class C>
 __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const uint32_t (&r)[32], int row, int c0,
                                                int tile128, int quad, int lane) {
     const bool row_ok = row < a.Mg;
-    if (row_ok && a.out != nullptr) {
-        float* o = a.out + static_cast<int64_t>(row) * a.Ng + c0;
+    if (row_ok && (a.out != nullptr || (C::EPI != EPI_DW && a.out_bf16 != nullptr))) {
+        const int64_t at = static_cast<int64_t>(row) * a.Ng + c0;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             if (c0 + 16 * h < a.Ng) {
+                float4 v[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int j = 16 * h + 4 * q;
-                    float4 v = make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                                           __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+                    v[q] = make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
+                                       __uint_as_float(r[j + 3]));
                     if constexpr (C::EPI != EPI_DX) {
                         const float4 s = __ldg(reinterpret_cast<const float4*>(a.scale + c0 + j));
-                        v.x *= s.x;
-                        v.y *= s.y;
-                        v.z *= s.z;
-                        v.w *= s.w;
+                        v[q].x *= s.x;
+                        v[q].y *= s.y;
+                        v[q].z *= s.z;
+                        v[q].w *= s.w;
                     }
                     if constexpr (C::EPI == EPI_DW) {
                         if (a.accumulate) {   // micro-batch accumulation: add to the stored gq
-                            const float4 old = *reinterpret_cast<const float4*>(o + j);
-                            v.x = old.x + v.x;
-                            v.y = old.y + v.y;
-                            v.z = old.z + v.z;
-                            v.w = old.w + v.w;
+                            const float4 old = *reinterpret_cast<const float4*>(a.out + at + j);
+                            v[q].x = old.x + v[q].x;
+                            v[q].y = old.y + v[q].y;
+                            v[q].z = old.z + v[q].z;
+                            v[q].w = old.w + v[q].w;
                         }
                     }
-                    *reinterpret_cast<float4*>(o + j) = v;
+                }
+                if (a.out != nullptr) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) *reinterpret_cast<float4*>(a.out + at + 16 * h + 4 * q) = v[q];
+                }
+                if constexpr (C::EPI != EPI_DW) {
+                    if (a.out_bf16 != nullptr) {   // 16 columns -> 32 bytes, round to nearest even
+                        uint32_t b[8];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const __nv_bfloat162 lo = __floats2bfloat162_rn(v[q].x, v[q].y);
+                            const __nv_bfloat162 hi = __floats2bfloat162_rn(v[q].z, v[q].w);
+                            b[2 * q] = *reinterpret_cast<const uint32_t*>(&lo);
+                            b[2 * q + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+                        }
+                        uint4* ob = reinterpret_cast<uint4*>(a.out_bf16 + at + 16 * h);
+                        ob[0] = make_uint4(b[0], b[1], b[2], b[3]);
+                        ob[1] = make_uint4(b[4], b[5], b[6], b[7]);
+                    }
                 }
             }
         }
@@ -990,7 +1012,7 @@ constexpr int kGroup = 8;
 
 int layer_align(const tern_layer& L) {
     if (L.K % 16 || L.N % 16) return TERN_ERR_ALIGN;
-    const void* ps[] = {L.X, L.dY, L.scale, L.Y, L.dX, L.gq, L.sgrad};
+    const void* ps[] = {L.X, L.dY, L.scale, L.Y, L.dX, L.gq, L.sgrad, L.Y_bf16, L.dX_bf16};
     for (const void* p : ps)
         if (p && !aligned16(p)) return TERN_ERR_ALIGN;
     const void* ws[] = {L.W->packed, L.W->t_bf16, L.W->whi_bf16, L.W->wlo_bf16};
@@ -1023,6 +1045,7 @@ int fwd_group(K kernel, const tern_layer* L, const int* idx, int n, int num_sms,
         const tern_layer& l = L[idx[i]];
         GemmArgs a = make_args<C>(l.M, l.N, l.K);
         a.out = l.Y;
+        a.out_bf16 = l.Y_bf16;
         a.scale = l.scale;
         if (int st = group_set<C>(g, i, l.X, l.K, l.M, l.W->t_bf16, nullptr, l.N, l.K, a)) return st;
     }
@@ -1037,6 +1060,7 @@ int dx_group(K kernel, const tern_layer* L, const int* idx, int n, int num_sms, 
         const tern_layer& l = L[idx[i]];
         GemmArgs a = make_args<C>(l.M, l.K, l.N);
         a.out = l.dX;
+        a.out_bf16 = l.dX_bf16;
         if (int st = group_set<C>(g, i, l.dY, l.N, l.M, l.W->whi_bf16, l.W->wlo_bf16, l.N, l.K, a)) return st;
     }
     group_close(g, n);
@@ -1149,7 +1173,8 @@ extern "C" int tern_linear_fwd_grouped(const tern_layer* layers, int count, void
     if (!layers || count < 1) return TERN_ERR_ARG;
     for (int i = 0; i < count; ++i) {
         const tern_layer& l = layers[i];
-        if (!l.X || !l.W || !l.W->t_bf16 || !l.scale || !l.Y || !dims_ok(l.M, l.K, l.N)) return TERN_ERR_ARG;
+        if (!l.X || !l.W || !l.W->t_bf16 || !l.scale || (!l.Y && !l.Y_bf16) || !dims_ok(l.M, l.K, l.N))
+            return TERN_ERR_ARG;
         if (int st = layer_align(l)) return st;
     }
     int num_sms = 0;
@@ -1189,8 +1214,9 @@ extern "C" int tern_linear_bwd_grouped(const tern_layer* layers, int count, void
     int64_t need = 0;
     for (int i = 0; i < count; ++i) {
         const tern_layer& l = layers[i];
-        if (!l.X || !l.dY || !l.W || !l.scale || (!l.dX && !l.gq && !l.sgrad)) return TERN_ERR_ARG;
-        if (l.dX && (!l.W->whi_bf16 || !l.W->wlo_bf16)) return TERN_ERR_ARG;
+        const bool dx = l.dX != nullptr || l.dX_bf16 != nullptr;
+        if (!l.X || !l.dY || !l.W || !l.scale || (!dx && !l.gq && !l.sgrad)) return TERN_ERR_ARG;
+        if (dx && (!l.W->whi_bf16 || !l.W->wlo_bf16)) return TERN_ERR_ARG;
         if (l.sgrad && !l.W->packed) return TERN_ERR_ARG;
         if (!dims_ok(l.M, l.K, l.N)) return TERN_ERR_ARG;
         if (int st = layer_align(l)) return st;
@@ -1208,7 +1234,7 @@ extern "C" int tern_linear_bwd_grouped(const tern_layer* layers, int count, void
 
     // dX of every layer that asks for it
     if (int st = for_groups(
-            layers, count, [](const tern_layer& l) { return l.dX != nullptr; },
+            layers, count, [](const tern_layer& l) { return l.dX != nullptr || l.dX_bf16 != nullptr; },
             [](const tern_layer& l) { return l.M; },
             [&](bool pair, const int* idx, int n) {
                 return pair ? dx_group<Dx2>(tern_dx_gemm<2, kGroup>, layers, idx, n, num_sms, s)

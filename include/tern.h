@@ -161,12 +161,17 @@ typedef struct tern_layer {
     float* gq;            /* [K][N] fp32, device (backward; NULL skips it) */
     float* sgrad;         /* [N] fp32, device (backward; NULL skips it) */
     int64_t M, K, N;
+    uint16_t* Y_bf16;     /* [M][N] bf16 (round to nearest even) copy of Y, device, or NULL */
+    uint16_t* dX_bf16;    /* [M][K] bf16 copy of dX, device, or NULL */
 } tern_layer;
 
 /*
  * tern_linear_fwd for every layer of `layers` (host array of count >= 1 layers;
  * each layer's own shape).  Same rules, errors and results as the single-layer
  * call, layer by layer; nothing is enqueued if any layer's arguments are bad.
+ * Y_bf16, when given, receives Y rounded to bf16 from the same epilogue, so the
+ * next layer of a chain reads its input without a separate cast; Y may then be
+ * NULL.
  * Layers are launched up to eight at a time; a layer's Y must not overlap
  * another layer's inputs.
  */
@@ -179,6 +184,8 @@ int tern_linear_fwd_grouped(const tern_layer* layers, int count, void* stream);
  * tern_linear_bwd_grouped_workspace() bytes (0 on bad shapes) add room for
  * splitting the G tiles of small layers along the token axis.  dX equals the
  * single-layer call's; gq and sgrad equal it up to the order of fp32 sums.
+ * dX_bf16 (with or without dX) receives dX rounded to bf16: the dY of the layer
+ * before in a chain.
  * flags: 0 or TERN_BWD_ACCUMULATE (every layer).  Errors as tern_linear_bwd_ex;
  * a NULL workspace is TERN_ERR_WORKSPACE.
  */

@@ -131,3 +131,80 @@ def test_grouped_argument_errors_enqueue_nothing(cuda_lib):
     assert bl.lib.tern_linear_bwd_grouped(barr, 2, ctypes.c_void_p(ws.data_ptr()), nb, 2, None) == bl.TERN_ERR_ARG
     assert bl.lib.tern_linear_bwd_grouped(barr, 2, ctypes.c_void_p(ws.data_ptr()), nb, 0, None) == bl.TERN_OK
     assert bl.tern_device_status() == bl.TERN_OK
+
+
+def _bf16_vs_oracle(name, got_bf16, ref, ref_abs):
+    """A bf16 output is the fp32 result rounded to nearest even: within the GEMM
+    tolerance of the oracle plus the rounding (at most 2^-8 of the value)."""
+    got = got_bf16.float().cpu().numpy().astype(np.float64)
+    tol = 1e-4 * ref_abs
+    bound = tol * (1 + 2.0 ** -8) + 2.0 ** -8 * np.abs(ref)
+    err = np.abs(got - ref)
+    assert np.all(err <= bound), f"{name}: max excess {np.max(err - bound):.3e}"
+
+
+@pytest.mark.parametrize("shapes", [[(300, 256, 384), (1000, 512, 512)], [(64, 144, 272)], [(513, 1024, 160)]])
+def test_bf16_outputs(cuda_lib, shapes):
+    """Y_bf16 and dX_bf16 are the fp32 outputs rounded to nearest even (bit-exact
+    against torch's CPU rounding of the fp32 results of the same call), within
+    tolerance of the oracle, and the same bits when the fp32 output is skipped."""
+    import oracle
+    bl = cuda_lib
+    layers = _layers(shapes, 600)
+    yb = [torch.empty(L.M, L.N, dtype=torch.bfloat16, device="cuda") for L in layers]
+    xb = [torch.empty(L.M, L.K, dtype=torch.bfloat16, device="cuda") for L in layers]
+    f = _fwd_dicts(layers)
+    b = _bwd_dicts(layers)
+    for i in range(len(layers)):
+        f[i]["Y_bf16"] = yb[i]
+        b[i]["dX_bf16"] = xb[i]
+    bl.tern_linear_fwd_grouped(f)
+    bl.tern_linear_bwd_grouped(b, _workspace(bl, layers))
+    assert bl.tern_device_status() == bl.TERN_OK
+    for L, y16, x16 in zip(layers, yb, xb):
+        assert torch.equal(y16.cpu().view(torch.int16), L.Y.cpu().to(torch.bfloat16).view(torch.int16))
+        assert torch.equal(x16.cpu().view(torch.int16), L.dX.cpu().to(torch.bfloat16).view(torch.int16))
+        inp = L.inp
+        Yr, Ya = oracle.fwd(inp.X, inp.q, inp.scale)
+        dXr, dXa = oracle.dx(inp.dY, inp.q, inp.scale)
+        _bf16_vs_oracle("Y_bf16", y16, Yr, Ya)
+        _bf16_vs_oracle("dX_bf16", x16, dXr, dXa)
+    # bf16 only
+    yb2 = [torch.empty_like(t) for t in yb]
+    xb2 = [torch.empty_like(t) for t in xb]
+    f2 = [dict(X=L.X, tiles=L.tiles, scale=L.scale, Y_bf16=t) for L, t in zip(layers, yb2)]
+    b2 = [dict(X=L.X, dY=L.dY, tiles=L.tiles, scale=L.scale, dX_bf16=t) for L, t in zip(layers, xb2)]
+    bl.tern_linear_fwd_grouped(f2)
+    bl.tern_linear_bwd_grouped(b2, _workspace(bl, layers))
+    torch.cuda.synchronize()
+    for t, t2 in zip(yb + xb, yb2 + xb2):
+        assert torch.equal(t.view(torch.int16), t2.view(torch.int16))
+
+
+def test_two_layer_chain_through_bf16(cuda_lib):
+    """Layer 1's Y_bf16 feeds layer 2 and layer 2's dX_bf16 is layer 1's dY: the
+    chain's layer-2 output and layer-1 gradients equal the single calls made on
+    the same bf16 intermediates (the intermediates themselves are checked above)."""
+    bl = cuda_lib
+    M, K1, N1 = 640, 256, 768
+    a = syn.linear_inputs(M, K1, N1, seed=701)
+    b = syn.linear_inputs(M, N1, K1, seed=702)
+    L1, L2 = Layer(a), Layer(b)
+    for L in (L1, L2):
+        bl.tern_materialize(L.q, L.scale, L.tiles, 2, 7)
+    X2 = torch.empty(M, N1, dtype=torch.bfloat16, device="cuda")
+    dY1 = torch.empty(M, N1, dtype=torch.bfloat16, device="cuda")
+    bl.tern_linear_fwd_grouped([dict(X=L1.X, tiles=L1.tiles, scale=L1.scale, Y_bf16=X2)])
+    bl.tern_linear_fwd_grouped([dict(X=X2, tiles=L2.tiles, scale=L2.scale, Y=L2.Y)])
+    bl.tern_linear_bwd_grouped([dict(X=X2, dY=L2.dY, tiles=L2.tiles, scale=L2.scale, dX_bf16=dY1, gq=L2.gq,
+                                     sgrad=L2.sgrad)], _workspace(bl, [L2]))
+    bl.tern_linear_bwd_grouped([dict(X=L1.X, dY=dY1, tiles=L1.tiles, scale=L1.scale, dX=L1.dX, gq=L1.gq,
+                                     sgrad=L1.sgrad)], _workspace(bl, [L1]))
+    assert bl.tern_device_status() == bl.TERN_OK
+    Y2 = torch.empty_like(L2.Y)
+    dX1 = torch.empty_like(L1.dX)
+    bl.tern_linear_fwd(X2, L2.tiles, L2.scale, Y2)
+    bl.tern_linear_bwd(L1.X, dY1, L1.tiles, L1.scale, dX1, None, None, None)
+    torch.cuda.synchronize()
+    assert torch.equal(Y2, L2.Y) and torch.equal(dX1, L1.dX)
+    assert torch.isfinite(L1.gq).all() and torch.isfinite(L2.sgrad).all()
