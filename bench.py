@@ -22,6 +22,7 @@ Under torchrun (N > 1) every rank runs an independent replica of the step
 from __future__ import annotations
 
 import argparse
+import faulthandler
 import hashlib
 import json
 import os
@@ -61,9 +62,50 @@ ADAM_HP = dict(lr=1e-3, b1=0.9, b2=0.95, eps=1e-8, wd=0.1)
 _T0 = time.perf_counter()
 
 
+_PHASE = ["start"]
+
+
 def progress(msg):
     """One line per bench phase on stderr (the JSON line alone goes to stdout)."""
+    _PHASE[0] = msg
     print(f"[bench {time.perf_counter() - _T0:7.1f} s] {msg}", file=sys.stderr, flush=True)
+
+
+class Watchdog:
+    """Ends the process if the extra measurements stall: after `limit_s` it writes
+    every thread's stack to stderr, prints the headline line (when given) with the
+    stalled phase named, and exits.  The process exit releases the GPU context."""
+
+    def __init__(self, limit_s, line, extra=None, diag=None):
+        self.line = line
+        self.extra = extra if extra is not None else {}
+        self.diag = diag
+        self.timer = threading.Timer(limit_s, self._fire, args=(limit_s,))
+        self.timer.daemon = True
+        self.timer.start()
+
+    def _fire(self, limit_s):
+        phase = _PHASE[0]
+        faulthandler.dump_traceback(file=sys.stderr, all_threads=True)
+        reads = []
+        if self.diag is not None:   # device-side records, twice: are GEMM CTAs still finishing?
+            for _ in range(2):
+                try:
+                    reads.append(self.diag())
+                except Exception as e:   # noqa: BLE001 - report whatever the read says
+                    reads.append(str(e))
+                time.sleep(2.0)
+            print(f"[bench] device diagnostics: {reads}", file=sys.stderr, flush=True)
+        progress(f"watchdog: the extra lines did not finish within {limit_s:.0f} s (phase '{phase}')")
+        if self.line is not None:
+            self.line.update(self.extra)
+            self.line["stalled"] = {"phase": phase, "limit_s": limit_s, "device": reads,
+                                    "note": "the headline and e2e were complete; the extra lines were cut"}
+            print(json.dumps(self.line), flush=True)
+        os._exit(0)
+
+    def cancel(self):
+        self.timer.cancel()
 
 
 def peaks():
@@ -527,6 +569,7 @@ def run_ours(args):
     import __graft_entry__
     __graft_entry__._builder().build()
     import bit_linear_gb300 as bl
+    bl.tern_device_diagnostics()   # creates its stream and buffer while the device is healthy
 
     pk = peaks()
     progress(f"generating inputs ({args.workload})")
@@ -627,13 +670,106 @@ def run_ours(args):
             "unit": "TFLOP/s", "frac": kern[dom]["tflops"] / pk["bf16_sus"], "traffic": traffic,
             "peak_kind": f"{pk['src']} sustained bf16 (kernel timed inside a long run of steps)"}
 
+    # ---- end to end through the C ABI: every step's inputs X and dY copied from
+    #      pinned host memory and the step's result (updated scales and their
+    #      gradient) read back.  The upload of step i+1 runs on a copy stream into
+    #      the other of two input buffers while step i computes (double buffering).
+    progress("end to end")
+    e2e_steps = min(args.steps, 50)
+    res_h = torch.empty(2, N, dtype=torch.float32).pin_memory()
+    Xb, dYb = [X, torch.empty_like(X)], [dY, torch.empty_like(dY)]
+    copy_streams = [torch.cuda.Stream(), torch.cuda.Stream()]   # X and dY on separate copy engines
+    copied = [[torch.cuda.Event(), torch.cuda.Event()] for _ in range(2)]
+    consumed = [torch.cuda.Event(), torch.cuda.Event()]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def upload(i):
+        b = i % 2
+        for cs, dst, src, ev in zip(copy_streams, (Xb[b], dYb[b]), (X_h, dY_h), copied[b]):
+            cs.wait_event(consumed[b] if i >= 2 else e0)
+            with torch.cuda.stream(cs):
+                dst.copy_(src, non_blocking=True)
+            ev.record(cs)
+
+    torch.cuda.synchronize()
+    e0.record(stream)
+    upload(0)
+    for i in range(e2e_steps):
+        if i + 1 < e2e_steps:
+            upload(i + 1)
+        b = i % 2
+        for ev in copied[b]:
+            stream.wait_event(ev)
+        step(None, Xb[b], dYb[b])
+        consumed[b].record(stream)
+        res_h[0].copy_(scale, non_blocking=True)
+        res_h[1].copy_(sgrad, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    h2d = X.numel() * 2 + dY.numel() * 2
+    d2h = 2 * N * 4
+    # the host -> device rate alone (X and dY on their two copy streams, no compute):
+    # the end-to-end step is copy-bound when h2d / rate exceeds the device step
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    c0.record(stream)
+    for cs in copy_streams:
+        cs.wait_event(c0)
+    for _ in range(3):
+        for cs, dst, src in zip(copy_streams, (Xb[0], dYb[0]), (X_h, dY_h)):
+            with torch.cuda.stream(cs):
+                dst.copy_(src, non_blocking=True)
+    for cs in copy_streams:
+        done = torch.cuda.Event()
+        done.record(cs)
+        stream.wait_event(done)
+    c1.record(stream)
+    torch.cuda.synchronize()
+    h2d_gbs = 3 * h2d / (c0.elapsed_time(c1) * 1e-3) / 1e9
+    del Xb, dYb
+
+    line = None
+    if rank == 0:
+        cpu = None
+        if ws == 1 and not args.skip_cpu:
+            progress("CPU oracle sample")
+            v, desc, cores = oracle_sample(inp, args.cpu_budget)
+            cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+        csum = clk.summary()
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": args.workload, "M": M, "K": K, "N": N, "theta": 2, "q_clamp": 7,
+                       "step": "materialise + fwd + bwd (dX, gq, sgrad) + AdamW on scale",
+                       "flops_per_step": flops, "l2": "inputs larger than L2 (X 268 MB, dY 805 MB)",
+                       "parallelism": f"replicas x{ws}"},
+            "frac_of_peak": {"measured_burst": value / ws / pk["bf16"], "measured_sustained": value / ws / pk["bf16_sus"],
+                             "spec_2250": value / ws / 2250.0, "peaks": pk["src"]},
+            "roofline": roof,
+            "kernels": kern,
+            "cpu_baseline": cpu,
+            "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12 * ws, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                    "steps": e2e_steps, "inputs": "X, dY uploaded from pinned host memory every step, "
+                                                  "double-buffered on two copy streams",
+                    "h2d_gbs_alone": h2d_gbs, "h2d_ms_per_step_alone": h2d / h2d_gbs / 1e6},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": csum,
+        }
+
+    # The extra lines below run after the headline is complete.  Should one of them
+    # stall, a watchdog prints the headline line with the stalled phase named (and
+    # every thread's stack on stderr) and ends the process.
+    extra = {}
+    dog = Watchdog(args.extras_limit, line if rank == 0 else None, extra, bl.tern_device_diagnostics)
     # ---- AdamW and ternarise bandwidth at their large sizes (separate timed loops)
     def bw_loop(fn, nbytes, reps=10, warm=3):
         # the reps run as one captured CUDA graph: a short kernel (tens of microseconds)
         # would otherwise wait on the host's launch rate between reps
         return graph_bw(torch, fn, nbytes, reps, warm, stream, pk["hbm"])
 
-    extra = {}
     if not args.skip_bandwidth and args.workload == "large_single_projection":
         progress("AdamW and ternarise bandwidth sweeps")
         del Y
@@ -674,75 +810,8 @@ def run_ours(args):
         progress("wide FFN chain")
         extra["wide_ffn_chain"] = wide_chain(bl, dev, stream, args.steps)
 
-    # ---- end to end through the C ABI: every step's inputs X and dY copied from
-    #      pinned host memory and the step's result (updated scales and their
-    #      gradient) read back.  The upload of step i+1 runs on a copy stream into
-    #      the other of two input buffers while step i computes (double buffering).
-    progress("end to end")
-    e2e_steps = min(args.steps, 50)
-    res_h = torch.empty(2, N, dtype=torch.float32).pin_memory()
-    Xb, dYb = [X, torch.empty_like(X)], [dY, torch.empty_like(dY)]
-    copy_streams = [torch.cuda.Stream(), torch.cuda.Stream()]   # X and dY on separate copy engines
-    copied = [[torch.cuda.Event(), torch.cuda.Event()] for _ in range(2)]
-    consumed = [torch.cuda.Event(), torch.cuda.Event()]
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-
-    def upload(i):
-        b = i % 2
-        for cs, dst, src, ev in zip(copy_streams, (Xb[b], dYb[b]), (X_h, dY_h), copied[b]):
-            cs.wait_event(consumed[b] if i >= 2 else e0)
-            with torch.cuda.stream(cs):
-                dst.copy_(src, non_blocking=True)
-            ev.record(cs)
-
-    torch.cuda.synchronize()
-    e0.record(stream)
-    upload(0)
-    for i in range(e2e_steps):
-        if i + 1 < e2e_steps:
-            upload(i + 1)
-        b = i % 2
-        for ev in copied[b]:
-            stream.wait_event(ev)
-        step(None, Xb[b], dYb[b])
-        consumed[b].record(stream)
-        res_h[0].copy_(scale, non_blocking=True)
-        res_h[1].copy_(sgrad, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    h2d = X.numel() * 2 + dY.numel() * 2
-    d2h = 2 * N * 4
-    del Xb, dYb
-
-    line = None
+    dog.cancel()
     if rank == 0:
-        cpu = None
-        if ws == 1 and not args.skip_cpu:
-            progress("CPU oracle sample")
-            v, desc, cores = oracle_sample(inp, args.cpu_budget)
-            cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
-        csum = clk.summary()
-        line = {
-            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": args.workload, "M": M, "K": K, "N": N, "theta": 2, "q_clamp": 7,
-                       "step": "materialise + fwd + bwd (dX, gq, sgrad) + AdamW on scale",
-                       "flops_per_step": flops, "l2": "inputs larger than L2 (X 268 MB, dY 805 MB)",
-                       "parallelism": f"replicas x{ws}"},
-            "frac_of_peak": {"measured_burst": value / ws / pk["bf16"], "measured_sustained": value / ws / pk["bf16_sus"],
-                             "spec_2250": value / ws / 2250.0, "peaks": pk["src"]},
-            "roofline": roof,
-            "kernels": kern,
-            "cpu_baseline": cpu,
-            "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12 * ws, "unit": "TFLOP/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                    "steps": e2e_steps, "inputs": "X, dY uploaded from pinned host memory every step, "
-                                                  "double-buffered on two copy streams"},
-            "gpu_launches": launches_per_step * args.steps,
-            "clocks": csum,
-        }
         line.update(extra)
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -760,6 +829,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of CPU oracle sampling")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-bandwidth", action="store_true")
+    ap.add_argument("--extras-limit", type=float, default=300.0,
+                    help="seconds after which the extra lines (bandwidth sweeps, RWKV block, FFN chain) are cut")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -43,7 +43,7 @@ ABI_SYMBOLS = ("tern_tiles_bytes", "tern_materialize", "tern_linear_fwd", "tern_
                "tern_linear_bwd", "tern_linear_bwd_ex", "tern_linear_bwd_noalloc", "tern_linear_fwd_grouped",
                "tern_linear_bwd_grouped_workspace", "tern_linear_bwd_grouped", "adamw_step", "tern_grad_sumsq_workspace",
                "tern_grad_sumsq", "adamw_step_multi", "tern_sr4_workspace", "tern_sr4_step", "tern_sr4_panel", "tern_strerror",
-               "tern_device_status", "tern_selftest_wait_timeout")
+               "tern_device_status", "tern_device_diagnostics", "tern_selftest_wait_timeout")
 
 
 class TernError(RuntimeError):
@@ -93,6 +93,7 @@ def _load():
         "tern_sr4_panel": ([vp, vp, vp, i64, i64, ci, ci, vp, vp, vp], ci),
         "tern_strerror": ([ci], ctypes.c_char_p),
         "tern_device_status": ([vp, ci], ci),
+        "tern_device_diagnostics": ([ctypes.POINTER(i64), ci], ci),
         "tern_selftest_wait_timeout": ([ctypes.c_uint, vp], ci),
     }
     for name, (args, res) in sigs.items():
@@ -375,6 +376,15 @@ def tern_sr4_panel(q, scale, counts, scale_stats, packed_prev=None, theta=2, q_c
 def tern_device_status(stream=None, clear=True) -> int:
     """Synchronise the stream; TERN_ERR_TIMEOUT if a kernel gave up on a bounded wait."""
     return int(lib.tern_device_status(_stream(stream), 1 if clear else 0))
+
+
+def tern_device_diagnostics(wait_ms=2000) -> dict:
+    """The device-side failure records (see tern.h), read on the library's own
+    non-blocking stream; usable while the caller's streams are stuck."""
+    out = (ctypes.c_int64 * 8)()
+    _check(lib.tern_device_diagnostics(out, int(wait_ms)), "tern_device_diagnostics")
+    return {"status": out[0], "ctas_entered": out[1], "ctas_set_up": out[2], "ctas_exited": out[3],
+            "first_give_up": {"site": out[4], "cta": out[5], "barrier": out[6], "parity": out[7]}}
 
 
 def workspace_for(M, K, N, device="cuda") -> torch.Tensor:

@@ -31,8 +31,11 @@
 // TERN_ERR_TIMEOUT in g_gemm_status, raises a CTA-wide abort flag, waits (again
 // bounded) for its own TMA copies and MMAs in flight, frees TMEM and returns.
 #include <algorithm>
+#include <chrono>
 #include <cmath>
+#include <cstring>
 #include <mutex>
+#include <thread>
 #include <type_traits>
 #include <vector>
 
@@ -43,6 +46,11 @@
 namespace tern {
 
 __device__ int g_gemm_status;
+// Failure diagnostics: GEMM CTAs counted at entry, after their set-up (TMEM
+// allocation, cluster barrier, dependent-launch wait) and at exit, and where the
+// first bounded wait gave up (site code, CTA, barrier's shared-memory address, parity).
+__device__ unsigned long long g_gemm_count[3];   // CTAs entered, past set-up, exited
+__device__ int g_gemm_site[4];
 
 namespace {
 
@@ -170,8 +178,12 @@ __host__ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int 
 
 // Bounded wait on an mbarrier phase.  Returns false on timeout (after recording
 // it) or, when `watch_abort`, once another role has raised the abort flag.
+// Site codes: (epilogue kind + 1) * 100 + CTA group * 10 + role, role 1 producer
+// stage wait, 2 producer tail, 3 MMA accumulator wait, 4 MMA stage wait, 5 MMA
+// drain, 6 MMA tail, 7 epilogue accumulator wait, 8 copies after an abort; 999
+// the self-test.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                             bool watch_abort, uint64_t limit_ns = kWaitLimitNs) {
+                                             bool watch_abort, int site, uint64_t limit_ns = kWaitLimitNs) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer();
     for (uint32_t it = 1;; ++it) {
@@ -181,6 +193,11 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
             if (ptx::globaltimer() - t0 > limit_ns) {
                 *abort_flag = 1;
                 atomicExch(&g_gemm_status, 1);
+                if (atomicCAS(&g_gemm_site[0], 0, site) == 0) {
+                    g_gemm_site[1] = static_cast<int>(blockIdx.x);
+                    g_gemm_site[2] = static_cast<int>(bar);
+                    g_gemm_site[3] = static_cast<int>(parity);
+                }
                 return false;
             }
         }
@@ -284,6 +301,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const uint32_t
 template <class C, int G>
 __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
     constexpr int CG = C::CG;
+    constexpr int SITE = (C::EPI + 1) * 100 + CG * 10;
     const int total_units = grp.unit_begin[grp.count];
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -297,6 +315,7 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
     const uint32_t TFULL0 = bar0 + 16u * C::STAGES, TEMPTY0 = TFULL0 + 16u, DRAIN = TFULL0 + 32u;
 
     ptx::pdl_trigger();
+    if (threadIdx.x == 32) atomicAdd(&g_gemm_count[0], 1ull);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = CG == 2 ? ptx::cluster_ctarank() : 0u;   // 0 = leader of the pair
     const int unit = CG == 2 ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
@@ -330,6 +349,7 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     ptx::pdl_wait();   // the set-up above overlapped the previous kernel; global memory from here on
+    if (threadIdx.x == 32) atomicAdd(&g_gemm_count[1], 1ull);
 
     uint32_t issued = 0, issued_parity = 0;   // producer: stages with a copy issued, and its phase
     if (warp == 0 && lane == 0) {
@@ -355,7 +375,7 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
             const int brow = nt * C::BN + static_cast<int>(rank) * C::B_ROWS;
             const int kb0 = (u % a.split) * a.kb_per, kb1 = min(a.num_kb, kb0 + a.kb_per);
             for (int kb = kb0; kb < kb1; ++kb) {
-                if (!wait_bounded(EMPTY0 + 8u * stage, phase ^ 1u, abort_flag, true)) {
+                if (!wait_bounded(EMPTY0 + 8u * stage, phase ^ 1u, abort_flag, true, SITE + 1)) {
                     ok = false;
                     break;
                 }
@@ -395,6 +415,15 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
                 }
             }
         }
+        // Producer tail: wait until the MMA has released every stage filled above.  The
+        // release is an asynchronous arrival (multicast to both CTAs of a pair) that may
+        // otherwise land after this CTA has exited, in the barriers of the next kernel's
+        // CTA on this SM (with programmatic dependent launch it is placed at once).
+        if (ok) {
+            for (int s = 0; s < C::STAGES; ++s)
+                if (issued & (1u << s))
+                    wait_bounded(EMPTY0 + 8u * s, (issued_parity >> s) & 1u, abort_flag, true, SITE + 2);
+        }
     } else if (warp == 1 && lane == 0 && rank == 0) {
         // ------------------------------------------------------------ MMA issuer (leader only)
         constexpr uint32_t IDESC = make_idesc(C::TILE_M, C::BN, C::A_MN, C::B_MN);
@@ -416,12 +445,12 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
             const int u = ug - grp.unit_begin[p];
             const int acc = local & 1;
             const uint32_t acc_parity = (local >> 1) & 1;
-            if (!wait_bounded(TEMPTY0 + 8u * acc, acc_parity ^ 1u, abort_flag, true)) break;
+            if (!wait_bounded(TEMPTY0 + 8u * acc, acc_parity ^ 1u, abort_flag, true, SITE + 3)) break;
             ptx::tc_fence_after();
             const uint32_t d_tmem = tmem_base + acc * C::BN;
             const int kb0 = (u % a.split) * a.kb_per, kb1 = min(a.num_kb, kb0 + a.kb_per);
             for (int kb = kb0; kb < kb1; ++kb) {
-                if (!wait_bounded(FULL0 + 8u * stage, phase, abort_flag, true)) {
+                if (!wait_bounded(FULL0 + 8u * stage, phase, abort_flag, true, SITE + 4)) {
                     ok = false;
                     break;
                 }
@@ -445,7 +474,16 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
         }
         // every MMA this thread issued completes before TMEM and shared memory go away
         if constexpr (CG == 2) ptx::mma_commit_pair(DRAIN); else ptx::mma_commit(DRAIN);
-        wait_bounded(DRAIN, 0, abort_flag, false);
+        wait_bounded(DRAIN, 0, abort_flag, false, SITE + 5);
+        // Accumulator tail: wait for the epilogues' release of the last use of each
+        // accumulator, so that the peer CTA's remote arrivals have landed before exit.
+        if (ok && !*abort_flag) {
+            for (int acc = 0; acc < 2; ++acc) {
+                if (local <= acc) continue;
+                const int last = (local - 1) - (((local - 1) - acc) & 1);   // last unit that used acc
+                wait_bounded(TEMPTY0 + 8u * acc, static_cast<uint32_t>(last >> 1) & 1u, abort_flag, true, SITE + 6);
+            }
+        }
     } else if (warp >= 2) {
         // ------------------------------------------------------------ epilogue
         const int quad = warp & 3;   // a warp may touch TMEM lanes 32*(warp%4) .. +31
@@ -457,7 +495,7 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
             const int u = ug - grp.unit_begin[p];
             const int acc = local & 1;
             const uint32_t acc_parity = (local >> 1) & 1;
-            if (!wait_bounded(TFULL0 + 8u * acc, acc_parity, abort_flag, true)) break;
+            if (!wait_bounded(TFULL0 + 8u * acc, acc_parity, abort_flag, true, SITE + 7)) break;
             ptx::tc_fence_after();
             int mt, nt;
             tile_coords<16 / CG>(a.tile_begin + u / a.split, a.tiles_m, a.tiles_n, mt, nt);
@@ -506,12 +544,14 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
         ptx::tc_fence_after();
         if constexpr (CG == 2) ptx::tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
         else ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
+        if (lane == 0) atomicAdd(&g_gemm_count[2], 1ull);
     }
     if (warp == 0 && lane == 0 && *abort_flag) {
         // after an abort, copies still in flight must land before the CTA's shared memory is released
         if constexpr (CG == 1) {
             for (int s = 0; s < C::STAGES; ++s)
-                if (issued & (1u << s)) wait_bounded(FULL0 + 8u * s, (issued_parity >> s) & 1u, abort_flag, false);
+                if (issued & (1u << s))
+                    wait_bounded(FULL0 + 8u * s, (issued_parity >> s) & 1u, abort_flag, false, SITE + 8);
         } else {
             // a pair's copies complete on the leader's barriers; give them time to land
             const uint64_t t0 = ptx::globaltimer();
@@ -554,7 +594,7 @@ __global__ void tern_wait_selftest(uint64_t limit_ns) {
         ptx::fence_mbar_init();
     }
     __syncthreads();
-    if (threadIdx.x == 0) wait_bounded(ptx::smem_u32(&bar), 0, &abort_flag, false, limit_ns);
+    if (threadIdx.x == 0) wait_bounded(ptx::smem_u32(&bar), 0, &abort_flag, false, 999, limit_ns);
 }
 
 // sgrad[c] = sum over the partial rows in ascending order (deterministic); with
@@ -900,8 +940,9 @@ int gemm_status_read(int clear) {
     int v = 0;
     TERN_CUDA_TRY(cudaMemcpyFromSymbol(&v, g_gemm_status, sizeof(int)));
     if (clear) {
-        const int zero = 0;
-        TERN_CUDA_TRY(cudaMemcpyToSymbol(g_gemm_status, &zero, sizeof(int)));
+        const int zero[4] = {0, 0, 0, 0};
+        TERN_CUDA_TRY(cudaMemcpyToSymbol(g_gemm_status, zero, sizeof(int)));
+        TERN_CUDA_TRY(cudaMemcpyToSymbol(g_gemm_site, zero, sizeof(zero)));
     }
     return v ? TERN_ERR_TIMEOUT : TERN_OK;
 }
@@ -1342,6 +1383,63 @@ extern "C" int tern_linear_bwd_noalloc(const uint16_t* X, const uint16_t* dY, co
     void* scratch = nullptr;
     if (int st = noalloc_scratch(&scratch)) return st;
     return tern_linear_bwd(X, dY, W, scale, dX, gq, sgrad, scratch, TERN_NOALLOC_SCRATCH_BYTES, M, K, N, stream);
+}
+
+// ===================================================================== diagnostics
+//
+// Read while other streams may be stuck: the copy runs on the library's own
+// non-blocking stream into pinned host memory (both created by the first call,
+// which should therefore come while the device is healthy), and the host polls
+// for at most `wait_ms`.
+
+namespace tern {
+namespace {
+
+struct DiagState {
+    std::once_flag once;
+    cudaError_t err = cudaErrorUnknown;
+    cudaStream_t stream = nullptr;
+    unsigned char* host = nullptr;   // pinned: status int at 0, counters at 8, site words at 32
+};
+DiagState g_diag[64];
+
+}  // namespace
+}  // namespace tern
+
+extern "C" int tern_device_diagnostics(int64_t* out, int wait_ms) {
+    if (!out || wait_ms < 0) return TERN_ERR_ARG;
+    int dev = 0;
+    TERN_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return TERN_ERR_DEVICE;
+    DiagState& d = g_diag[dev];
+    std::call_once(d.once, [&d] {
+        d.err = cudaStreamCreateWithFlags(&d.stream, cudaStreamNonBlocking);
+        if (d.err == cudaSuccess) d.err = cudaHostAlloc(reinterpret_cast<void**>(&d.host), 64, cudaHostAllocDefault);
+    });
+    TERN_CUDA_TRY(d.err);
+    // copy-engine reads: they do not need a free SM
+    TERN_CUDA_TRY(cudaMemcpyFromSymbolAsync(d.host, g_gemm_status, sizeof(int), 0, cudaMemcpyDeviceToHost, d.stream));
+    TERN_CUDA_TRY(cudaMemcpyFromSymbolAsync(d.host + 8, g_gemm_count, sizeof(g_gemm_count), 0,
+                                            cudaMemcpyDeviceToHost, d.stream));
+    TERN_CUDA_TRY(cudaMemcpyFromSymbolAsync(d.host + 32, g_gemm_site, sizeof(g_gemm_site), 0,
+                                            cudaMemcpyDeviceToHost, d.stream));
+    for (int t = 0; t <= wait_ms; ++t) {
+        const cudaError_t q = cudaStreamQuery(d.stream);
+        if (q == cudaSuccess) {
+            int st = 0, site[4];
+            unsigned long long cnt[3];
+            std::memcpy(&st, d.host, sizeof(int));
+            std::memcpy(cnt, d.host + 8, sizeof(cnt));
+            std::memcpy(site, d.host + 32, sizeof(site));
+            out[0] = st;
+            for (int i = 0; i < 3; ++i) out[1 + i] = static_cast<int64_t>(cnt[i]);
+            for (int i = 0; i < 4; ++i) out[4 + i] = site[i];
+            return TERN_OK;
+        }
+        if (q != cudaErrorNotReady) return TERN_ERR_CUDA;
+        std::this_thread::sleep_for(std::chrono::milliseconds(1));
+    }
+    return TERN_ERR_TIMEOUT;
 }
 
 extern "C" int tern_selftest_wait_timeout(unsigned limit_us, void* stream) {

@@ -11,8 +11,10 @@
 // dither); a non-finite x_i leaves q_i unchanged.
 //
 // Three launches instead of the page's single-thread scale kernel:
-//   1. tern_sr4_absum     per-CTA fp64 sums of |gq*inv_bs| over fixed contiguous
-//                         slices (deterministic), written to the workspace;
+//   1. tern_sr4_absum     per-CTA sums of |gq*inv_bs| over fixed contiguous slices
+//                         (deterministic): each thread keeps an fp32 sum and the
+//                         exact error of its additions (two-sum), the CTA adds the
+//                         threads' pairs in fp64; written to the workspace;
 //   2. tern_sr4_finalize  one CTA: fixed-order sum, mean, s (fp32);
 //   3. tern_sr4_update    streaming update, 16 weights per thread per iteration
 //                         (16-byte q loads/stores, 4 float4 gq loads).
@@ -46,11 +48,17 @@ struct Sr4Args {
     float* s_out;        // optional copy for the caller
 };
 
-__device__ __forceinline__ int8_t sr4_one(const Sr4Args& a, int8_t q, float g, float s, int64_t i) {
+// Counter of element i: key + (idx_base + i + 1) * G (mod 2^64); consecutive
+// elements step by G.
+__device__ __forceinline__ uint64_t sr4_counter(const Sr4Args& a, int64_t i) {
+    return a.key + static_cast<uint64_t>(a.idx_base + i + 1) * kG;
+}
+
+__device__ __forceinline__ int8_t sr4_one(const Sr4Args& a, int8_t q, float g, float s, uint64_t z) {
     const float x = __fmul_rn(__fmul_rn(g, a.inv_bs), s);
     float u = 0.5f;
     if (a.dither) {
-        const uint64_t d = mix64(a.key + static_cast<uint64_t>(a.idx_base + i + 1) * kG);
+        const uint64_t d = mix64(z);
         u = static_cast<float>(d >> 40) * (1.0f / 16777216.0f);
     }
     const float y = __fadd_rn(x, u);
@@ -63,16 +71,41 @@ __device__ __forceinline__ int8_t sr4_one(const Sr4Args& a, int8_t q, float g, f
 
 }  // namespace
 
+// s + c += x as an unevaluated pair of fp32 values (Knuth's two-sum gives the
+// rounding error of each addition exactly), so a thread's partial sum keeps about
+// twice fp32's precision while the loop runs at fp32 rate.
+__device__ __forceinline__ void two_sum_add(float& s, float& c, float x) {
+    const float t = __fadd_rn(s, x);
+    const float xv = __fsub_rn(t, s);
+    const float sv = __fsub_rn(t, xv);
+    const float e = __fadd_rn(__fsub_rn(s, sv), __fsub_rn(x, xv));
+    s = t;
+    c = __fadd_rn(c, e);
+}
+
 __global__ void __launch_bounds__(256) tern_sr4_absum(const Sr4Args a) {
     ptx::pdl_trigger();
     ptx::pdl_wait();
-    // block b owns the contiguous slice [b*n/B, (b+1)*n/B)
-    const int64_t lo = a.n * blockIdx.x / gridDim.x, hi = a.n * (blockIdx.x + 1) / gridDim.x;
-    double acc = 0.0;
-    for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x)
-        acc += fabs(static_cast<double>(__fmul_rn(a.gq[i], a.inv_bs)));
+    // block b owns the float4 groups [b*n4/B, (b+1)*n4/B); the last block also the
+    // n % 4 trailing elements.  Fixed slicing: the sum order does not depend on the GPU.
+    const int64_t n4 = a.n / 4;
+    const int64_t lo = n4 * blockIdx.x / gridDim.x, hi = n4 * (blockIdx.x + 1) / gridDim.x;
+    const float4* g4 = reinterpret_cast<const float4*>(a.gq);
+    float s = 0.0f, c = 0.0f;
+#pragma unroll 4
+    for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x) {
+        const float4 v = __ldg(g4 + i);
+        two_sum_add(s, c, fabsf(__fmul_rn(v.x, a.inv_bs)));
+        two_sum_add(s, c, fabsf(__fmul_rn(v.y, a.inv_bs)));
+        two_sum_add(s, c, fabsf(__fmul_rn(v.z, a.inv_bs)));
+        two_sum_add(s, c, fabsf(__fmul_rn(v.w, a.inv_bs)));
+    }
+    if (blockIdx.x == gridDim.x - 1) {
+        const int64_t t = n4 * 4 + threadIdx.x;
+        if (t < a.n) two_sum_add(s, c, fabsf(__fmul_rn(a.gq[t], a.inv_bs)));
+    }
     __shared__ double red[256];
-    red[threadIdx.x] = acc;
+    red[threadIdx.x] = static_cast<double>(s) + static_cast<double>(c);
     __syncthreads();
     for (int w = 128; w > 0; w >>= 1) {
         if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
@@ -122,12 +155,13 @@ __global__ void __launch_bounds__(256) tern_sr4_update(const Sr4Args a) {
             gv[4 * k + 3] = f.w;
         }
         int8_t* qb = reinterpret_cast<int8_t*>(&qv);
+        uint64_t z = sr4_counter(a, e0);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) qb[j] = sr4_one(a, qb[j], gv[j], s, e0 + j);
+        for (int j = 0; j < 16; ++j, z += kG) qb[j] = sr4_one(a, qb[j], gv[j], s, z);
         *reinterpret_cast<int4*>(a.q + e0) = qv;
     }
     const int64_t t = groups * 16 + tid;   // scalar tail
-    if (t < a.n) a.q[t] = sr4_one(a, a.q[t], a.gq[t], s, t);
+    if (t < a.n) a.q[t] = sr4_one(a, a.q[t], a.gq[t], s, sr4_counter(a, t));
 }
 
 }  // namespace tern

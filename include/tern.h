@@ -314,6 +314,20 @@ const char* tern_strerror(int status);
 int tern_device_status(void* stream, int clear);
 
 /*
+ * Failure diagnostics (no counterpart in the paper), readable while other
+ * streams are stuck: copies the device-side records on the library's own
+ * non-blocking stream into pinned host memory and polls for up to `wait_ms`.
+ *   out[0]    the status word (1 when a bounded wait gave up since the last clear)
+ *   out[1..3] GEMM CTAs counted at entry, after set-up and at exit (since load)
+ *   out[4..7] the first give-up since the last clear: site code ((epilogue kind
+ *             + 1) * 100 + CTA group * 10 + role), CTA index, the barrier's
+ *             shared-memory address and the parity waited for; zeros when none
+ * The first call creates the stream and the 64-byte pinned buffer; make it while
+ * the device is healthy.  TERN_ERR_TIMEOUT when the copies did not finish in time.
+ */
+int tern_device_diagnostics(int64_t* out, int wait_ms);
+
+/*
  * Self-test of failure detection (no counterpart in the paper): enqueue one
  * kernel that waits, with the GEMMs' bounded-wait routine and a limit of
  * limit_us microseconds (1..2e6), on an mbarrier nothing arrives on.  It gives

@@ -58,3 +58,31 @@ def test_bench_rejects_too_few_warmups(bad):
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", *bad],
                        capture_output=True, text=True, timeout=60)
     assert r.returncode != 0
+
+
+def test_watchdog_prints_the_headline_and_exits_when_the_extras_stall():
+    import json
+    import subprocess
+    import sys
+    code = ("import sys, time; sys.path.insert(0, %r); import bench\n"
+            "line = {'metric': 'm', 'value': 1.0}\n"
+            "extra = {'adamw': {'gbs': 2.0}}\n"
+            "bench.progress('RWKV block')\n"
+            "dog = bench.Watchdog(0.3, line, extra)\n"
+            "time.sleep(30)\n") % ROOT
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=20)
+    assert r.returncode == 0
+    out = json.loads(r.stdout.strip().splitlines()[-1])
+    assert out["value"] == 1.0 and out["adamw"] == {"gbs": 2.0}
+    assert out["stalled"]["phase"] == "RWKV block"
+    assert "watchdog" in r.stderr
+
+
+def test_watchdog_cancelled_in_time_stays_silent():
+    import subprocess
+    import sys
+    code = ("import sys, time; sys.path.insert(0, %r); import bench\n"
+            "dog = bench.Watchdog(0.5, {'value': 1.0})\n"
+            "dog.cancel(); time.sleep(1.0); print('done')\n") % ROOT
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=20)
+    assert r.returncode == 0 and r.stdout.strip() == "done"
