@@ -34,7 +34,7 @@ TERN_ERR_SCRATCH_LIMIT = -7
 TERN_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 TERN_TILE_PACKED, TERN_TILE_T, TERN_TILE_WHI, TERN_TILE_WLO = 0, 1, 2, 3
-TERN_ADAM_MAX_TENSORS = 128
+TERN_ADAM_MAX_TENSORS = 64
 TERN_BWD_ACCUMULATE = 1
 
 # the C ABI's exported symbols (tests check the library exports every one)

@@ -154,6 +154,12 @@ struct SumArgs {
     const float* g[TERN_ADAM_MAX_TENSORS];
 };
 
+// Every launch's parameter block stays within 4 KB (the tables above are sized by
+// TERN_ADAM_MAX_TENSORS), so all launches take the same driver path; a launch with
+// a larger block (6 KB at 128 tensors), issued with programmatic dependent launch,
+// was the one launch of that kind in a chain that stopped making progress.
+static_assert(sizeof(MultiArgs) <= 4096 && sizeof(SumArgs) <= 4096, "kernel parameter block over 4 KB");
+
 template <class A>
 __device__ __forceinline__ int chunk_tensor(const A& a, int64_t ch) {
     int lo = 0, hi = a.ntensors - 1;   // last t with first_chunk[t] <= ch

@@ -90,6 +90,8 @@ struct GemmGroup {
     int count;
 };
 
+static_assert(sizeof(GemmGroup<8>) <= 4096, "kernel parameter block over 4 KB");
+
 template <int G>
 __device__ __forceinline__ int group_find(const GemmGroup<G>& g, int unit) {
     int p = 0;
@@ -185,12 +187,19 @@ __host__ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int 
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                              bool watch_abort, int site, uint64_t limit_ns = kWaitLimitNs) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = ptx::globaltimer();
+    // The time waited is the sum of the timer's forward steps between polls, each
+    // counted up to 1 ms: a timer that steps backwards, or jumps forward once, cannot
+    // end a healthy wait.  A poll count backs the bound should the timer stall.
+    uint64_t last = ptx::globaltimer(), waited = 0;
     for (uint32_t it = 1;; ++it) {
         if (ptx::mbar_try_wait(bar, parity)) return true;
         if ((it & 63u) == 0) {
             if (watch_abort && *abort_flag) return false;
-            if (ptx::globaltimer() - t0 > limit_ns) {
+            const uint64_t now = ptx::globaltimer();
+            const int64_t step = static_cast<int64_t>(now - last);
+            last = now;
+            if (step > 0) waited += static_cast<uint64_t>(step < 1000000 ? step : 1000000);
+            if (waited > limit_ns || it >= (1u << 30)) {
                 *abort_flag = 1;
                 atomicExch(&g_gemm_status, 1);
                 if (atomicCAS(&g_gemm_site[0], 0, site) == 0) {
@@ -495,7 +504,9 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
             const int u = ug - grp.unit_begin[p];
             const int acc = local & 1;
             const uint32_t acc_parity = (local >> 1) & 1;
-            if (!wait_bounded(TFULL0 + 8u * acc, acc_parity, abort_flag, true, SITE + 7)) break;
+            // one decision per warp: the loads below are warp-collective
+            const bool full = wait_bounded(TFULL0 + 8u * acc, acc_parity, abort_flag, true, SITE + 7);
+            if (!__all_sync(0xffffffffu, full)) break;
             ptx::tc_fence_after();
             int mt, nt;
             tile_coords<16 / CG>(a.tile_begin + u / a.split, a.tiles_m, a.tiles_n, mt, nt);

@@ -239,7 +239,9 @@ typedef struct tern_adam_scalars {
     float lr, bc1, bc2, gmul;
 } tern_adam_scalars;
 
-#define TERN_ADAM_MAX_TENSORS 128
+/* Tensors per multi-tensor call; more tensors take several calls.  The bound keeps
+ * each launch's parameter block (the per-tensor table) under 4 KB. */
+#define TERN_ADAM_MAX_TENSORS 64
 
 /*
  * Global gradient sum of squares over several tensors, fp64, in a fixed order

@@ -155,3 +155,17 @@ def test_grouped_workspace_and_argument_checks(lib):
     assert b(arr, 2, None, 0, 0, None) == lib.TERN_ERR_WORKSPACE
     assert b(arr, 2, P(0x70000), 100, 0, None) == lib.TERN_ERR_WORKSPACE
     assert b(arr, 2, P(0x70000), 1 << 20, 4, None) == lib.TERN_ERR_ARG     # unknown flag
+
+
+def test_multi_tensor_calls_take_at_most_the_table_size(lib):
+    """adamw_step_multi and tern_grad_sumsq reject more than TERN_ADAM_MAX_TENSORS
+    tensors (the per-tensor table travels in the launch's parameter block)."""
+    k = lib.TERN_ADAM_MAX_TENSORS + 1
+    ptrs = (ctypes.c_void_p * k)(*([0x10000] * k))
+    ns = (ctypes.c_int64 * k)(*([16] * k))
+    f = lib.lib.adamw_step_multi
+    assert f(ptrs, ptrs, ptrs, ptrs, ns, k, P(0x20000), 0.9, 0.95, 1e-8, 0.1, 1, None, 0.0, None, None) == \
+        lib.TERN_ERR_ARG
+    assert lib.lib.tern_grad_sumsq(ptrs, ns, k, P(0x20000), P(0x30000), 1 << 20, None) == lib.TERN_ERR_ARG
+    assert lib.lib.tern_grad_sumsq_workspace(ns, k) == 0
+    assert lib.TERN_ADAM_MAX_TENSORS == 64
