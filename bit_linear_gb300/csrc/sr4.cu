@@ -213,9 +213,9 @@ extern "C" int tern_sr4_step(int8_t* q, const float* gq, int64_t numel, float in
 // theta) and churn (ternary differs from the previous 2-bit tiles), plus the
 // scale's min / mean / max.  The page copies q and scale to the host and loops
 // there; here one streaming pass over q (and the previous packed tiles) counts
-// with byte-SIMD compares, warp sums and one integer atomic per warp and
-// counter (integer sums, so the result does not depend on the order), and one
-// CTA reduces the scale in a fixed order.
+// with byte-SIMD compares (four 16-byte loads in flight per thread), warp sums
+// and one integer atomic per warp and counter (integer sums, so the result does
+// not depend on the order), and one CTA reduces the scale in a fixed order.
 
 namespace tern {
 namespace {
@@ -233,39 +233,66 @@ struct PanelArgs {
 
 }  // namespace
 
+namespace {
+
+// Counts of one 16-weight group (one 16-byte load) into c[0..5].
+__device__ __forceinline__ void panel_group(const PanelArgs& a, const int4 raw, const uint32_t prev, uint32_t (&c)[6]) {
+    const uint32_t w[4] = {static_cast<uint32_t>(raw.x), static_cast<uint32_t>(raw.y), static_cast<uint32_t>(raw.z),
+                           static_cast<uint32_t>(raw.w)};
+    uint32_t code = 0;
+    uint32_t npos = 0, nneg = 0, nrail = 0, ndead = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t pos = __vcmpges4(w[k], a.th_pos);
+        const uint32_t neg = __vcmples4(w[k], a.th_neg);
+        const uint32_t mag = __vabs4(w[k]);             // |q| per byte (-128 stays 0x80, i.e. 128)
+        npos += __popc(pos & 0x01010101u);
+        nneg += __popc(neg & 0x01010101u);
+        nrail += __popc(__vcmpeq4(mag, a.cl) & 0x01010101u);
+        ndead += __popc(__vcmpltu4(mag, a.th_pos) & 0x01010101u);
+        uint32_t x = (pos & 0x01010101u) | (neg & 0x03030303u);
+        x = (x | (x >> 6) | (x >> 12) | (x >> 18)) & 0xFFu;
+        code |= x << (8 * k);
+    }
+    c[0] += nneg;
+    c[1] += 16 - npos - nneg;
+    c[2] += npos;
+    c[3] += nrail;
+    c[4] += ndead;
+    if (a.prev) {
+        const uint32_t d = code ^ prev;
+        c[5] += __popc((d | (d >> 1)) & 0x55555555u);    // 2-bit fields that differ
+    }
+}
+
+}  // namespace
+
+// Four groups per thread per pass, their loads issued before any is used; 32-bit
+// counts per thread (at most 16 per group), 64-bit once per warp.
 __global__ void __launch_bounds__(256) tern_panel_counts(const PanelArgs a) {
     ptx::pdl_trigger();
     ptx::pdl_wait();
-    unsigned long long c[6] = {0, 0, 0, 0, 0, 0};
+    constexpr int U = 4;
+    uint32_t c[6] = {0, 0, 0, 0, 0, 0};
     const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t gi = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; gi < a.groups; gi += nth) {
-        const int4 raw = __ldcs(reinterpret_cast<const int4*>(a.q) + gi);
-        const uint32_t w[4] = {static_cast<uint32_t>(raw.x), static_cast<uint32_t>(raw.y),
-                               static_cast<uint32_t>(raw.z), static_cast<uint32_t>(raw.w)};
-        uint32_t code = 0;
-        int npos = 0, nneg = 0, nrail = 0, ndead = 0;
+    const int4* q4 = reinterpret_cast<const int4*>(a.q);
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; base < a.groups;
+         base += nth * U) {
+        int4 raw[U];
+        uint32_t prev[U];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const uint32_t pos = __vcmpges4(w[k], a.th_pos);
-            const uint32_t neg = __vcmples4(w[k], a.th_neg);
-            const uint32_t mag = __vabs4(w[k]);             // |q| per byte (-128 stays 0x80, i.e. 128)
-            npos += __popc(pos & 0x01010101u);
-            nneg += __popc(neg & 0x01010101u);
-            nrail += __popc(__vcmpeq4(mag, a.cl) & 0x01010101u);
-            ndead += __popc(__vcmpltu4(mag, a.th_pos) & 0x01010101u);
-            uint32_t x = (pos & 0x01010101u) | (neg & 0x03030303u);
-            x = (x | (x >> 6) | (x >> 12) | (x >> 18)) & 0xFFu;
-            code |= x << (8 * k);
+        for (int u = 0; u < U; ++u) {
+            const int64_t gi = base + u * nth;
+            raw[u] = make_int4(0, 0, 0, 0);
+            prev[u] = 0;
+            if (gi < a.groups) {
+                raw[u] = __ldcs(q4 + gi);
+                if (a.prev) prev[u] = __ldcs(a.prev + gi);
+            }
         }
-        c[0] += nneg;
-        c[1] += 16 - npos - nneg;
-        c[2] += npos;
-        c[3] += nrail;
-        c[4] += ndead;
-        if (a.prev) {
-            const uint32_t d = code ^ __ldcs(a.prev + gi);
-            c[5] += __popc((d | (d >> 1)) & 0x55555555u);    // 2-bit fields that differ
-        }
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (base + u * nth < a.groups) panel_group(a, raw[u], prev[u], c);
     }
 #pragma unroll
     for (int k = 0; k < 6; ++k) {
