@@ -54,13 +54,22 @@ __device__ __forceinline__ uint64_t sr4_counter(const Sr4Args& a, int64_t i) {
     return a.key + static_cast<uint64_t>(a.idx_base + i + 1) * kG;
 }
 
+// The top 24 bits of mix64(z): the final xor-shift by 31 does not reach bits
+// 40..63, so they are bits 40..63 of the second product, whose upper 32 bits need
+// one high and two low 32-bit multiplies instead of a full 64-bit product.
+__device__ __forceinline__ uint32_t mix64_top24(uint64_t z) {
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    const uint64_t y = z ^ (z >> 27);
+    constexpr uint32_t c_lo = 0x133111EBu, c_hi = 0x94D049BBu;   // 0x94D049BB133111EB
+    const uint32_t y_lo = static_cast<uint32_t>(y), y_hi = static_cast<uint32_t>(y >> 32);
+    const uint32_t top = __umulhi(y_lo, c_lo) + y_lo * c_hi + y_hi * c_lo;   // bits 32..63 of y * c
+    return top >> 8;
+}
+
 __device__ __forceinline__ int8_t sr4_one(const Sr4Args& a, int8_t q, float g, float s, uint64_t z) {
     const float x = __fmul_rn(__fmul_rn(g, a.inv_bs), s);
     float u = 0.5f;
-    if (a.dither) {
-        const uint64_t d = mix64(z);
-        u = static_cast<float>(d >> 40) * (1.0f / 16777216.0f);
-    }
+    if (a.dither) u = static_cast<float>(mix64_top24(z)) * (1.0f / 16777216.0f);
     const float y = __fadd_rn(x, u);
     if (!isfinite(y)) return q;
     const float f = fminf(fmaxf(floorf(y), -300.0f), 300.0f);
