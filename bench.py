@@ -292,15 +292,24 @@ def run_reference(args):
 
 # --------------------------------------------------------------------------- our arm
 
+def code_hash(src_files):
+    """Hash of the sources' code: comments, trailing blanks and empty lines removed, so
+    that a comment edit does not count as a kernel change."""
+    h = hashlib.sha256()
+    for f in src_files:
+        text = open(f, encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines()]
+        h.update("\n".join(ln for ln in lines if ln).encode())
+    return h.hexdigest()[:16]
+
+
 def traffic_from_profiles(kernel, src_files):
-    """dram bytes per launch committed under profiles/, if the kernel source is unchanged since."""
+    """dram bytes per launch committed under profiles/, if the kernel code is unchanged since."""
     p = os.path.join(ROOT, "profiles", "traffic.md")
     if not os.path.exists(p):
         return None
-    h = hashlib.sha256()
-    for f in src_files:
-        h.update(open(f, "rb").read())
-    digest = h.hexdigest()[:16]
+    digest = code_hash(src_files)
     for ln in open(p):
         m = re.match(r"^\|\s*(\w+)\s*\|\s*([0-9.eE+]+)\s*\|\s*(\w+)\s*\|", ln)
         if m and m.group(1) == kernel and m.group(3) == digest:

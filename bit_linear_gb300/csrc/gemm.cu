@@ -20,16 +20,21 @@
 // the 128-byte (or 64-byte) swizzle that the tcgen05 shared-memory descriptors
 // describe, so no operand is ever transposed in memory.
 //
-// Kernel shape (one CTA per SM, persistent over output tiles of 128 x BN):
+// Kernel shape: persistent, one CTA per SM; outputs of more than 128 rows use CTA
+// pairs (a 2-CTA cluster, cta_group::2) on 256 x BN tiles, smaller ones single
+// CTAs on 128 x BN tiles.  A launch walks the work units of a group of up to 8
+// independent problems (one layer is a group of one).
 //   warp 0     TMA producer (one thread): STAGES-deep ring of operand stages
-//   warp 1     TMEM allocator + MMA issuer (one thread)
+//   warp 1     TMEM allocator + MMA issuer (one thread, the pair's leader)
 //   warps 2-5  epilogue: TMEM -> registers -> global, one TMEM lane quarter each
 // Two TMEM accumulators (2 x BN columns) let the epilogue of tile i overlap the
-// main loop of tile i+1.
+// main loop of tile i+1.  Before exit the producer waits for the release of every
+// stage it filled and the MMA thread for the release of the last accumulators, so
+// no asynchronous arrival lands in shared memory the next kernel's CTA owns.
 //
-// Every mbarrier wait is bounded (globaltimer); on expiry a kernel records
-// TERN_ERR_TIMEOUT in g_gemm_status, raises a CTA-wide abort flag, waits (again
-// bounded) for its own TMA copies and MMAs in flight, frees TMEM and returns.
+// Every mbarrier wait is bounded; on expiry a kernel records TERN_ERR_TIMEOUT in
+// g_gemm_status (and the site in g_gemm_site), raises a CTA-wide abort flag, waits
+// (again bounded) for its own TMA copies and MMAs in flight, frees TMEM and returns.
 #include <algorithm>
 #include <chrono>
 #include <cmath>
