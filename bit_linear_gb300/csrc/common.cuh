@@ -33,7 +33,10 @@ namespace tern {
 // (programmatic dependent launch): the next kernel on the stream may launch while
 // this one finishes, and each kernel waits for its predecessor (ptx::pdl_wait)
 // before it touches global memory.  Launch latency and prologues (barrier set-up,
-// TMEM allocation) then overlap the previous kernel's tail.
+// TMEM allocation) then overlap the previous kernel's tail.  Kernels let their
+// dependents launch (ptx::pdl_trigger) at entry, except the GEMMs, which do so only
+// once their TMEM is allocated: a dependent's block placed on the same SM before
+// that could hold the SM's TMEM allocation permit while it waits for the GEMM.
 template <class... KArgs, class... Args>
 int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args) {
     cudaLaunchConfig_t cfg{};

@@ -328,7 +328,6 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
     const uint32_t FULL0 = bar0, EMPTY0 = bar0 + 8u * C::STAGES;
     const uint32_t TFULL0 = bar0 + 16u * C::STAGES, TEMPTY0 = TFULL0 + 16u, DRAIN = TFULL0 + 32u;
 
-    ptx::pdl_trigger();
     if (threadIdx.x == 32) atomicAdd(&g_gemm_count[0], 1ull);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = CG == 2 ? ptx::cluster_ctarank() : 0u;   // 0 = leader of the pair
@@ -362,6 +361,11 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
     if constexpr (CG == 2) ptx::cluster_sync(); else __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Dependents may launch only now, with TMEM allocated in every CTA of the grid: a
+    // CTA holds the SM's TMEM allocation permit until it relinquishes it or exits, so
+    // a dependent's block placed on this SM earlier (waiting, in its dependent-launch
+    // wait, for this grid to finish) could hold the permit this CTA's allocation needs.
+    ptx::pdl_trigger();
     ptx::pdl_wait();   // the set-up above overlapped the previous kernel; global memory from here on
     if (threadIdx.x == 32) atomicAdd(&g_gemm_count[1], 1ull);
 
@@ -965,6 +969,10 @@ int gemm_status_read(int clear) {
 
 }  // namespace tern
 
+namespace tern {
+int gemm_setup(int num_sms);   // every GEMM kernel configured once per device (below)
+}  // namespace tern
+
 using namespace tern;
 
 extern "C" int tern_linear_fwd(const uint16_t* X, const tern_tiles* W, const float* scale, float* Y, int64_t M,
@@ -975,6 +983,7 @@ extern "C" int tern_linear_fwd(const uint16_t* X, const tern_tiles* W, const flo
     if (!aligned16(X) || !aligned16(W->t_bf16) || !aligned16(scale) || !aligned16(Y)) return TERN_ERR_ALIGN;
     int num_sms = 0;
     if (int st = check_device(&num_sms)) return st;
+    if (int st = gemm_setup(num_sms)) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (use_pair(M)) return run_fwd<Fwd2>(tern_fwd_gemm<2, 1>, X, W->t_bf16, scale, Y, M, K, N, num_sms, s);
     return run_fwd<Fwd1>(tern_fwd_gemm<1, 1>, X, W->t_bf16, scale, Y, M, K, N, num_sms, s);
@@ -1016,6 +1025,7 @@ extern "C" int tern_linear_bwd_ex(const uint16_t* X, const uint16_t* dY, const t
     if (sgrad && (!workspace || ws_bytes < tern_linear_bwd_workspace_min(M, K, N))) return TERN_ERR_WORKSPACE;
     int num_sms = 0;
     if (int st = check_device(&num_sms)) return st;
+    if (int st = gemm_setup(num_sms)) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     if (dX) {
@@ -1236,6 +1246,7 @@ extern "C" int tern_linear_fwd_grouped(const tern_layer* layers, int count, void
     }
     int num_sms = 0;
     if (int st = check_device(&num_sms)) return st;
+    if (int st = gemm_setup(num_sms)) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return for_groups(
         layers, count, [](const tern_layer&) { return true; }, [](const tern_layer& l) { return l.M; },
@@ -1284,6 +1295,7 @@ extern "C" int tern_linear_bwd_grouped(const tern_layer* layers, int count, void
     if (static_cast<int64_t>(ws_bytes) < need) return TERN_ERR_WORKSPACE;
     int num_sms = 0;
     if (int st = check_device(&num_sms)) return st;
+    if (int st = gemm_setup(num_sms)) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char* ws = static_cast<char*>(workspace);
     float* tail = reinterpret_cast<float*>(ws + need);
@@ -1342,6 +1354,51 @@ extern "C" int tern_linear_bwd_grouped(const tern_layer* layers, int count, void
     }
     return TERN_OK;
 }
+
+namespace tern {
+
+// Configure and load every GEMM kernel of the library once per device, before its
+// first launch: the shared-memory attribute, the co-resident cluster count and the
+// kernels' code (cudaFuncGetAttributes loads a lazily loaded kernel).  No kernel is
+// then first used in the middle of a chain of dependent launches or under capture.
+int gemm_setup(int num_sms) {
+    static std::once_flag once[64];
+    static int status[64];
+    int dev = 0;
+    TERN_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return TERN_ERR_DEVICE;
+    std::call_once(once[dev], [&] {
+        static_assert(kGroup == 8, "grouped instantiations below");
+        int st = TERN_OK, u = 0;
+        auto gemm = [&](int r) {
+            if (st == TERN_OK) st = r;
+        };
+        gemm(persistent_units<Fwd1>(tern_fwd_gemm<1, 1>, num_sms, &u));
+        gemm(persistent_units<Fwd2>(tern_fwd_gemm<2, 1>, num_sms, &u));
+        gemm(persistent_units<Dx1>(tern_dx_gemm<1, 1>, num_sms, &u));
+        gemm(persistent_units<Dx2>(tern_dx_gemm<2, 1>, num_sms, &u));
+        gemm(persistent_units<Dw1>(tern_dw_gemm<1, 1>, num_sms, &u));
+        gemm(persistent_units<Dw2>(tern_dw_gemm<2, 1>, num_sms, &u));
+        gemm(persistent_units<Fwd1>(tern_fwd_gemm<1, 8>, num_sms, &u));
+        gemm(persistent_units<Fwd2>(tern_fwd_gemm<2, 8>, num_sms, &u));
+        gemm(persistent_units<Dx1>(tern_dx_gemm<1, 8>, num_sms, &u));
+        gemm(persistent_units<Dx2>(tern_dx_gemm<2, 8>, num_sms, &u));
+        gemm(persistent_units<Dw1>(tern_dw_gemm<1, 8>, num_sms, &u));
+        gemm(persistent_units<Dw2>(tern_dw_gemm<2, 8>, num_sms, &u));
+        cudaFuncAttributes fa;
+        auto load = [&](cudaError_t e) {
+            if (st == TERN_OK && e != cudaSuccess) st = TERN_ERR_CUDA;
+        };
+        load(cudaFuncGetAttributes(&fa, tern_dw_split_reduce<1>));
+        load(cudaFuncGetAttributes(&fa, tern_dw_split_reduce<8>));
+        load(cudaFuncGetAttributes(&fa, tern_sgrad_reduce));
+        load(cudaFuncGetAttributes(&fa, tern_sgrad_reduce_group));
+        status[dev] = st;
+    });
+    return status[dev];
+}
+
+}  // namespace tern
 
 // ===================================================================== backward without a workspace
 //
