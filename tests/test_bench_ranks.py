@@ -86,3 +86,16 @@ def test_watchdog_cancelled_in_time_stays_silent():
             "dog.cancel(); time.sleep(1.0); print('done')\n") % ROOT
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=20)
     assert r.returncode == 0 and r.stdout.strip() == "done"
+
+
+def test_code_hash_ignores_comments_but_not_code(tmp_path):
+    """The traffic figures stay keyed to the GEMM code: a comment edit keeps the
+    key, a code edit changes it."""
+    import bench
+    a = tmp_path / "a.cu"
+    a.write_text("// header\nint f(int x) {  // twice\n    return 2 * x; /* note */\n}\n")
+    h0 = bench.code_hash([str(a)])
+    a.write_text("// another header\n\nint f(int x) {\n    return 2 * x; /* other\n note */\n}\n")
+    assert bench.code_hash([str(a)]) == h0
+    a.write_text("int f(int x) {\n    return 3 * x;\n}\n")
+    assert bench.code_hash([str(a)]) != h0
