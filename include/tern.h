@@ -176,8 +176,8 @@ typedef struct tern_layer {
  * another layer's inputs.
  * Known issue: in a process that had first run long single-layer steps of a large
  * projection, a sequence of eager grouped calls (forward and backward of a block)
- * has stalled, with one CTA pair of a GEMM unable to finish allocating its tensor
- * memory; the same calls in a fresh process have not.  The cause is not known;
+ * has stalled, with one CTA pair of a GEMM unable to finish its set-up (tensor
+ * memory allocation, cluster barrier); the same calls in a fresh process have not.  The cause is not known;
  * tern_device_diagnostics reports the state if it happens.
  */
 int tern_linear_fwd_grouped(const tern_layer* layers, int count, void* stream);
