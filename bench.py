@@ -676,6 +676,8 @@ def run_ours(args):
     for n, f in credited.items():
         kern[n]["tflops"] = f / (per[n] * 1e-3) / 1e12
         kern[n]["frac_of_sustained"] = kern[n]["tflops"] / pk["bf16_sus"]
+    # dX runs two bf16 passes (W_hi and W_lo) into one accumulator: 4*M*K*N executed
+    kern["dx"]["executed_tflops"] = 2.0 * kern["dx"]["tflops"]
     mat_bytes = K * N * (1 + 0.25 + 2 + 2 + 2) + N * 4
     kern["materialize"]["gbs"] = mat_bytes / (per["materialize"] * 1e-3) / 1e9
     dom = max(credited, key=lambda n: per[n])
