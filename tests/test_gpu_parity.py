@@ -152,7 +152,7 @@ def test_full_size_sampled(cuda_lib, name):
         inp = syn.linear_inputs(M, K, N, seed=0 if name == "wide_up" else 1, scale_lo=c["scale_lo"],
                                 scale_hi=c["scale_hi"], zero_prob=c["zero_prob"])
     layer = Layer(inp).run()
-    sampled_oracle_check(layer, n=2048, ncols=24)
+    sampled_oracle_check(layer, n=4096, ncols=64)
 
 
 # ----------------------------------------------------------------- AdamW

@@ -55,6 +55,33 @@ MUTANTS = [
      [S.test_round_half_up_without_dither, lambda: S.test_stochastic_rounding_is_unbiased(0.3)]),
     ("SR4 scale multiplies", "return target_step / mean;", "return target_step * mean;", 0,
      [S.test_scale_sets_the_mean_step]),
+    # the tolerance denominators (sum of |term| of each output's dot product) made too large
+    ("Y abs sum drops |T|", "aab[c] += fabs(term);", "aab[c] += fabs(x);", 0,
+     [lambda: P.test_abs_sums_are_products_of_absolute_values((12, 40, 32), 31)]),
+    ("dX abs sum drops |T|", "sa += fabs(term);",
+     "sa += fabs(dy[c] * (double)a->scale[c]);", 0,
+     [lambda: P.test_abs_sums_are_products_of_absolute_values((12, 40, 32), 31)]),
+    ("dX abs sum counts each term twice", "sa += fabs(term);", "sa += 2.0 * fabs(term);", 0,
+     [P.test_abs_sums_equal_the_outputs_when_every_term_has_one_sign]),
+    ("gq abs sum drops |s|", "if (gqabs) gqabs[r * N + c] = Ga[r * N + c] * fabs(s);",
+     "if (gqabs) gqabs[r * N + c] = Ga[r * N + c];", 0,
+     [lambda: P.test_abs_sums_are_products_of_absolute_values((12, 40, 32), 31)]),
+    ("gq abs sum uses the signed scale", "if (gqabs) gqabs[r * N + c] = Ga[r * N + c] * fabs(s);",
+     "if (gqabs) gqabs[r * N + c] = Ga[r * N + c] * s;", 0,
+     [lambda: P.test_abs_sums_are_products_of_absolute_values((12, 40, 32), 31)]),
+    ("G abs sum without |.|", "ga[c] += fabs(term);", "ga[c] += term;", 0,
+     [lambda: P.test_abs_sums_are_products_of_absolute_values((12, 40, 32), 31)]),
+    ("sgrad abs sum drops |T|", "sa += Ga[r * N + c] * (double)abs(w);", "sa += Ga[r * N + c];", 0,
+     [lambda: P.test_abs_sums_are_products_of_absolute_values((12, 40, 32), 31)]),
+    ("sampled Y abs sum drops |s|", "*outabs = fabs((double)s) * aab;", "*outabs = aab;", 0,
+     [lambda: P.test_abs_sums_are_products_of_absolute_values((12, 40, 32), 31), P.test_sampled_entries_equal_full_outputs]),
+    ("sampled dX abs sum drops |T|", "aab += fabs(term);\n    }\n    *out = acc;",
+     "aab += fabs(or_bf16_value(dyrow[c]) * (double)scale[c]);\n    }\n    *out = acc;", 0,
+     [lambda: P.test_abs_sums_are_products_of_absolute_values((12, 40, 32), 31), P.test_sampled_entries_equal_full_outputs]),
+    ("sampled gq abs sum drops |s|", "*outabs = aab * fabs((double)s);", "*outabs = aab;", 0,
+     [lambda: P.test_abs_sums_are_products_of_absolute_values((12, 40, 32), 31), P.test_sampled_entries_equal_full_outputs]),
+    ("sampled sgrad abs sum drops |T|", "sa += G[K + r] * (double)abs(w);", "sa += G[K + r];", 0,
+     [lambda: P.test_abs_sums_are_products_of_absolute_values((12, 40, 32), 31), P.test_sampled_entries_equal_full_outputs]),
     ("clip inverted", "if (max_norm > 0.0 && norm > max_norm) return max_norm / norm;",
      "if (max_norm > 0.0 && norm > max_norm) return norm / max_norm;", 0,
      [P.test_sumsq_and_norm, P.test_clipped_gradient_has_the_clip_norm]),

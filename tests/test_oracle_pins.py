@@ -436,3 +436,61 @@ def test_g_of_a_concatenated_batch_is_the_sum_over_micro_batches():
     ssum = sum(oracle.dw(p.X, p.dY, q, scale)[2] for p in parts)
     assert np.all(np.abs(gsum - g) <= 1e-12 * ga + 1e-18)
     assert np.all(np.abs(ssum - s) <= 1e-12 * sa + 1e-18)
+
+
+# ----------------------------------------------------------------- the tolerance denominators
+#
+# Every GEMM parity verdict divides by the oracle's sum of |term| of each output's
+# dot product.  These pins compute those sums a second way, as products of the
+# absolute-value matrices (numpy fp64 matmul, ternary from the hand-tabulated
+# truth table), and check the special case where every term has one sign and the
+# sum of |term| is the |sum|: a denominator that is too large (a dropped |T|, an
+# |s| left out or doubled, a term counted twice) fails one of them.
+
+def _tern_table(q):
+    table = {int(a): int(b) for a, b in _rows("ternary_theta2.txt")}
+    return np.vectorize(table.get)(q).astype(np.float64)
+
+
+@pytest.mark.parametrize("shape,seed", [((12, 40, 32), 31), ((33, 16, 48), 32), ((5, 64, 16), 33)])
+def test_abs_sums_are_products_of_absolute_values(shape, seed):
+    M, K, N = shape
+    X, q, scale, dY = _small(M, K, N, seed=seed)
+    q = np.clip(q, -7, 7)
+    scale = scale.copy()
+    scale[::3] *= -1.0                       # negative scales: only |s| may enter a sum
+    aX, adY, aT = np.abs(_f(X)), np.abs(_f(dY)), np.abs(_tern_table(q))
+    aS = np.abs(scale.astype(np.float64))
+    _, Ya = oracle.fwd(X, q, scale)
+    _, dXa = oracle.dx(dY, q, scale)
+    _, gqa, _, sga = oracle.dw(X, dY, q, scale)
+    np.testing.assert_allclose(Ya, (aX @ aT) * aS[None, :], rtol=1e-12, atol=0)
+    np.testing.assert_allclose(dXa, (adY * aS[None, :]) @ aT.T, rtol=1e-12, atol=0)
+    np.testing.assert_allclose(gqa, (aX.T @ adY) * aS[None, :], rtol=1e-12, atol=0)
+    np.testing.assert_allclose(sga, ((aX.T @ adY) * aT).sum(axis=0), rtol=1e-12, atol=0)
+    # the single-entry versions used at full size
+    rng = np.random.default_rng(seed)
+    for m, r, c in zip(rng.integers(0, M, 6), rng.integers(0, K, 6), rng.integers(0, N, 6)):
+        assert oracle.fwd_at(X[m], q[:, c], scale[c])[1] == pytest.approx((aX[m] @ aT[:, c]) * aS[c], rel=1e-12)
+        assert oracle.dx_at(dY[m], q[r], scale)[1] == pytest.approx((adY[m] * aS) @ aT[r], rel=1e-12)
+        assert oracle.gq_at(X[:, r], dY[:, c], scale[c])[1] == pytest.approx((aX[:, r] @ adY[:, c]) * aS[c],
+                                                                            rel=1e-12)
+        assert oracle.sgrad_at(X, dY[:, c], q[:, c])[1] == pytest.approx(((aX.T @ adY[:, c]) * aT[:, c]).sum(),
+                                                                         rel=1e-12)
+
+
+def test_abs_sums_equal_the_outputs_when_every_term_has_one_sign():
+    # X >= 0, dY >= 0, T >= 0 and scale > 0: each sum of |term| is the output itself,
+    # and with every sign flipped (X <= 0, scale < 0) it is the output's magnitude
+    M, K, N = 9, 48, 32
+    X, q, scale, dY = _small(M, K, N, seed=34)
+    Xp, dYp = X & np.uint16(0x7FFF), dY & np.uint16(0x7FFF)       # clear the bf16 sign bits
+    qp = np.abs(q).astype(np.int8)
+    for Xs, sc, sign in ((Xp, scale, 1.0), (Xp | np.uint16(0x8000), -scale, 1.0), (Xp | np.uint16(0x8000), scale, -1.0)):
+        Y, Ya = oracle.fwd(Xs, qp, sc)
+        np.testing.assert_allclose(Ya, sign * Y, rtol=1e-13, atol=0)
+        dX, dXa = oracle.dx(dYp, qp, sc)
+        np.testing.assert_allclose(dXa, np.abs(dX), rtol=1e-13, atol=0)
+        gq, gqa, sg, sga = oracle.dw(Xs, dYp, qp, sc)
+        np.testing.assert_allclose(gqa, np.abs(gq), rtol=1e-13, atol=0)
+        np.testing.assert_allclose(sga, np.abs(sg), rtol=1e-13, atol=0)
