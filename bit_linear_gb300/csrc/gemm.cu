@@ -32,9 +32,16 @@
 // stage it filled and the MMA thread for the release of the last accumulators, so
 // no asynchronous arrival lands in shared memory the next kernel's CTA owns.
 //
-// Every mbarrier wait is bounded; on expiry a kernel records TERN_ERR_TIMEOUT in
-// g_gemm_status (and the site in g_gemm_site), raises a CTA-wide abort flag, waits
-// (again bounded) for its own TMA copies and MMAs in flight, frees TMEM and returns.
+// Every mbarrier wait of the pipeline is bounded; on expiry a kernel records
+// TERN_ERR_TIMEOUT in g_gemm_status (and the site in g_gemm_site), raises a CTA-wide
+// abort flag, waits (again bounded) for its own TMA copies and MMAs in flight, frees
+// TMEM and returns.  Three waits of the set-up have no bound, because the hardware
+// offers none: the TMEM allocation (tcgen05.alloc blocks until the columns are
+// free), the cluster barrier of a CTA pair (barrier.cluster) and the dependent-launch
+// wait (griddepcontrol.wait).  The GEMMs are launched without programmatic stream
+// serialization, so each one starts only after every earlier kernel on its stream has
+// completed: no GEMM CTA shares an SM with a CTA that still holds TMEM, and its set-up
+// never waits on another grid.
 #include <algorithm>
 #include <chrono>
 #include <cmath>
@@ -61,6 +68,10 @@ namespace {
 
 constexpr int kBM = 128;           // rows of A (and of D) per CTA
 constexpr int kThreads = 192;
+// Output staging of the epilogue: per epilogue warp two 32 x 32 fp32 buffers (4 KB each,
+// 128-byte swizzle), from which one lane issues the TMA store of each chunk.
+constexpr int kStageBuf = 32 * 32 * 4;
+constexpr int kStagingBytes = 4 * 2 * kStageBuf;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait; a healthy wait takes microseconds
 
 enum { EPI_FWD = 0, EPI_DX = 1, EPI_DW = 2 };
@@ -90,12 +101,15 @@ struct GemmGroup {
     CUtensorMap mA[G];
     CUtensorMap mB0[G];
     CUtensorMap mB1[G];
+    CUtensorMap mOut[G];   // fp32 output in 32 x 32 boxes: out, or partial_g for split units
     GemmArgs args[G];
     int unit_begin[G + 1];
     int count;
 };
 
-static_assert(sizeof(GemmGroup<8>) <= 4096, "kernel parameter block over 4 KB");
+// Problems per grouped launch: four tensor maps each keep the parameter block under 4 KB.
+constexpr int kGroup = 6;
+static_assert(sizeof(GemmGroup<kGroup>) <= 4096, "kernel parameter block over 4 KB");
 
 template <int G>
 __device__ __forceinline__ int group_find(const GemmGroup<G>& g, int unit) {
@@ -118,7 +132,7 @@ struct Cfg {
     static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES;   // per CTA
     static constexpr int TX_BYTES = CG * STAGE_BYTES;            // landing on the leader's barrier
     static constexpr int TMEM_COLS = 2 * BN;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + kStagingBytes + 1024 + 256;
     static_assert(CG == 1 || CG == 2, "CTA group");
     static_assert(BK == 64 || (BK == 32 && !A_MN && !B_MN), "MN-major operands use 64-deep k-blocks");
     static_assert(BN % 64 == 0 && BN <= 256 && B_ROWS % 64 == 0, "BN");
@@ -128,12 +142,12 @@ struct Cfg {
 
 // One CTA per 128 x 256 tile (small problems).
 using Fwd1 = Cfg<1, 256, 64, false, true, 1, EPI_FWD, 4>;   // A = X (K-major), B = T [K][N] (MN-major)
-using Dx1 = Cfg<1, 256, 32, false, false, 2, EPI_DX, 5>;    // A = dY (K-major), B = W_hi, W_lo (K-major)
+using Dx1 = Cfg<1, 256, 32, false, false, 2, EPI_DX, 4>;    // A = dY (K-major), B = W_hi, W_lo (K-major)
 using Dw1 = Cfg<1, 256, 64, true, true, 1, EPI_DW, 4>;      // A = X^T, B = dY^T (both MN-major)
 // A CTA pair per 256 x 256 tile: half the shared-memory operand traffic per MMA.
-using Fwd2 = Cfg<2, 256, 64, false, true, 1, EPI_FWD, 7>;
+using Fwd2 = Cfg<2, 256, 64, false, true, 1, EPI_FWD, 6>;
 using Dx2 = Cfg<2, 256, 64, false, false, 2, EPI_DX, 4>;
-using Dw2 = Cfg<2, 256, 64, true, true, 1, EPI_DW, 7>;
+using Dw2 = Cfg<2, 256, 64, true, true, 1, EPI_DW, 6>;
 
 // tcgen05 instruction descriptor, kind::f16: bf16 A/B, fp32 D, M x N, operand majors.
 __host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool a_mn, bool b_mn) {
@@ -235,58 +249,73 @@ __device__ __forceinline__ float warp_column_sums(float (&v)[32], int lane) {
     return v[0];
 }
 
-// One 32-column chunk of a warp's 32 rows: r[] is row `row`, columns c0..c0+31.
-// tile128 is the index of the 128-row block the row lies in.
+// Stage one 32 x 32 fp32 chunk of a warp (lane = row, v = its 32 columns) in shared
+// memory with the 128-byte swizzle of the output tensor map, then let one lane issue
+// the chunk's TMA store (or fp32 add) at column x, row y; rows and columns past the
+// tensor's edge are clipped by the copy.  Two buffers per warp: before one is
+// rewritten, the store issued from it two chunks earlier must have read it.
+__device__ __forceinline__ void store_chunk(const CUtensorMap* map, uint32_t stage, int& nchunk, const float (&v)[32],
+                                            int x, int y, bool add, int lane) {
+    const uint32_t buf = stage + static_cast<uint32_t>(nchunk & 1) * kStageBuf;
+    if (nchunk >= 2 && lane == 0) ptx::bulk_wait_read<1>();
+    __syncwarp();
+    const uint32_t row = buf + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        ptx::st_shared_v4(row + (static_cast<uint32_t>(c ^ (lane & 7)) << 4), v[4 * c], v[4 * c + 1], v[4 * c + 2],
+                          v[4 * c + 3]);
+    ptx::fence_proxy_async_smem();   // the generic-proxy writes above, before the async-proxy read
+    __syncwarp();
+    if (lane == 0) {
+        if (add) ptx::tma_reduce_add_2d(map, buf, x, y);
+        else ptx::tma_store_2d(map, buf, x, y);
+        ptx::bulk_commit();
+    }
+    ++nchunk;
+}
+
+// One 32-column chunk of a warp's 32 rows: r[] is row `row` (the warp's rows start at
+// `wrow`), columns c0..c0+31.  tile128 is the index of the 128-row block the rows lie in.
 template <class C>
-__device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const uint32_t (&r)[32], int row, int c0,
+__device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const CUtensorMap* omap, uint32_t stage,
+                                               int& nchunk, const uint32_t (&r)[32], int row, int wrow, int c0,
                                                int tile128, int quad, int lane) {
     const bool row_ok = row < a.Mg;
-    if (row_ok && (a.out != nullptr || (C::EPI != EPI_DW && a.out_bf16 != nullptr))) {
-        const int64_t at = static_cast<int64_t>(row) * a.Ng + c0;
+    const bool hi_ok = c0 + 16 < a.Ng;   // N is a multiple of 16: the chunk's second half may lie past it
+    float v[32];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            if (c0 + 16 * h < a.Ng) {
-                float4 v[4];
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+    if (C::EPI == EPI_FWD || (C::EPI == EPI_DW && a.out != nullptr)) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int j = 16 * h + 4 * q;
-                    v[q] = make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
-                                       __uint_as_float(r[j + 3]));
-                    if constexpr (C::EPI != EPI_DX) {
-                        const float4 s = __ldg(reinterpret_cast<const float4*>(a.scale + c0 + j));
-                        v[q].x *= s.x;
-                        v[q].y *= s.y;
-                        v[q].z *= s.z;
-                        v[q].w *= s.w;
+        for (int q = 0; q < 8; ++q) {
+            if (q < 4 || hi_ok) {
+                const float4 sc = __ldg(reinterpret_cast<const float4*>(a.scale + c0 + 4 * q));
+                v[4 * q] *= sc.x;
+                v[4 * q + 1] *= sc.y;
+                v[4 * q + 2] *= sc.z;
+                v[4 * q + 3] *= sc.w;
+            }
+        }
+    }
+    // fp32 output through shared memory and TMA (gq += ... with accumulate: a TMA add);
+    // the condition is the same for the whole warp
+    if (a.out != nullptr && wrow < a.Mg)
+        store_chunk(omap, stage, nchunk, v, c0, wrow, C::EPI == EPI_DW && a.accumulate != 0, lane);
+    if constexpr (C::EPI != EPI_DW) {
+        if (a.out_bf16 != nullptr && row_ok) {   // 16 columns -> 32 bytes, round to nearest even
+            const int64_t at = static_cast<int64_t>(row) * a.Ng + c0;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if (h == 0 || hi_ok) {
+                    uint32_t b[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const __nv_bfloat162 t = __floats2bfloat162_rn(v[16 * h + 2 * q], v[16 * h + 2 * q + 1]);
+                        b[q] = *reinterpret_cast<const uint32_t*>(&t);
                     }
-                    if constexpr (C::EPI == EPI_DW) {
-                        if (a.accumulate) {   // micro-batch accumulation: add to the stored gq
-                            const float4 old = *reinterpret_cast<const float4*>(a.out + at + j);
-                            v[q].x = old.x + v[q].x;
-                            v[q].y = old.y + v[q].y;
-                            v[q].z = old.z + v[q].z;
-                            v[q].w = old.w + v[q].w;
-                        }
-                    }
-                }
-                if (a.out != nullptr) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) *reinterpret_cast<float4*>(a.out + at + 16 * h + 4 * q) = v[q];
-                }
-                if constexpr (C::EPI != EPI_DW) {
-                    if (a.out_bf16 != nullptr) {   // 16 columns -> 32 bytes, round to nearest even
-                        uint32_t b[8];
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const __nv_bfloat162 lo = __floats2bfloat162_rn(v[q].x, v[q].y);
-                            const __nv_bfloat162 hi = __floats2bfloat162_rn(v[q].z, v[q].w);
-                            b[2 * q] = *reinterpret_cast<const uint32_t*>(&lo);
-                            b[2 * q + 1] = *reinterpret_cast<const uint32_t*>(&hi);
-                        }
-                        uint4* ob = reinterpret_cast<uint4*>(a.out_bf16 + at + 16 * h);
-                        ob[0] = make_uint4(b[0], b[1], b[2], b[3]);
-                        ob[1] = make_uint4(b[4], b[5], b[6], b[7]);
-                    }
+                    uint4* ob = reinterpret_cast<uint4*>(a.out_bf16 + at + 16 * h);
+                    ob[0] = make_uint4(b[0], b[1], b[2], b[3]);
+                    ob[1] = make_uint4(b[4], b[5], b[6], b[7]);
                 }
             }
         }
@@ -298,16 +327,16 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const uint32_t
         if (row_ok) {
             const uint32_t* pr = a.packed + static_cast<int64_t>(row) * (a.Ng / 16) + c0 / 16;
             w0 = __ldg(pr);
-            if (c0 + 16 < a.Ng) w1 = __ldg(pr + 1);
+            if (hi_ok) w1 = __ldg(pr + 1);
         }
-        float v[32];
+        float t[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
             const uint32_t code = ((i < 16 ? w0 : w1) >> (2 * (i & 15))) & 3u;
             const float g = __uint_as_float(r[i]);
-            v[i] = (code & 1u) ? ((code & 2u) ? -g : g) : 0.0f;
+            t[i] = (code & 1u) ? ((code & 2u) ? -g : g) : 0.0f;
         }
-        const float colsum = warp_column_sums(v, lane);
+        const float colsum = warp_column_sums(t, lane);
         if (c0 + lane < a.Ng) a.partial[static_cast<int64_t>(tile128 * 4 + quad) * a.Ng + c0 + lane] = colsum;
     }
 }
@@ -321,7 +350,8 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + C::STAGES * C::STAGE_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + C::STAGES * C::STAGE_BYTES + kStagingBytes);
+    const uint32_t staging0 = base + static_cast<uint32_t>(C::STAGES * C::STAGE_BYTES);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 5);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const uint32_t bar0 = ptx::smem_u32(bars);
@@ -361,12 +391,12 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
     if constexpr (CG == 2) ptx::cluster_sync(); else __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    // Dependents may launch only now, with TMEM allocated in every CTA of the grid: a
-    // CTA holds the SM's TMEM allocation permit until it relinquishes it or exits, so
-    // a dependent's block placed on this SM earlier (waiting, in its dependent-launch
-    // wait, for this grid to finish) could hold the permit this CTA's allocation needs.
+    // With TMEM allocated in every CTA of the grid, a dependent small kernel (a reduce,
+    // AdamW) may launch and wait for this grid on the SMs it leaves free.  The wait is
+    // a no-op here (the GEMMs are launched with full stream serialization); it stays so
+    // that the kernel is correct under any launch.
     ptx::pdl_trigger();
-    ptx::pdl_wait();   // the set-up above overlapped the previous kernel; global memory from here on
+    ptx::pdl_wait();
     if (threadIdx.x == 32) atomicAdd(&g_gemm_count[1], 1ull);
 
     uint32_t issued = 0, issued_parity = 0;   // producer: stages with a copy issued, and its phase
@@ -435,8 +465,8 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
         }
         // Producer tail: wait until the MMA has released every stage filled above.  The
         // release is an asynchronous arrival (multicast to both CTAs of a pair) that may
-        // otherwise land after this CTA has exited, in the barriers of the next kernel's
-        // CTA on this SM (with programmatic dependent launch it is placed at once).
+        // otherwise land after this CTA has exited, in the barriers of the next CTA
+        // placed on this SM.
         if (ok) {
             for (int s = 0; s < C::STAGES; ++s)
                 if (issued & (1u << s))
@@ -506,6 +536,8 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
         // ------------------------------------------------------------ epilogue
         const int quad = warp & 3;   // a warp may touch TMEM lanes 32*(warp%4) .. +31
         const uint32_t tempty_leader = CG == 2 ? ptx::mapa_shared(TEMPTY0, 0) : TEMPTY0;
+        const uint32_t stage = staging0 + static_cast<uint32_t>(warp - 2) * 2u * kStageBuf;
+        int nchunk = 0;   // chunks this warp has staged (its buffer parity)
         int local = 0;
         for (int ug = unit; ug < total_units; ug += units, ++local) {
             const int p = group_find(grp, ug);
@@ -521,24 +553,24 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
             tile_coords<16 / CG>(a.tile_begin + u / a.split, a.tiles_m, a.tiles_n, mt, nt);
             const int row0 = mt * C::TILE_M + static_cast<int>(rank) * kBM;
             const uint32_t trow = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * C::BN;
+            const CUtensorMap* omap = &grp.mOut[p];
             if (C::EPI == EPI_DW && a.partial_g != nullptr) {
-                // split unit: the raw partial tile, row-major TILE_M x BN, for the reduce kernel
-                float* pg = a.partial_g + static_cast<int64_t>(u) * C::TILE_M * C::BN +
-                            static_cast<int64_t>(static_cast<int>(rank) * kBM + quad * 32 + lane) * C::BN;
+                // split unit: the raw partial tile (row-major TILE_M x BN, unit after unit in
+                // partial_g, which omap describes) for the reduce kernel
+                const int prow = u * C::TILE_M + static_cast<int>(rank) * kBM + quad * 32;
 #pragma unroll 1
                 for (int j = 0; j < C::BN / 32; ++j) {
                     uint32_t r[32];
                     ptx::tmem_ld_32x32b_x32(trow + j * 32, r);
                     ptx::tmem_wait_ld();
+                    float v[32];
 #pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        *reinterpret_cast<float4*>(pg + j * 32 + 4 * q) =
-                            make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                                        __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+                    store_chunk(omap, stage, nchunk, v, j * 32, prow, false, lane);
                 }
             } else if (row0 < a.Mg) {   // a pair's second half may lie wholly past the last row
                 const int tile128 = mt * CG + static_cast<int>(rank);
-                const int row = row0 + quad * 32 + lane;
+                const int wrow = row0 + quad * 32;
 #pragma unroll 1
                 for (int j = 0; j < C::BN / 32; ++j) {
                     const int c0 = nt * C::BN + j * 32;
@@ -546,7 +578,7 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
                     uint32_t r[32];
                     ptx::tmem_ld_32x32b_x32(trow + j * 32, r);
                     ptx::tmem_wait_ld();
-                    epilogue_chunk<C>(a, r, row, c0, tile128, quad, lane);
+                    epilogue_chunk<C>(a, omap, stage, nchunk, r, wrow + lane, wrow, c0, tile128, quad, lane);
                 }
             }
             ptx::tc_fence_before();
@@ -556,6 +588,10 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
                 else ptx::mbar_arrive(TEMPTY0 + 8u * acc);
             }
         }
+        // every TMA store of this warp has written its box before the CTA's shared
+        // memory goes away (the copies end by themselves: nothing they wait on)
+        if (lane == 0) ptx::bulk_wait_all();
+        __syncwarp();
     }
 
     ptx::tc_fence_before();
@@ -617,6 +653,21 @@ __global__ void tern_wait_selftest(uint64_t limit_ns) {
     if (threadIdx.x == 0) wait_bounded(ptx::smem_u32(&bar), 0, &abort_flag, false, 999, limit_ns);
 }
 
+// sum_i partial[i][c] in ascending i; eight loads go out before their (ordered) adds.
+__device__ __forceinline__ float ordered_column_sum(const float* __restrict__ partial, int nparts, int N, int c) {
+    float s = 0.0f;
+    int i = 0;
+    for (; i + 8 <= nparts; i += 8) {
+        float x[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x[k] = partial[static_cast<int64_t>(i + k) * N + c];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) s += x[k];
+    }
+    for (; i < nparts; ++i) s += partial[static_cast<int64_t>(i) * N + c];
+    return s;
+}
+
 // sgrad[c] = sum over the partial rows in ascending order (deterministic); with
 // accumulate, that sum is added to the stored sgrad[c].
 __global__ void tern_sgrad_reduce(const float* __restrict__ partial, int nparts, int N, float* __restrict__ sgrad,
@@ -625,16 +676,9 @@ __global__ void tern_sgrad_reduce(const float* __restrict__ partial, int nparts,
     ptx::pdl_wait();
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
     if (c >= N) return;
-    float s = 0.0f;
-    for (int i = 0; i < nparts; ++i) s += partial[static_cast<int64_t>(i) * N + c];
-    sgrad[c] = accumulate ? sgrad[c] + s : s;
+    sgrad[c] = accumulate ? sgrad[c] + ordered_column_sum(partial, nparts, N, c) : ordered_column_sum(partial, nparts, N, c);
 }
 
-// Finish the split G tiles: G = sum over the tile's slices in slice order, then
-// the same epilogue as the G kernel (gq = G*scale[c], or += with accumulate,
-// and the sgrad partial of each 32-row group).  One CTA per 32 x 32 block of a
-// tile: warp w takes rows 4w..4w+3 of the block, lane l column l; the eight
-// warps' column sums are added in warp order through shared memory.
 // The split tiles of up to G problems: problem p owns blocks [block_begin[p], block_begin[p+1]).
 template <int G>
 struct ReduceGroup {
@@ -644,6 +688,13 @@ struct ReduceGroup {
     int tile_m, tile_n;
 };
 
+// Finish the split G tiles: G = sum over the tile's slices in slice order, then the
+// same epilogue as the G kernel (gq = G*scale[c], or += with accumulate, and the sgrad
+// partial of each 32-row group).  One CTA per 32-row group and 128-column half of a
+// tile: warp w takes rows 4w..4w+3 of the group, lane l columns 4l..4l+3 of the half
+// (16-byte loads: a warp reads 512 contiguous bytes of a row; two slices' loads go out
+// before their adds); the eight warps' column sums are added in warp order through
+// shared memory.
 template <int G>
 __global__ void __launch_bounds__(256) tern_dw_split_reduce(const __grid_constant__ ReduceGroup<G> grp) {
     ptx::pdl_trigger();
@@ -653,53 +704,92 @@ __global__ void __launch_bounds__(256) tern_dw_split_reduce(const __grid_constan
     const GemmArgs& a = grp.args[p];
     const int block = static_cast<int>(blockIdx.x) - grp.block_begin[p];
     const int tile_m = grp.tile_m, tile_n = grp.tile_n;
-    const int row_groups = tile_m / 32, col_groups = tile_n / 32;
-    const int per_tile = row_groups * col_groups;
+    const int halves = tile_n / 128;
+    const int per_tile = (tile_m / 32) * halves;
     const int j = block / per_tile;                        // split tile
-    const int rg = (block % per_tile) / col_groups;        // 32-row group within the tile
-    const int cgi = block % col_groups;                    // 32-column group within the tile
+    const int rg = (block % per_tile) / halves;            // 32-row group within the tile
+    const int hf = block % halves;                         // 128-column half within the tile
     int tm, tn;
     if (tile_m == 2 * kBM) tile_coords<8>(a.tile_begin + j, a.tiles_m, a.tiles_n, tm, tn);
     else tile_coords<16>(a.tile_begin + j, a.tiles_m, a.tiles_n, tm, tn);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int c_in = cgi * 32 + lane;                      // column within the tile
+    const int c_in = hf * 128 + lane * 4;                  // first of this thread's columns in the tile
     const int col = tn * tile_n + c_in;
     const int r_base = tm * tile_m + rg * 32;
     // partial rows exist for every 32-row group of the 128-row blocks that hold rows;
     // a group wholly past the last row still writes its (zero) partial
     if (r_base >= ((a.Mg + kBM - 1) / kBM) * kBM) return;
-    const bool col_ok = col < a.Ng;
-    float colsum = 0.0f;
+    const bool col_ok = col < a.Ng;                        // N % 16 == 0: all four columns or none
+    const int64_t tile_elems = static_cast<int64_t>(tile_m) * tile_n;
+    const float* base = a.partial_g + static_cast<int64_t>(j) * a.split * tile_elems +
+                        static_cast<int64_t>(rg * 32 + warp * 4) * tile_n + c_in;
+    float4 g[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int r_in = rg * 32 + warp * 4 + i;           // row within the tile
-        const int row = tm * tile_m + r_in;
-        const float* p = a.partial_g + static_cast<int64_t>(j) * a.split * tile_m * tile_n +
-                         static_cast<int64_t>(r_in) * tile_n + c_in;
-        float g = 0.0f;
-        for (int sl = 0; sl < a.split; ++sl) g += p[static_cast<int64_t>(sl) * tile_m * tile_n];
-        if (row < a.Mg && col_ok) {
+    for (int i = 0; i < 4; ++i) g[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto add = [](float4& s, const float4& x) {
+        s.x += x.x;
+        s.y += x.y;
+        s.z += x.z;
+        s.w += x.w;
+    };
+    int sl = 0;
+    for (; sl + 2 <= a.split; sl += 2) {
+        float4 x0[4], x1[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            x0[i] = __ldcs(reinterpret_cast<const float4*>(base + sl * tile_elems + i * tile_n));
+            x1[i] = __ldcs(reinterpret_cast<const float4*>(base + (sl + 1) * tile_elems + i * tile_n));
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            add(g[i], x0[i]);
+            add(g[i], x1[i]);
+        }
+    }
+    if (sl < a.split) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) add(g[i], __ldcs(reinterpret_cast<const float4*>(base + sl * tile_elems + i * tile_n)));
+    }
+    float cs[4] = {0.f, 0.f, 0.f, 0.f};
+    if (col_ok) {
+        const float4 sc = a.out ? *reinterpret_cast<const float4*>(a.scale + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int row = r_base + warp * 4 + i;
+            if (row >= a.Mg) break;
             if (a.out) {
-                const float v = g * a.scale[col];
-                float* o = a.out + static_cast<int64_t>(row) * a.Ng + col;
-                *o = a.accumulate ? *o + v : v;
+                float4 v = make_float4(g[i].x * sc.x, g[i].y * sc.y, g[i].z * sc.z, g[i].w * sc.w);
+                float4* o = reinterpret_cast<float4*>(a.out + static_cast<int64_t>(row) * a.Ng + col);
+                if (a.accumulate) {
+                    const float4 old = *o;
+                    v = make_float4(old.x + v.x, old.y + v.y, old.z + v.z, old.w + v.w);
+                }
+                *o = v;
             }
             if (a.partial) {
-                const uint32_t code =
-                    (a.packed[static_cast<int64_t>(row) * (a.Ng / 16) + col / 16] >> (2 * (col % 16))) & 3u;
-                colsum += (code & 1u) ? ((code & 2u) ? -g : g) : 0.0f;
+                const uint32_t w = a.packed[static_cast<int64_t>(row) * (a.Ng / 16) + col / 16] >> (2 * (col % 16));
+                const float gv[4] = {g[i].x, g[i].y, g[i].z, g[i].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t code = (w >> (2 * k)) & 3u;
+                    cs[k] += (code & 1u) ? ((code & 2u) ? -gv[k] : gv[k]) : 0.0f;
+                }
             }
         }
     }
     if (a.partial == nullptr) return;
-    __shared__ float red[8][32];
-    red[warp][lane] = colsum;
-    __syncthreads();
-    if (warp == 0 && col_ok) {
-        float s = 0.0f;
+    __shared__ float red[8][128];
 #pragma unroll
-        for (int w = 0; w < 8; ++w) s += red[w][lane];
-        a.partial[static_cast<int64_t>(r_base / 32) * a.Ng + col] = s;
+    for (int k = 0; k < 4; ++k) red[warp][lane * 4 + k] = cs[k];
+    __syncthreads();
+    if (threadIdx.x < 128) {
+        const int cc = tn * tile_n + hf * 128 + static_cast<int>(threadIdx.x);
+        if (cc < a.Ng) {
+            float s = 0.0f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) s += red[w][threadIdx.x];
+            a.partial[static_cast<int64_t>(r_base / 32) * a.Ng + cc] = s;
+        }
     }
 }
 
@@ -736,6 +826,21 @@ int map_bf16(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, int 
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? TERN_OK : TERN_ERR_CUDA;
+}
+
+// Tensor map of a row-major fp32 output [rows][cols], written by the epilogues in boxes
+// of 32 x 32 with the 128-byte swizzle (cols % 4 == 0, base 16-byte aligned).
+int map_f32_out(CUtensorMap* m, const float* ptr, int64_t cols, int64_t rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return TERN_ERR_CUDA;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 4};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? TERN_OK : TERN_ERR_CUDA;
 }
@@ -801,7 +906,9 @@ int persistent_units(K kernel, int num_sms, int* units) {
 }
 
 // Persistent launch of a problem group: one CTA (or CTA pair) per SM (pair of
-// SMs), at most one per work unit, with programmatic dependent launch.
+// SMs), at most one per work unit.  No programmatic stream serialization: the grid
+// starts once every earlier kernel on the stream has completed, so its TMEM
+// allocation and cluster barrier (waits without a bound) never wait on another grid.
 template <class C, class K, int G>
 int launch(K kernel, const GemmGroup<G>& grp, int num_sms, cudaStream_t s) {
     int units = 0;
@@ -809,18 +916,16 @@ int launch(K kernel, const GemmGroup<G>& grp, int num_sms, cudaStream_t s) {
     const int total = grp.unit_begin[grp.count];
     if (total <= 0) return TERN_OK;
     cudaLaunchConfig_t cfg{};
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[1];
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = s;
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = 2;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = C::CG == 2 ? 2 : 1;
+    cfg.numAttrs = C::CG == 2 ? 1 : 0;
     cfg.gridDim = dim3(C::CG * std::min(total, units));
     TERN_CUDA_TRY(cudaLaunchKernelEx(&cfg, kernel, grp));
     return TERN_OK;
@@ -846,6 +951,9 @@ int group_set(GemmGroup<G>& g, int p, const void* A, int64_t a_inner, int64_t a_
         g.mB1[p] = g.mB0[p];
     }
     g.args[p] = a;
+    // the epilogue's fp32 output: out [Mg][Ng], or the split units' partial tiles
+    if (a.partial_g) return map_f32_out(&g.mOut[p], a.partial_g, C::BN, static_cast<int64_t>(a.num_units) * C::TILE_M);
+    if (a.out) return map_f32_out(&g.mOut[p], a.out, a.Ng, a.Mg);
     return TERN_OK;
 }
 
@@ -882,6 +990,10 @@ int run_dx(K kernel, const uint16_t* dY, const uint16_t* whi, const uint16_t* wl
 
 // Largest number of split units the tail of a G launch may use (bounds the workspace).
 constexpr int kMaxTailUnits = 128;
+// ... and of a grouped G launch, whose split covers every tile of the group (at M = 8192
+// the six RWKV-style projections have 48 G tiles of 128 k-blocks: split three ways they
+// fill two waves of 76 pairs)
+constexpr int kMaxGroupTailUnits = 256;
 
 template <class C>
 int64_t dw_tail_bytes(int64_t M, int64_t K_, int64_t N) {
@@ -937,6 +1049,8 @@ int run_dw(K kernel, const uint16_t* X, const uint16_t* dY, const float* scale, 
                 t.split = split;
                 t.kb_per = kb_per;
                 t.partial_g = tail;
+                if (int st = map_f32_out(&g.mOut[0], tail, C::BN, static_cast<int64_t>(t.num_units) * C::TILE_M))
+                    return st;
                 group_close(g, 1);
                 if (int st = launch<C>(kernel, g, num_sms, s)) return st;
                 ReduceGroup<1> r;
@@ -945,7 +1059,7 @@ int run_dw(K kernel, const uint16_t* X, const uint16_t* dY, const float* scale, 
                 r.tile_m = C::TILE_M;
                 r.tile_n = C::BN;
                 r.block_begin[0] = 0;
-                r.block_begin[1] = R * (C::TILE_M / 32) * (C::BN / 32);
+                r.block_begin[1] = R * (C::TILE_M / 32) * (C::BN / 128);
                 return launch_split_reduce<C>(r, s);
             }
         }
@@ -1075,7 +1189,6 @@ extern "C" int tern_linear_bwd(const uint16_t* X, const uint16_t* dY, const tern
 namespace tern {
 namespace {
 
-constexpr int kGroup = 8;
 
 int layer_align(const tern_layer& L) {
     if (L.K % 16 || L.N % 16) return TERN_ERR_ALIGN;
@@ -1105,9 +1218,20 @@ int for_groups(const tern_layer* L, int count, Pick pick, Rows rows_of, Fn fn) {
     return TERN_OK;
 }
 
+// The layers of a launch in descending order of k-blocks per tile (stable): the
+// persistent pairs take units in concatenation order, so the longest tiles start
+// first and the short ones fill the last wave.
+template <class KbOf>
+void longest_first(const int* idx, int n, int* out, KbOf kb_of) {
+    for (int i = 0; i < n; ++i) out[i] = idx[i];
+    std::stable_sort(out, out + n, [&](int a, int b) { return kb_of(a) > kb_of(b); });
+}
+
 template <class C, class K>
-int fwd_group(K kernel, const tern_layer* L, const int* idx, int n, int num_sms, cudaStream_t s) {
+int fwd_group(K kernel, const tern_layer* L, const int* idx_in, int n, int num_sms, cudaStream_t s) {
     GemmGroup<kGroup> g;
+    int idx[kGroup];
+    longest_first(idx_in, n, idx, [&](int i) { return make_args<C>(L[i].M, L[i].N, L[i].K).num_kb; });
     for (int i = 0; i < n; ++i) {
         const tern_layer& l = L[idx[i]];
         GemmArgs a = make_args<C>(l.M, l.N, l.K);
@@ -1121,8 +1245,10 @@ int fwd_group(K kernel, const tern_layer* L, const int* idx, int n, int num_sms,
 }
 
 template <class C, class K>
-int dx_group(K kernel, const tern_layer* L, const int* idx, int n, int num_sms, cudaStream_t s) {
+int dx_group(K kernel, const tern_layer* L, const int* idx_in, int n, int num_sms, cudaStream_t s) {
     GemmGroup<kGroup> g;
+    int idx[kGroup];
+    longest_first(idx_in, n, idx, [&](int i) { return make_args<C>(L[i].M, L[i].K, L[i].N).num_kb; });
     for (int i = 0; i < n; ++i) {
         const tern_layer& l = L[idx[i]];
         GemmArgs a = make_args<C>(l.M, l.K, l.N);
@@ -1136,11 +1262,11 @@ int dx_group(K kernel, const tern_layer* L, const int* idx, int n, int num_sms, 
 
 // Split factor for a group of G problems with `tiles` tiles in all: the one
 // that minimises waves per slice, every problem keeping at least one k-block
-// per slice and the split units within kMaxTailUnits.
+// per slice and the split units within kMaxGroupTailUnits.
 int group_split(int tiles, int min_kb, int units) {
     int best = 1;
     double best_cost = std::ceil(static_cast<double>(tiles) / units);
-    for (int sp = 2; sp <= min_kb && tiles * sp <= kMaxTailUnits; ++sp) {
+    for (int sp = 2; sp <= min_kb && tiles * sp <= kMaxGroupTailUnits; ++sp) {
         const double cost = std::ceil(static_cast<double>(tiles) * sp / units) / sp;
         if (cost < best_cost - 1e-9) {
             best = sp;
@@ -1157,7 +1283,7 @@ int64_t group_tail_bytes(const tern_layer* L, const int* idx, int n) {
         const GemmArgs a = make_args<C>(L[idx[i]].K, L[idx[i]].N, L[idx[i]].M);
         units += static_cast<int64_t>(a.num_tiles) * a.num_kb;
     }
-    return std::min<int64_t>(kMaxTailUnits, units) * C::TILE_M * C::BN * static_cast<int64_t>(sizeof(float));
+    return std::min<int64_t>(kMaxGroupTailUnits, units) * C::TILE_M * C::BN * static_cast<int64_t>(sizeof(float));
 }
 
 // The G GEMMs of a group with the fused gq / sgrad epilogue.  When the group's
@@ -1167,14 +1293,17 @@ template <class C, class K>
 int dw_group(K kernel, const tern_layer* L, const int* idx, int n, float* const* partial, float* tail,
              int64_t tail_bytes, int accumulate, int num_sms, cudaStream_t s) {
     GemmGroup<kGroup> g;
+    int pos[kGroup], order[kGroup];
+    for (int i = 0; i < n; ++i) pos[i] = i;
+    longest_first(pos, n, order, [&](int i) { return make_args<C>(L[idx[i]].K, L[idx[i]].N, L[idx[i]].M).num_kb; });
     int tiles = 0, min_kb = 1 << 30;
     for (int i = 0; i < n; ++i) {
-        const tern_layer& l = L[idx[i]];
+        const tern_layer& l = L[idx[order[i]]];
         GemmArgs a = make_args<C>(l.K, l.N, l.M);
         a.out = l.gq;
         a.scale = l.scale;
         a.packed = l.W->packed;
-        a.partial = partial[i];
+        a.partial = partial[order[i]];
         a.accumulate = accumulate;
         if (int st = group_set<C>(g, i, l.X, l.K, l.M, l.dY, nullptr, l.N, l.M, a)) return st;
         tiles += a.num_tiles;
@@ -1202,9 +1331,11 @@ int dw_group(K kernel, const tern_layer* L, const int* idx, int n, float* const*
         a.kb_per = kb_per;
         a.num_units = a.num_tiles * a.split;
         a.partial_g = tail + off;
+        if (int st = map_f32_out(&g.mOut[i], a.partial_g, C::BN, static_cast<int64_t>(a.num_units) * C::TILE_M))
+            return st;
         off += static_cast<int64_t>(a.num_units) * C::TILE_M * C::BN;
         r.args[i] = a;
-        r.block_begin[i + 1] = r.block_begin[i] + a.num_tiles * (C::TILE_M / 32) * (C::BN / 32);
+        r.block_begin[i + 1] = r.block_begin[i] + a.num_tiles * (C::TILE_M / 32) * (C::BN / 128);
     }
     group_close(g, n);
     if (int st = launch<C>(kernel, g, num_sms, s)) return st;
@@ -1229,8 +1360,7 @@ __global__ void __launch_bounds__(256) tern_sgrad_reduce_group(const __grid_cons
     while (p + 1 < g.count && static_cast<int>(blockIdx.x) >= g.block_begin[p + 1]) ++p;
     const int c = (static_cast<int>(blockIdx.x) - g.block_begin[p]) * blockDim.x + threadIdx.x;
     if (c >= g.N[p]) return;
-    float s = 0.0f;
-    for (int i = 0; i < g.nparts[p]; ++i) s += g.partial[p][static_cast<int64_t>(i) * g.N[p] + c];
+    const float s = ordered_column_sum(g.partial[p], g.nparts[p], g.N[p], c);
     g.sgrad[p][c] = g.accumulate ? g.sgrad[p][c] + s : s;
 }
 
@@ -1368,7 +1498,6 @@ int gemm_setup(int num_sms) {
     TERN_CUDA_TRY(cudaGetDevice(&dev));
     if (dev < 0 || dev >= 64) return TERN_ERR_DEVICE;
     std::call_once(once[dev], [&] {
-        static_assert(kGroup == 8, "grouped instantiations below");
         int st = TERN_OK, u = 0;
         auto gemm = [&](int r) {
             if (st == TERN_OK) st = r;
@@ -1379,18 +1508,18 @@ int gemm_setup(int num_sms) {
         gemm(persistent_units<Dx2>(tern_dx_gemm<2, 1>, num_sms, &u));
         gemm(persistent_units<Dw1>(tern_dw_gemm<1, 1>, num_sms, &u));
         gemm(persistent_units<Dw2>(tern_dw_gemm<2, 1>, num_sms, &u));
-        gemm(persistent_units<Fwd1>(tern_fwd_gemm<1, 8>, num_sms, &u));
-        gemm(persistent_units<Fwd2>(tern_fwd_gemm<2, 8>, num_sms, &u));
-        gemm(persistent_units<Dx1>(tern_dx_gemm<1, 8>, num_sms, &u));
-        gemm(persistent_units<Dx2>(tern_dx_gemm<2, 8>, num_sms, &u));
-        gemm(persistent_units<Dw1>(tern_dw_gemm<1, 8>, num_sms, &u));
-        gemm(persistent_units<Dw2>(tern_dw_gemm<2, 8>, num_sms, &u));
+        gemm(persistent_units<Fwd1>(tern_fwd_gemm<1, kGroup>, num_sms, &u));
+        gemm(persistent_units<Fwd2>(tern_fwd_gemm<2, kGroup>, num_sms, &u));
+        gemm(persistent_units<Dx1>(tern_dx_gemm<1, kGroup>, num_sms, &u));
+        gemm(persistent_units<Dx2>(tern_dx_gemm<2, kGroup>, num_sms, &u));
+        gemm(persistent_units<Dw1>(tern_dw_gemm<1, kGroup>, num_sms, &u));
+        gemm(persistent_units<Dw2>(tern_dw_gemm<2, kGroup>, num_sms, &u));
         cudaFuncAttributes fa;
         auto load = [&](cudaError_t e) {
             if (st == TERN_OK && e != cudaSuccess) st = TERN_ERR_CUDA;
         };
         load(cudaFuncGetAttributes(&fa, tern_dw_split_reduce<1>));
-        load(cudaFuncGetAttributes(&fa, tern_dw_split_reduce<8>));
+        load(cudaFuncGetAttributes(&fa, tern_dw_split_reduce<kGroup>));
         load(cudaFuncGetAttributes(&fa, tern_sgrad_reduce));
         load(cudaFuncGetAttributes(&fa, tern_sgrad_reduce_group));
         status[dev] = st;

@@ -27,10 +27,16 @@
  * encoder).  Inputs must not alias outputs.
  *
  * Errors: every call returns TERN_OK (0) or a negative status, checks its
- * arguments before enqueueing anything, and never exits the process.  Kernels
- * that wait on the tensor-core pipeline give up after a bounded time and
- * record TERN_ERR_TIMEOUT in a device status word that tern_device_status()
- * reads back.
+ * arguments before enqueueing anything, and never exits the process.  Inside
+ * the GEMM kernels, every wait on the tensor-core pipeline (an mbarrier between
+ * the TMA producer, the MMA issuer and the epilogue) gives up after a bounded
+ * time and records TERN_ERR_TIMEOUT in a device status word that
+ * tern_device_status() reads back.  Three waits of a GEMM's set-up have no
+ * bound, because the hardware gives none: the tensor-memory allocation
+ * (tcgen05.alloc), the cluster barrier of a CTA pair and the dependent-launch
+ * wait.  The GEMMs are launched with full stream serialization (no
+ * programmatic dependent launch), so a GEMM starts only after every earlier
+ * kernel on its stream has completed and those waits never wait on another grid.
  */
 #ifndef TERN_H
 #define TERN_H
@@ -172,13 +178,16 @@ typedef struct tern_layer {
  * Y_bf16, when given, receives Y rounded to bf16 from the same epilogue, so the
  * next layer of a chain reads its input without a separate cast; Y may then be
  * NULL.
- * Layers are launched up to eight at a time; a layer's Y must not overlap
+ * Layers are launched up to six at a time; a layer's Y must not overlap
  * another layer's inputs.
- * Known issue: in a process that had first run long single-layer steps of a large
- * projection, a sequence of eager grouped calls (forward and backward of a block)
- * has stalled, with one CTA pair of a GEMM unable to finish its set-up (tensor
- * memory allocation, cluster barrier); the same calls in a fresh process have not.  The cause is not known;
- * tern_device_diagnostics reports the state if it happens.
+ * Known issue of an earlier build: with the GEMMs launched by programmatic
+ * dependent launch (their set-up overlapping the previous kernel), a process that
+ * had first run long single-layer steps of a large projection and then a sequence
+ * of eager grouped calls stalled, with one CTA pair of a GEMM unable to finish its
+ * set-up (tensor-memory allocation, cluster barrier).  The cause was not found.
+ * The GEMMs are now launched with full stream serialization, so that set-up no
+ * longer overlaps any other grid; tern_device_diagnostics reports the state
+ * should a stall happen.
  */
 int tern_linear_fwd_grouped(const tern_layer* layers, int count, void* stream);
 

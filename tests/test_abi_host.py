@@ -134,8 +134,8 @@ def test_noalloc_rejects_sizes_beyond_its_scratch_before_touching_the_device(lib
 def test_grouped_workspace_and_argument_checks(lib):
     shapes = [(1024, 512, 512)] * 4
     # sgrad partials of each layer (4 x 128-row blocks x 4 quarters x 512 columns), then
-    # 128 split tiles of 256 x 256 fp32 (the group has 4 x 4 tiles x 16 k-blocks to split)
-    assert lib.tern_linear_bwd_grouped_workspace(shapes) == 4 * (4 * 4 * 512 * 4) + 128 * 256 * 256 * 4
+    # 256 split tiles of 256 x 256 fp32 (the group has 4 x 4 tiles x 16 k-blocks to split)
+    assert lib.tern_linear_bwd_grouped_workspace(shapes) == 4 * (4 * 4 * 512 * 4) + 256 * 256 * 256 * 4
     assert lib.tern_linear_bwd_grouped_workspace([(0, 512, 512)]) == 0
     t = _tiles(lib)
     arr = (lib._Layer * 2)()
