@@ -367,7 +367,8 @@ def rwkv_block(bl, dev, stream, steps):
                     the output projection, the channel-mixing key and value one after
                     another (and the reverse in the backward);
       per_layer     the single-layer calls.
-    Each is timed eager and replayed as one CUDA graph."""
+    Each is timed eager and replayed as one CUDA graph.  The grouped schedules use the
+    prepared calls (arguments marshalled once); per_layer uses the plain functions."""
     import torch
     M = 8192
     shapes = syn.RWKV_SHAPES
@@ -388,14 +389,12 @@ def rwkv_block(bl, dev, stream, steps):
         layers.append(L)
     adam_scalars = torch.tensor([ADAM_HP["lr"], 1 - ADAM_HP["b1"], 1 - ADAM_HP["b2"], 1.0], device=dev)
 
-    def materialise_all():
-        for L in layers:
-            bl.tern_materialize(L["q"], L["scale"], L["tiles"], 2, 7)
-
-    def adam_all():
-        bl.adamw_step_multi([L["scale"] for L in layers], [L["sgrad"] for L in layers], [L["m"] for L in layers],
-                            [L["v"] for L in layers], adam_scalars, ADAM_HP["b1"], ADAM_HP["b2"], ADAM_HP["eps"],
-                            ADAM_HP["wd"])
+    # the grouped schedules call the library through prepared calls (arguments marshalled
+    # once), as a training loop repeating the step on the same buffers does
+    mats = [bl.Materialize(L["q"], L["scale"], L["tiles"], 2, 7) for L in layers]
+    adam_all = bl.MultiAdamW([L["scale"] for L in layers], [L["sgrad"] for L in layers], [L["m"] for L in layers],
+                             [L["v"] for L in layers], adam_scalars, ADAM_HP["b1"], ADAM_HP["b2"], ADAM_HP["eps"],
+                             ADAM_HP["wd"])
 
     def per_layer():
         for L in layers:
@@ -405,18 +404,23 @@ def rwkv_block(bl, dev, stream, steps):
             bl.adamw_step(L["scale"], L["sgrad"], L["m"], L["v"], 1, **ADAM_HP)
 
     def grouped(fwd_groups, bwd_groups):
-        gws = {tuple(gr): torch.empty(bl.tern_linear_bwd_grouped_workspace(
-            [(M, layers[i]["K"], layers[i]["N"]) for i in gr]) // 4, device=dev) for gr in bwd_groups}
+        fwds = [bl.GroupedForward([dict(X=layers[i]["X"], tiles=layers[i]["tiles"], scale=layers[i]["scale"],
+                                        Y=layers[i]["Y"]) for i in gr]) for gr in fwd_groups]
+        bwds = []
+        for gr in bwd_groups:
+            ws_ = torch.empty(bl.tern_linear_bwd_grouped_workspace([(M, layers[i]["K"], layers[i]["N"]) for i in gr])
+                              // 4, device=dev)
+            bwds.append(bl.GroupedBackward([dict(X=layers[i]["X"], dY=layers[i]["dY"], tiles=layers[i]["tiles"],
+                                                 scale=layers[i]["scale"], dX=layers[i]["dX"], gq=layers[i]["gq"],
+                                                 sgrad=layers[i]["sgrad"]) for i in gr], ws_))
 
         def step():
-            materialise_all()
-            for gr in fwd_groups:
-                bl.tern_linear_fwd_grouped([dict(X=layers[i]["X"], tiles=layers[i]["tiles"],
-                                                 scale=layers[i]["scale"], Y=layers[i]["Y"]) for i in gr])
-            for gr in bwd_groups:
-                bl.tern_linear_bwd_grouped([dict(X=layers[i]["X"], dY=layers[i]["dY"], tiles=layers[i]["tiles"],
-                                                 scale=layers[i]["scale"], dX=layers[i]["dX"], gq=layers[i]["gq"],
-                                                 sgrad=layers[i]["sgrad"]) for i in gr], gws[tuple(gr)])
+            for m_ in mats:
+                m_()
+            for f_ in fwds:
+                f_()
+            for b_ in bwds:
+                b_()
             adam_all()
         return step
 

@@ -9,6 +9,10 @@ current stream.  The functions carry the C names:
     tern_linear_bwd(X, dY, tiles, scale, dX, gq, sgrad, workspace)
     adamw_step(w, g, m, v, t, lr, b1, b2, eps, wd, gmul=1.0, decoupled=True)
 
+Materialize, GroupedForward, GroupedBackward and MultiAdamW are the same calls with
+their arguments checked and marshalled once, for loops that repeat them on the
+same buffers.
+
 Importing this package loads ``lib/libtern.so``; if it is missing the import
 fails (run ``bit_linear_gb300.build.build()`` or ``__graft_entry__.build()``).
 There is no fallback path.
@@ -171,16 +175,25 @@ def tern_tiles_bytes(K, N, which) -> int:
     return int(lib.tern_tiles_bytes(int(K), int(N), int(which)))
 
 
+class Materialize:
+    """tern_materialize with its arguments marshalled once; see GroupedForward."""
+
+    def __init__(self, q, scale, tiles: Tiles, theta=2, q_clamp=7, q_clamped=None):
+        K, N = q.shape
+        if (tiles.K, tiles.N) != (K, N):
+            raise ValueError("tiles shape does not match q")
+        self._ct = tiles._c()
+        self._args = (_ptr(q, torch.int8, (K, N), "q"), _ptr(q_clamped, torch.int8, (K, N), "q_clamped"),
+                      _ptr(scale, torch.float32, (N,), "scale"), K, N, int(theta), int(q_clamp),
+                      ctypes.byref(self._ct))
+        self._refs = (q, scale, tiles, q_clamped)
+
+    def __call__(self, stream=None):
+        _check(lib.tern_materialize(*self._args, _stream(stream)), "tern_materialize")
+
+
 def tern_materialize(q, scale, tiles: Tiles, theta=2, q_clamp=7, q_clamped=None, stream=None):
-    K, N = q.shape
-    if (tiles.K, tiles.N) != (K, N):
-        raise ValueError("tiles shape does not match q")
-    ct = tiles._c()
-    _check(lib.tern_materialize(_ptr(q, torch.int8, (K, N), "q"),
-                                _ptr(q_clamped, torch.int8, (K, N), "q_clamped"),
-                                _ptr(scale, torch.float32, (N,), "scale"),
-                                K, N, int(theta), int(q_clamp), ctypes.byref(ct), _stream(stream)),
-           "tern_materialize")
+    Materialize(q, scale, tiles, theta, q_clamp, q_clamped)(stream)
 
 
 def tern_linear_fwd(X, tiles: Tiles, scale, Y, stream=None):
@@ -262,10 +275,40 @@ def _layers(layers, backward):
     return arr, keep
 
 
+class GroupedForward:
+    """tern_linear_fwd_grouped with its arguments checked and marshalled once: calling
+    the object enqueues the grouped forward of the same buffers again (a training loop
+    calls it every step).  It keeps references to the tensors it was given."""
+
+    def __init__(self, layers):
+        self._arr, self._keep = _layers(layers, False)
+        self._n = len(layers)
+        self._refs = list(layers)
+
+    def __call__(self, stream=None):
+        _check(lib.tern_linear_fwd_grouped(self._arr, self._n, _stream(stream)), "tern_linear_fwd_grouped")
+
+
+class GroupedBackward:
+    """tern_linear_bwd_grouped with its arguments (and workspace) marshalled once; see
+    GroupedForward."""
+
+    def __init__(self, layers, workspace, accumulate=False):
+        self._arr, self._keep = _layers(layers, True)
+        self._n = len(layers)
+        self._ws = _ptr(workspace, workspace.dtype, None, "workspace")
+        self._ws_bytes = workspace.numel() * workspace.element_size()
+        self._flags = TERN_BWD_ACCUMULATE if accumulate else 0
+        self._refs = (list(layers), workspace)
+
+    def __call__(self, stream=None):
+        _check(lib.tern_linear_bwd_grouped(self._arr, self._n, self._ws, self._ws_bytes, self._flags,
+                                           _stream(stream)), "tern_linear_bwd_grouped")
+
+
 def tern_linear_fwd_grouped(layers, stream=None):
     """Y = X * W_eff for every layer (dicts with X, tiles, scale, Y and/or Y_bf16), in grouped launches."""
-    arr, _keep = _layers(layers, False)
-    _check(lib.tern_linear_fwd_grouped(arr, len(layers), _stream(stream)), "tern_linear_fwd_grouped")
+    GroupedForward(layers)(stream)
 
 
 def tern_linear_bwd_grouped_workspace(shapes) -> int:
@@ -279,11 +322,7 @@ def tern_linear_bwd_grouped_workspace(shapes) -> int:
 def tern_linear_bwd_grouped(layers, workspace, stream=None, accumulate=False):
     """dX (fp32 and/or bf16), gq and sgrad for every layer (dicts with X, dY, tiles, scale, dX, dX_bf16,
     gq, sgrad)."""
-    arr, _keep = _layers(layers, True)
-    ws_bytes = workspace.numel() * workspace.element_size()
-    _check(lib.tern_linear_bwd_grouped(arr, len(layers), _ptr(workspace, workspace.dtype, None, "workspace"),
-                                       ws_bytes, TERN_BWD_ACCUMULATE if accumulate else 0, _stream(stream)),
-           "tern_linear_bwd_grouped")
+    GroupedBackward(layers, workspace, accumulate)(stream)
 
 
 def adamw_step(w, g, m, v, t, lr, b1, b2, eps, wd, gmul=1.0, decoupled=True, stream=None):
@@ -324,24 +363,35 @@ def tern_grad_sumsq(grads, sumsq, workspace, stream=None):
            "tern_grad_sumsq")
 
 
+class MultiAdamW:
+    """adamw_step_multi with its arguments marshalled once (the per-step scalars stay in
+    device memory, so the same call serves every step); see GroupedForward."""
+
+    def __init__(self, ws, gs, ms, vs, scalars, b1, b2, eps, wd, decoupled=True, sumsq=None, max_norm=0.0,
+                 skipped=None):
+        k = len(ws)
+        if not (len(gs) == len(ms) == len(vs) == k):
+            raise ValueError("w, g, m, v lists differ in length")
+        for i in range(k):
+            if not (ws[i].numel() == gs[i].numel() == ms[i].numel() == vs[i].numel()):
+                raise ValueError(f"tensor {i}: w, g, m, v sizes differ")
+        self._args = (_ptr_array(ws, torch.float32, "w"), _ptr_array(gs, torch.float32, "g"),
+                      _ptr_array(ms, torch.float32, "m"), _ptr_array(vs, torch.float32, "v"), _n_array(ws), k,
+                      _ptr(scalars, torch.float32, (4,), "scalars"), float(b1), float(b2), float(eps), float(wd),
+                      1 if decoupled else 0, _ptr(sumsq, torch.float64, None, "sumsq"), float(max_norm),
+                      _ptr(skipped, torch.int32, None, "skipped"))
+        self._refs = (list(ws), list(gs), list(ms), list(vs), scalars, sumsq, skipped)
+
+    def __call__(self, stream=None):
+        _check(lib.adamw_step_multi(*self._args, _stream(stream)), "adamw_step_multi")
+
+
 def adamw_step_multi(ws, gs, ms, vs, scalars, b1, b2, eps, wd, decoupled=True, sumsq=None, max_norm=0.0,
                      skipped=None, stream=None):
     """AdamW over several tensors in one launch; `scalars` is a device float32 [4]
     tensor {lr, bc1, bc2, gmul}; `sumsq` (device float64 [1]) enables the global-norm
     clip (max_norm > 0) and the non-finite skip; `skipped` is a device int32 [1]."""
-    k = len(ws)
-    if not (len(gs) == len(ms) == len(vs) == k):
-        raise ValueError("w, g, m, v lists differ in length")
-    for i in range(k):
-        if not (ws[i].numel() == gs[i].numel() == ms[i].numel() == vs[i].numel()):
-            raise ValueError(f"tensor {i}: w, g, m, v sizes differ")
-    _check(lib.adamw_step_multi(_ptr_array(ws, torch.float32, "w"), _ptr_array(gs, torch.float32, "g"),
-                                _ptr_array(ms, torch.float32, "m"), _ptr_array(vs, torch.float32, "v"),
-                                _n_array(ws), k, _ptr(scalars, torch.float32, (4,), "scalars"), float(b1),
-                                float(b2), float(eps), float(wd), 1 if decoupled else 0,
-                                _ptr(sumsq, torch.float64, None, "sumsq"), float(max_norm),
-                                _ptr(skipped, torch.int32, None, "skipped"), _stream(stream)),
-           "adamw_step_multi")
+    MultiAdamW(ws, gs, ms, vs, scalars, b1, b2, eps, wd, decoupled, sumsq, max_norm, skipped)(stream)
 
 
 def tern_sr4_workspace(numel) -> int:

@@ -274,28 +274,36 @@ __device__ __forceinline__ void store_chunk(const CUtensorMap* map, uint32_t sta
     ++nchunk;
 }
 
-// One 32-column chunk of a warp's 32 rows: r[] is row `row` (the warp's rows start at
-// `wrow`), columns c0..c0+31.  tile128 is the index of the 128-row block the rows lie in.
+// A tile's column scales, spread over the warp: lane l holds columns 8l..8l+7 of the
+// tile starting at column col0 (zeros past the last column).  Loaded one tile ahead of
+// their use, so that no chunk waits on a cold load.
+__device__ __forceinline__ void load_tile_scales(const float* scale, int col0, int Ng, int lane, float (&sc)[8]) {
+    const int c = col0 + 8 * lane;   // N % 16 == 0: the eight columns are all in range or all out
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+    if (scale != nullptr && c < Ng) {
+        a = __ldg(reinterpret_cast<const float4*>(scale + c));
+        b = __ldg(reinterpret_cast<const float4*>(scale + c + 4));
+    }
+    sc[0] = a.x, sc[1] = a.y, sc[2] = a.z, sc[3] = a.w, sc[4] = b.x, sc[5] = b.y, sc[6] = b.z, sc[7] = b.w;
+}
+
+// One 32-column chunk j of a warp's 32 rows: r[] is row `row` (the warp's rows start at
+// `wrow`), columns c0..c0+31 (c0 = the tile's first column + 32j); sc holds the tile's
+// scales as load_tile_scales spreads them.  tile128 is the index of the 128-row block
+// the rows lie in.
 template <class C>
 __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const CUtensorMap* omap, uint32_t stage,
-                                               int& nchunk, const uint32_t (&r)[32], int row, int wrow, int c0,
-                                               int tile128, int quad, int lane) {
+                                               int& nchunk, const uint32_t (&r)[32], const float (&sc)[8], int j,
+                                               int row, int wrow, int c0, int tile128, int quad, int lane) {
     const bool row_ok = row < a.Mg;
     const bool hi_ok = c0 + 16 < a.Ng;   // N is a multiple of 16: the chunk's second half may lie past it
     float v[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
     if (C::EPI == EPI_FWD || (C::EPI == EPI_DW && a.out != nullptr)) {
+        // column c0 + i of the chunk is register i % 8 of lane 4j + i / 8
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            if (q < 4 || hi_ok) {
-                const float4 sc = __ldg(reinterpret_cast<const float4*>(a.scale + c0 + 4 * q));
-                v[4 * q] *= sc.x;
-                v[4 * q + 1] *= sc.y;
-                v[4 * q + 2] *= sc.z;
-                v[4 * q + 3] *= sc.w;
-            }
-        }
+        for (int i = 0; i < 32; ++i) v[i] *= __shfl_sync(0xffffffffu, sc[i & 7], 4 * j + (i >> 3));
     }
     // fp32 output through shared memory and TMA (gq += ... with accumulate: a TMA add);
     // the condition is the same for the whole warp
@@ -539,6 +547,26 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
         const uint32_t stage = staging0 + static_cast<uint32_t>(warp - 2) * 2u * kStageBuf;
         int nchunk = 0;   // chunks this warp has staged (its buffer parity)
         int local = 0;
+        // the column scales of a unit's tile (none for dX and for split units' raw tiles)
+        auto unit_scales = [&](int ugn, float (&sc)[8]) {
+            const float* sp = nullptr;
+            int col0 = 0, ng = 0;
+            if (C::EPI != EPI_DX && ugn < total_units) {
+                const int pn = group_find(grp, ugn);
+                const GemmArgs& an = grp.args[pn];
+                if (an.partial_g == nullptr && (C::EPI == EPI_FWD || an.out != nullptr)) {
+                    int mtn, ntn;
+                    tile_coords<16 / CG>(an.tile_begin + (ugn - grp.unit_begin[pn]) / an.split, an.tiles_m,
+                                         an.tiles_n, mtn, ntn);
+                    sp = an.scale;
+                    col0 = ntn * C::BN;
+                    ng = an.Ng;
+                }
+            }
+            load_tile_scales(sp, col0, ng, lane, sc);
+        };
+        float sc_cur[8], sc_next[8];
+        unit_scales(unit, sc_cur);
         for (int ug = unit; ug < total_units; ug += units, ++local) {
             const int p = group_find(grp, ug);
             const GemmArgs& a = grp.args[p];
@@ -549,6 +577,7 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
             const bool full = wait_bounded(TFULL0 + 8u * acc, acc_parity, abort_flag, true, SITE + 7);
             if (!__all_sync(0xffffffffu, full)) break;
             ptx::tc_fence_after();
+            unit_scales(ug + units, sc_next);   // in flight while this tile drains
             int mt, nt;
             tile_coords<16 / CG>(a.tile_begin + u / a.split, a.tiles_m, a.tiles_n, mt, nt);
             const int row0 = mt * C::TILE_M + static_cast<int>(rank) * kBM;
@@ -578,9 +607,12 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
                     uint32_t r[32];
                     ptx::tmem_ld_32x32b_x32(trow + j * 32, r);
                     ptx::tmem_wait_ld();
-                    epilogue_chunk<C>(a, omap, stage, nchunk, r, wrow + lane, wrow, c0, tile128, quad, lane);
+                    epilogue_chunk<C>(a, omap, stage, nchunk, r, sc_cur, j, wrow + lane, wrow, c0, tile128, quad,
+                                      lane);
                 }
             }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) sc_cur[i] = sc_next[i];
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -815,34 +847,73 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+// Encoded tensor maps, cached per process: a map depends only on the address, the
+// element type, the extents, the box and the swizzle (not on the device or stream),
+// so a call that repeats a layer's buffers (every training step) reuses its maps
+// instead of encoding them again on the host.  Direct-mapped, 1024 entries.
+struct MapKey {
+    const void* ptr;
+    int64_t inner, outer;
+    int box_inner, box_outer, sw, dtype;
+    bool operator==(const MapKey& o) const {
+        return ptr == o.ptr && inner == o.inner && outer == o.outer && box_inner == o.box_inner &&
+               box_outer == o.box_outer && sw == o.sw && dtype == o.dtype;
+    }
+};
+struct MapSlot {
+    MapKey key;
+    CUtensorMap map;
+    bool valid;
+};
+constexpr int kMapCache = 1024;
+MapSlot g_map_cache[kMapCache];
+std::mutex g_map_mu;
+
+int encode_2d(CUtensorMap* m, const MapKey& k) {
+    size_t h = reinterpret_cast<uintptr_t>(k.ptr) >> 4;
+    h ^= static_cast<size_t>(k.inner) * 0x9E3779B97F4A7C15ull ^ static_cast<size_t>(k.outer) * 0xC2B2AE3D27D4EB4Full;
+    h ^= static_cast<size_t>(k.box_inner * 131 + k.box_outer * 7 + k.sw * 3 + k.dtype) * 0x165667B19E3779F9ull;
+    MapSlot& slot = g_map_cache[(h ^ (h >> 29)) % kMapCache];
+    {
+        std::lock_guard<std::mutex> lock(g_map_mu);
+        if (slot.valid && slot.key == k) {
+            *m = slot.map;
+            return TERN_OK;
+        }
+    }
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return TERN_ERR_CUDA;
+    const int esize = k.dtype == CU_TENSOR_MAP_DATA_TYPE_FLOAT32 ? 4 : 2;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(k.inner), static_cast<cuuint64_t>(k.outer)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(k.inner) * esize};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(k.box_inner), static_cast<cuuint32_t>(k.box_outer)};
+    cuuint32_t estr[2] = {1, 1};
+    // operands are read with 256-byte L2 promotion; outputs are only written
+    const CUtensorMapL2promotion l2 =
+        esize == 2 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_NONE;
+    CUresult r = enc(m, static_cast<CUtensorMapDataType>(k.dtype), 2, const_cast<void*>(k.ptr), dims, strides, box,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, static_cast<CUtensorMapSwizzle>(k.sw), l2,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return TERN_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    slot.key = k;
+    slot.map = *m;
+    slot.valid = true;
+    return TERN_OK;
+}
+
 // Tensor map of a row-major bf16 matrix [outer][inner] read in boxes of box_outer x box_inner.
 int map_bf16(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, int box_inner, int box_outer,
              CUtensorMapSwizzle sw) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return TERN_ERR_CUDA;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * 2};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer)};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? TERN_OK : TERN_ERR_CUDA;
+    return encode_2d(m, MapKey{ptr, inner, outer, box_inner, box_outer, static_cast<int>(sw),
+                               static_cast<int>(CU_TENSOR_MAP_DATA_TYPE_BFLOAT16)});
 }
 
 // Tensor map of a row-major fp32 output [rows][cols], written by the epilogues in boxes
 // of 32 x 32 with the 128-byte swizzle (cols % 4 == 0, base 16-byte aligned).
 int map_f32_out(CUtensorMap* m, const float* ptr, int64_t cols, int64_t rows) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return TERN_ERR_CUDA;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 4};
-    cuuint32_t box[2] = {32, 32};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(ptr), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? TERN_OK : TERN_ERR_CUDA;
+    return encode_2d(m, MapKey{ptr, cols, rows, 32, 32, static_cast<int>(CU_TENSOR_MAP_SWIZZLE_128B),
+                               static_cast<int>(CU_TENSOR_MAP_DATA_TYPE_FLOAT32)});
 }
 
 // Boxes of one operand: K-major tiles are read as one box of BK x rows; MN-major

@@ -208,3 +208,43 @@ def test_two_layer_chain_through_bf16(cuda_lib):
     torch.cuda.synchronize()
     assert torch.equal(Y2, L2.Y) and torch.equal(dX1, L1.dX)
     assert torch.isfinite(L1.gq).all() and torch.isfinite(L2.sgrad).all()
+
+
+def test_prepared_calls_repeat_the_plain_calls(cuda_lib):
+    """Materialize, GroupedForward, GroupedBackward and MultiAdamW (arguments marshalled
+    once) give the plain functions' results, call after call."""
+    bl = cuda_lib
+    layers = _layers(MIXED[:4], 700)
+    ws = _workspace(bl, layers)
+    fwd = bl.GroupedForward(_fwd_dicts(layers))
+    bwd = bl.GroupedBackward(_bwd_dicts(layers), ws)
+    mats = [bl.Materialize(L.q, L.scale, L.tiles, 2, 7) for L in layers]
+    for _ in range(2):
+        for m in mats:
+            m()
+        fwd()
+        bwd()
+        assert bl.tern_device_status() == bl.TERN_OK
+        for L in layers:
+            full_oracle_check(L)
+    ref = [(L.Y.clone(), L.dX.clone()) for L in layers]
+    bl.tern_linear_fwd_grouped(_fwd_dicts(layers))
+    bl.tern_linear_bwd_grouped(_bwd_dicts(layers), ws)
+    torch.cuda.synchronize()
+    for L, (Y, dX) in zip(layers, ref):
+        assert torch.equal(L.Y, Y) and torch.equal(L.dX, dX)
+    n = [L.N for L in layers]
+    w = [L.scale.clone() for L in layers]
+    g = [L.sgrad.clone() for L in layers]
+    m1, v1 = [torch.zeros(k, device="cuda") for k in n], [torch.zeros(k, device="cuda") for k in n]
+    m2, v2 = [torch.zeros(k, device="cuda") for k in n], [torch.zeros(k, device="cuda") for k in n]
+    w2 = [x.clone() for x in w]
+    sc = torch.tensor([1e-3, 0.1, 0.05, 1.0], device="cuda")
+    prep = bl.MultiAdamW(w, g, m1, v1, sc, 0.9, 0.95, 1e-8, 0.1)
+    prep()
+    prep()
+    bl.adamw_step_multi(w2, g, m2, v2, sc, 0.9, 0.95, 1e-8, 0.1)
+    bl.adamw_step_multi(w2, g, m2, v2, sc, 0.9, 0.95, 1e-8, 0.1)
+    torch.cuda.synchronize()
+    for a, b in zip(w + m1 + v1, w2 + m2 + v2):
+        assert torch.equal(a, b)
