@@ -367,7 +367,9 @@ def rwkv_block(bl, dev, stream, steps):
                     the output projection, the channel-mixing key and value one after
                     another (and the reverse in the backward);
       per_layer     the single-layer calls.
-    Each is timed eager and replayed as one CUDA graph.  The grouped schedules use the
+    independent_2bit_T is the independent schedule with the forward reading T as the 2-bit
+    codes (materialise then skips the bf16 T plane).  Each is timed eager and replayed as
+    one CUDA graph.  The grouped schedules use the
     prepared calls (arguments marshalled once); per_layer uses the plain functions."""
     import torch
     M = 8192
@@ -391,7 +393,6 @@ def rwkv_block(bl, dev, stream, steps):
 
     # the grouped schedules call the library through prepared calls (arguments marshalled
     # once), as a training loop repeating the step on the same buffers does
-    mats = [bl.Materialize(L["q"], L["scale"], L["tiles"], 2, 7) for L in layers]
     adam_all = bl.MultiAdamW([L["scale"] for L in layers], [L["sgrad"] for L in layers], [L["m"] for L in layers],
                              [L["v"] for L in layers], adam_scalars, ADAM_HP["b1"], ADAM_HP["b2"], ADAM_HP["eps"],
                              ADAM_HP["wd"])
@@ -403,19 +404,23 @@ def rwkv_block(bl, dev, stream, steps):
             bl.tern_linear_bwd(L["X"], L["dY"], L["tiles"], L["scale"], L["dX"], L["gq"], L["sgrad"], L["ws"])
             bl.adamw_step(L["scale"], L["sgrad"], L["m"], L["v"], 1, **ADAM_HP)
 
-    def grouped(fwd_groups, bwd_groups):
-        fwds = [bl.GroupedForward([dict(X=layers[i]["X"], tiles=layers[i]["tiles"], scale=layers[i]["scale"],
+    def grouped(fwd_groups, bwd_groups, packed_t=False):
+        # packed_t: the forward reads T as the 2-bit codes and materialise skips the bf16 T plane
+        tl = [bl.Tiles(L["K"], L["N"], packed=L["tiles"].packed, whi_bf16=L["tiles"].whi_bf16,
+                       wlo_bf16=L["tiles"].wlo_bf16) if packed_t else L["tiles"] for L in layers]
+        mats_ = [bl.Materialize(L["q"], L["scale"], t_, 2, 7) for L, t_ in zip(layers, tl)]
+        fwds = [bl.GroupedForward([dict(X=layers[i]["X"], tiles=tl[i], scale=layers[i]["scale"],
                                         Y=layers[i]["Y"]) for i in gr]) for gr in fwd_groups]
         bwds = []
         for gr in bwd_groups:
             ws_ = torch.empty(bl.tern_linear_bwd_grouped_workspace([(M, layers[i]["K"], layers[i]["N"]) for i in gr])
                               // 4, device=dev)
-            bwds.append(bl.GroupedBackward([dict(X=layers[i]["X"], dY=layers[i]["dY"], tiles=layers[i]["tiles"],
+            bwds.append(bl.GroupedBackward([dict(X=layers[i]["X"], dY=layers[i]["dY"], tiles=tl[i],
                                                  scale=layers[i]["scale"], dX=layers[i]["dX"], gq=layers[i]["gq"],
                                                  sgrad=layers[i]["sgrad"]) for i in gr], ws_))
 
         def step():
-            for m_ in mats:
+            for m_ in mats_:
                 m_()
             for f_ in fwds:
                 f_()
@@ -426,10 +431,12 @@ def rwkv_block(bl, dev, stream, steps):
 
     schedules = {
         "independent": grouped([[0, 1, 2, 3, 4, 5]], [[0, 1, 2, 3, 4, 5]]),
+        "independent_2bit_T": grouped([[0, 1, 2, 3, 4, 5]], [[0, 1, 2, 3, 4, 5]], packed_t=True),
         "dependency": grouped([[0, 1, 2], [3], [4], [5]], [[5], [4], [3], [0, 1, 2]]),
         "per_layer": per_layer,
     }
-    launches = {"independent": 6 + 1 + 4 + 1, "dependency": 6 + 4 + 4 * 3 + 1, "per_layer": 6 * 6}
+    launches = {"independent": 6 + 1 + 4 + 1, "independent_2bit_T": 6 + 1 + 4 + 1, "dependency": 6 + 4 + 4 * 3 + 1,
+                "per_layer": 6 * 6}
     flops = 6.0 * M * sum(K * N for K, N in shapes)
     reps = max(20, min(steps, 200))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -663,7 +670,9 @@ def run_ours(args):
     scale0 = torch.from_numpy(inp.scale).to(dev)
     scale = scale0.clone()
     ms, vs = torch.zeros(N, device=dev), torch.zeros(N, device=dev)
-    tiles = bl.Tiles.empty(K, N)
+    # the forward's T operand: bf16 planes (t_operand "bf16") or the 2-bit codes expanded
+    # inside the GEMM ("packed": the materialise pass then skips the bf16 T plane)
+    tiles = bl.Tiles.empty(K, N, t=(args.t_operand == "bf16"))
     Y = torch.empty(M, N, device=dev)
     dX = torch.empty(M, K, device=dev)
     gq = torch.empty(K, N, device=dev)
@@ -673,22 +682,23 @@ def run_ours(args):
     names = ["materialize", "fwd", "dx", "dw", "adamw"]
     step_no = [0]
 
-    def step(ev=None, Xs=None, dYs=None):
+    def step(ev=None, Xs=None, dYs=None, tl=None):
         Xs = X if Xs is None else Xs
         dYs = dY if dYs is None else dYs
+        tl = tiles if tl is None else tl
         step_no[0] += 1
         if ev is not None:
             ev[0].record(stream)
-        bl.tern_materialize(q, scale, tiles, 2, 7)
+        bl.tern_materialize(q, scale, tl, 2, 7)
         if ev is not None:
             ev[1].record(stream)
-        bl.tern_linear_fwd(Xs, tiles, scale, Y)
+        bl.tern_linear_fwd(Xs, tl, scale, Y)
         if ev is not None:
             ev[2].record(stream)
-        bl.tern_linear_bwd(Xs, dYs, tiles, scale, dX, None, None, None)
+        bl.tern_linear_bwd(Xs, dYs, tl, scale, dX, None, None, None)
         if ev is not None:
             ev[3].record(stream)
-        bl.tern_linear_bwd(Xs, dYs, tiles, scale, None, gq, sgrad, wsp)
+        bl.tern_linear_bwd(Xs, dYs, tl, scale, None, gq, sgrad, wsp)
         if ev is not None:
             ev[4].record(stream)
         bl.adamw_step(scale, sgrad, ms, vs, step_no[0], **ADAM_HP)
@@ -741,7 +751,7 @@ def run_ours(args):
         kern[n]["frac_of_measured_burst"] = kern[n]["tflops"] / pk["bf16"]
     # dX runs two bf16 passes (W_hi and W_lo) into one accumulator: 4*M*K*N executed
     kern["dx"]["executed_tflops"] = 2.0 * kern["dx"]["tflops"]
-    mat_bytes = K * N * (1 + 0.25 + 2 + 2 + 2) + N * 4
+    mat_bytes = K * N * (1 + 0.25 + (2 if args.t_operand == "bf16" else 0) + 2 + 2) + N * 4
     kern["materialize"]["gbs"] = mat_bytes / (per["materialize"] * 1e-3) / 1e9
     kern["materialize"]["frac_of_measured_hbm"] = kern["materialize"]["gbs"] / pk["hbm"]
     dom = max(credited, key=lambda n: per[n])
@@ -755,6 +765,26 @@ def run_ours(args):
             "frac_of_measured_sustained": kern[dom]["tflops"] / pk["bf16_sus"],
             "credited": "2*M*K*N per launch" + (" (the kernel executes twice that: two bf16 passes)"
                                                 if dom == "dx" else "")}
+
+    # ---- the same step with the forward's other T operand (bf16 plane or 2-bit codes)
+    progress("step with the other forward operand")
+    other = "packed" if args.t_operand == "bf16" else "bf16"
+    tiles_o = bl.Tiles.empty(K, N, t=(other == "bf16"))
+    for _ in range(3):
+        step(tl=tiles_o)
+    torch.cuda.synchronize()
+    evo = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        step(evo[i], tl=tiles_o)
+    torch.cuda.synchronize()
+    if bl.tern_device_status() != bl.TERN_OK:
+        raise RuntimeError("a kernel gave up on a bounded wait (other forward operand)")
+    per_o = {n: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evo) for j, n in enumerate(names)}
+    ms_o = evo[0][0].elapsed_time(evo[-1][5]) / args.steps
+    variant = {"t_operand": other, "ms_per_step": ms_o, "tflops": flops / (ms_o * 1e-3) / 1e12,
+               "kernels_ms": per_o, "fwd_tflops": 2.0 * M * K * N / (per_o["fwd"] * 1e-3) / 1e12,
+               "materialize_bytes_per_weight": 1 + 0.25 + (2 if other == "bf16" else 0) + 4}
+    del tiles_o
 
     # ---- end to end through the C ABI: every step's inputs X and dY copied from
     #      pinned host memory and the step's result (updated scales and their
@@ -846,7 +876,8 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": large_config(M, K, N, ws),
+            "config": dict(large_config(M, K, N, ws), t_operand=args.t_operand),
+            "other_t_operand": variant,
             "frac_of_peak": {"spec_dense_bf16_2250": value / ws / SPEC_BF16_TFLOPS,
                              "measured_burst": value / ws / pk["bf16"],
                              "measured_sustained": value / ws / pk["bf16_sus"],
@@ -994,6 +1025,8 @@ def main():
     ap.add_argument("--extras-limit", type=float, default=300.0,
                     help="seconds after which the bandwidth sweeps are cut (the headline line is printed)")
     ap.add_argument("--skip-workloads", action="store_true", help="leave out the RWKV block and the FFN chain")
+    ap.add_argument("--t-operand", choices=["bf16", "packed"], default="bf16",
+                    help="the forward's T operand: the bf16 plane, or the 2-bit codes expanded inside the GEMM")
     ap.add_argument("--workload-limit", type=float, default=300.0,
                     help="seconds after which a child workload process is killed")
     args = ap.parse_args()

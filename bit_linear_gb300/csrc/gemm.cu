@@ -91,6 +91,7 @@ struct GemmArgs {
     int tile_begin, num_units, split, kb_per;
     float* partial_g;
     uint16_t* out_bf16;       // [Mg][Ng] bf16 (RNE) copy of out, or its only output (EPI_FWD, EPI_DX)
+    const uint32_t* bpacked;  // forward from 2-bit codes: T as [Kg][Ng/16] words (the B operand)
 };
 
 // Up to G independent problems in one launch: their work units are concatenated
@@ -121,23 +122,29 @@ __device__ __forceinline__ int group_find(const GemmGroup<G>& g, int unit) {
 // CG CTAs (1, or a 2-CTA cluster) share one MMA of M = 128*CG rows by N = BN columns.
 // Each CTA loads its 128 rows of A and BN/CG rows of B per k-block of BK, and its
 // TMEM holds its own 128 rows of D.
-template <int CG_, int BN_, int BK_, bool A_MN_, bool B_MN_, int NB_, int EPI_, int STAGES_>
+// PK: the B operand (the forward's T) is read as 2-bit codes and expanded to bf16 in
+// shared memory by converter warps (warps 6-13: two teams of four that take alternate
+// k-blocks) instead of being copied by TMA.
+template <int CG_, int BN_, int BK_, bool A_MN_, bool B_MN_, int NB_, int EPI_, int STAGES_, bool PK_ = false>
 struct Cfg {
     static constexpr int CG = CG_, BN = BN_, BK = BK_, NB = NB_, EPI = EPI_, STAGES = STAGES_;
-    static constexpr bool A_MN = A_MN_, B_MN = B_MN_;
+    static constexpr bool A_MN = A_MN_, B_MN = B_MN_, PK = PK_;
+    static constexpr int THREADS = PK ? 448 : kThreads;   // PK: two teams of four converter warps
     static constexpr int TILE_M = kBM * CG;
     static constexpr int B_ROWS = BN / CG;
     static constexpr int A_BYTES = kBM * BK * 2;
     static constexpr int B_BYTES = B_ROWS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES;   // per CTA
-    static constexpr int TX_BYTES = CG * STAGE_BYTES;            // landing on the leader's barrier
+    static constexpr int TX_BYTES = CG * (PK ? A_BYTES : STAGE_BYTES);   // TMA bytes on the leader's barrier
+    static constexpr int P_BYTES = PK ? BK * (B_ROWS / 16) * 4 : 0;     // 2-bit codes of a stage's B (PK)
     static constexpr int TMEM_COLS = 2 * BN;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + kStagingBytes + 1024 + 256;
+    static constexpr int SMEM_BYTES = STAGES * (STAGE_BYTES + P_BYTES) + kStagingBytes + 1024 + 256;
     static_assert(CG == 1 || CG == 2, "CTA group");
     static_assert(BK == 64 || (BK == 32 && !A_MN && !B_MN), "MN-major operands use 64-deep k-blocks");
     static_assert(BN % 64 == 0 && BN <= 256 && B_ROWS % 64 == 0, "BN");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of two");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
+    static_assert(!PK || (EPI == EPI_FWD && B_MN && NB == 1 && BK == 64), "packed operand: the forward's T");
 };
 
 // One CTA per 128 x 256 tile (small problems).
@@ -148,6 +155,9 @@ using Dw1 = Cfg<1, 256, 64, true, true, 1, EPI_DW, 4>;      // A = X^T, B = dY^T
 using Fwd2 = Cfg<2, 256, 64, false, true, 1, EPI_FWD, 6>;
 using Dx2 = Cfg<2, 256, 64, false, false, 2, EPI_DX, 4>;
 using Dw2 = Cfg<2, 256, 64, true, true, 1, EPI_DW, 6>;
+// The forward with T read as 2-bit codes.
+using FwdP1 = Cfg<1, 256, 64, false, true, 1, EPI_FWD, 3, true>;
+using FwdP2 = Cfg<2, 256, 64, false, true, 1, EPI_FWD, 5, true>;
 
 // tcgen05 instruction descriptor, kind::f16: bf16 A/B, fp32 D, M x N, operand majors.
 __host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool a_mn, bool b_mn) {
@@ -274,6 +284,13 @@ __device__ __forceinline__ void store_chunk(const CUtensorMap* map, uint32_t sta
     ++nchunk;
 }
 
+// Two weights of a packed word as one bf16 pair: t holds code i at bits 0-1 and code
+// i+8 at bits 16-17 (the word shifted right by 2i); bit 0 of a code is "non-zero", bit 1
+// "negative" (00 -> 0x0000, 01 -> 0x3F80 = +1, 11 -> 0xBF80 = -1).
+__device__ __forceinline__ uint32_t tern_pair_bf16(uint32_t t) {
+    return (t & 0x00010001u) * 0x3F80u | ((t << 14) & 0x80008000u);
+}
+
 // A tile's column scales, spread over the warp: lane l holds columns 8l..8l+7 of the
 // tile starting at column col0 (zeros past the last column).  Loaded one tile ahead of
 // their use, so that no chunk waits on a cold load.
@@ -298,8 +315,17 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const CUtensor
     const bool row_ok = row < a.Mg;
     const bool hi_ok = c0 + 16 < a.Ng;   // N is a multiple of 16: the chunk's second half may lie past it
     float v[32];
+    if constexpr (C::PK) {
+        // the converters store columns i and i+8 of each 16-column group as the bf16 pair at
+        // positions 2i, 2i+1: accumulator column 2i holds column i, 2i+1 holds i+8
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+        for (int g = 0; g < 2; ++g)
+#pragma unroll
+            for (int n = 0; n < 16; ++n) v[16 * g + n] = __uint_as_float(r[16 * g + 2 * (n & 7) + (n >> 3)]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+    }
     if (C::EPI == EPI_FWD || (C::EPI == EPI_DW && a.out != nullptr)) {
         // column c0 + i of the chunk is register i % 8 of lane 4j + i / 8
 #pragma unroll
@@ -358,13 +384,19 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + C::STAGES * C::STAGE_BYTES + kStagingBytes);
+    uint64_t* bars =
+        reinterpret_cast<uint64_t*>(gbase + C::STAGES * (C::STAGE_BYTES + C::P_BYTES) + kStagingBytes);
     const uint32_t staging0 = base + static_cast<uint32_t>(C::STAGES * C::STAGE_BYTES);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 5);
+    const uint32_t pring0 = staging0 + static_cast<uint32_t>(kStagingBytes);   // PK: codes of each stage
+    // FULL, EMPTY (per stage), TFULL, TEMPTY (per accumulator), DRAIN, then (PK only) BREADY
+    // (per stage: converters done with its B operand) and PFULL (per stage: its codes landed
+    // in this CTA), then the TMEM address and abort flag
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 5 + (C::PK ? 2 * C::STAGES : 0));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const uint32_t bar0 = ptx::smem_u32(bars);
     const uint32_t FULL0 = bar0, EMPTY0 = bar0 + 8u * C::STAGES;
     const uint32_t TFULL0 = bar0 + 16u * C::STAGES, TEMPTY0 = TFULL0 + 16u, DRAIN = TFULL0 + 32u;
+    const uint32_t BREADY0 = DRAIN + 8u, PFULL0 = BREADY0 + 8u * C::STAGES;
 
     if (threadIdx.x == 32) atomicAdd(&g_gemm_count[0], 1ull);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -382,6 +414,12 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
             ptx::mbar_init(TEMPTY0 + 8u * b, 4 * CG);   // every epilogue warp of the group
         }
         ptx::mbar_init(DRAIN, 1);
+        if constexpr (C::PK) {
+            for (int s = 0; s < C::STAGES; ++s) {
+                ptx::mbar_init(BREADY0 + 8u * s, 4 * CG);   // converter warps of the group
+                ptx::mbar_init(PFULL0 + 8u * s, 1);
+            }
+        }
         *abort_flag = 0;
         ptx::fence_mbar_init();
         ptx::fence_proxy_async_smem();
@@ -446,6 +484,11 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
                     else ptx::tma_load_2d(dst, m, x, y, full_at);
                 };
                 const int k0 = kb * C::BK;
+                if constexpr (C::PK) {   // this CTA's B rows as 2-bit codes, for its converters
+                    const uint32_t pfull = PFULL0 + 8u * stage;
+                    ptx::mbar_arrive_expect_tx(pfull, C::P_BYTES);
+                    ptx::tma_load_2d(pring0 + stage * C::P_BYTES, tmB0, brow / 16, k0, pfull);
+                }
                 if constexpr (C::A_MN) {
 #pragma unroll
                     for (int j = 0; j < kBM / 64; ++j) load(sA + j * 64 * C::BK * 2, tmA, arow + j * 64, k0);
@@ -453,7 +496,7 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
                     load(sA, tmA, k0, arow);
                 }
 #pragma unroll
-                for (int b = 0; b < C::NB; ++b) {
+                for (int b = 0; b < (C::PK ? 0 : C::NB); ++b) {
                     const CUtensorMap* tmB = b == 0 ? tmB0 : tmB1;
                     const uint32_t sB = sB0 + b * C::B_BYTES;
                     if constexpr (C::B_MN) {
@@ -510,6 +553,10 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
                     ok = false;
                     break;
                 }
+                if (C::PK && !wait_bounded(BREADY0 + 8u * stage, phase, abort_flag, true, SITE + 4)) {
+                    ok = false;
+                    break;
+                }
                 ptx::tc_fence_after();
                 const uint32_t sA = base + stage * C::STAGE_BYTES;
                 const uint32_t sB0 = sA + C::A_BYTES;
@@ -540,7 +587,83 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
                 wait_bounded(TEMPTY0 + 8u * acc, static_cast<uint32_t>(last >> 1) & 1u, abort_flag, true, SITE + 6);
             }
         }
-    } else if (warp >= 2) {
+    } else if (C::PK && warp >= 6) {
+        // ------------------------------------------------------------ operand converters
+        // The producer copies each stage's B rows as 2-bit codes (TMA, P_BYTES) into this
+        // CTA's ring; thread ct takes k-row ct/2 and half ct&1 of those rows (WPT words of 16
+        // columns), expands them into the swizzled MN-major bf16 layout a TMA copy of T
+        // would have written (64-column chunks of 64 k-rows x 128 B), and the warps signal
+        // the MMA issuer.  The stage is free when its codes land: the producer copies them
+        // only after the stage's release.
+        constexpr int WPT = C::B_ROWS / 32;
+        const int team = (warp - 6) >> 2;   // team t takes the k-blocks whose running index is t mod 2
+        const int ct = static_cast<int>(threadIdx.x) - 192 - 128 * team;
+        const int kr = ct >> 1, half = ct & 1;
+        const uint32_t bready_peer = CG == 2 ? ptx::mapa_shared(BREADY0, 0) : BREADY0;
+        int stage = 0;
+        uint32_t phase = 0;
+        int seq = 0;   // running k-block index over this CTA's units
+        for (int ug = unit; ug < total_units; ug += units) {
+            const int p = group_find(grp, ug);
+            const GemmArgs& a = grp.args[p];
+            const int u = ug - grp.unit_begin[p];
+            const int kb0 = (u % a.split) * a.kb_per, kb1 = min(a.num_kb, kb0 + a.kb_per);
+            bool ok = true;
+            for (int kb = kb0; kb < kb1; ++kb, ++seq) {
+                if ((seq & 1) != team) {   // the other team's k-block: only follow the stage ring
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                    continue;
+                }
+                const bool landed = wait_bounded(PFULL0 + 8u * stage, phase, abort_flag, true, SITE + 9);
+                if (!__all_sync(0xffffffffu, landed)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t src = pring0 + stage * C::P_BYTES + static_cast<uint32_t>(kr) * (C::B_ROWS / 16) * 4u +
+                                     static_cast<uint32_t>(half) * WPT * 4u;
+                const uint32_t sB = base + stage * C::STAGE_BYTES + C::A_BYTES;
+#pragma unroll
+                for (int h = 0; h < WPT / 4; ++h) {
+                    uint32_t w[4];
+                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                                 : "r"(src + h * 16u)
+                                 : "memory");
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int col = (half * WPT + 4 * h + j) * 16;   // first column of the word in the CTA's rows
+                        const uint32_t row = sB + (col >> 6) * (64u * C::BK * 2u) + static_cast<uint32_t>(kr) * 128u;
+                        const int u0 = (col & 63) >> 3;                 // its first 16-byte unit in the row
+                        uint32_t q[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) q[i] = tern_pair_bf16(w[j] >> (2 * i));
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                         row + (static_cast<uint32_t>(u0 ^ (kr & 7)) << 4)),
+                                     "r"(q[0]), "r"(q[1]), "r"(q[2]), "r"(q[3])
+                                     : "memory");
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                         row + (static_cast<uint32_t>((u0 + 1) ^ (kr & 7)) << 4)),
+                                     "r"(q[4]), "r"(q[5]), "r"(q[6]), "r"(q[7])
+                                     : "memory");
+                    }
+                }
+                ptx::fence_proxy_async_smem();   // generic-proxy writes, read next by the tensor core
+                __syncwarp();
+                if (lane == 0) {
+                    if (CG == 2 && rank != 0) ptx::mbar_arrive_cluster(bready_peer + 8u * stage);
+                    else ptx::mbar_arrive(BREADY0 + 8u * stage);
+                }
+                if (++stage == C::STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+        }
+    } else if (warp >= 2 && warp < 6) {
         // ------------------------------------------------------------ epilogue
         const int quad = warp & 3;   // a warp may touch TMEM lanes 32*(warp%4) .. +31
         const uint32_t tempty_leader = CG == 2 ? ptx::mapa_shared(TEMPTY0, 0) : TEMPTY0;
@@ -638,8 +761,11 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
         // after an abort, copies still in flight must land before the CTA's shared memory is released
         if constexpr (CG == 1) {
             for (int s = 0; s < C::STAGES; ++s)
-                if (issued & (1u << s))
+                if (issued & (1u << s)) {
                     wait_bounded(FULL0 + 8u * s, (issued_parity >> s) & 1u, abort_flag, false, SITE + 8);
+                    if constexpr (C::PK)
+                        wait_bounded(PFULL0 + 8u * s, (issued_parity >> s) & 1u, abort_flag, false, SITE + 8);
+                }
         } else {
             // a pair's copies complete on the leader's barriers; give them time to land
             const uint64_t t0 = ptx::globaltimer();
@@ -656,6 +782,12 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
 template <int CG, int G>
 __global__ void __launch_bounds__(kThreads, 1) tern_fwd_gemm(const __grid_constant__ GemmGroup<G> grp) {
     gemm_body<std::conditional_t<CG == 2, Fwd2, Fwd1>, G>(grp);
+}
+
+// The forward with T read as 2-bit codes (expanded in shared memory by converter warps).
+template <int CG, int G>
+__global__ void __launch_bounds__(448, 1) tern_fwdp_gemm(const __grid_constant__ GemmGroup<G> grp) {
+    gemm_body<std::conditional_t<CG == 2, FwdP2, FwdP1>, G>(grp);
 }
 
 template <int CG, int G>
@@ -883,14 +1015,14 @@ int encode_2d(CUtensorMap* m, const MapKey& k) {
     }
     EncodeTiledFn enc = encode_fn();
     if (!enc) return TERN_ERR_CUDA;
-    const int esize = k.dtype == CU_TENSOR_MAP_DATA_TYPE_FLOAT32 ? 4 : 2;
+    const int esize = k.dtype == CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 ? 2 : 4;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(k.inner), static_cast<cuuint64_t>(k.outer)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(k.inner) * esize};
     cuuint32_t box[2] = {static_cast<cuuint32_t>(k.box_inner), static_cast<cuuint32_t>(k.box_outer)};
     cuuint32_t estr[2] = {1, 1};
     // operands are read with 256-byte L2 promotion; outputs are only written
     const CUtensorMapL2promotion l2 =
-        esize == 2 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_NONE;
+        k.dtype == CU_TENSOR_MAP_DATA_TYPE_FLOAT32 ? CU_TENSOR_MAP_L2_PROMOTION_NONE : CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
     CUresult r = enc(m, static_cast<CUtensorMapDataType>(k.dtype), 2, const_cast<void*>(k.ptr), dims, strides, box,
                      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, static_cast<CUtensorMapSwizzle>(k.sw), l2,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -963,7 +1095,7 @@ int persistent_units(K kernel, int num_sms, int* units) {
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.gridDim = dim3(2 * (num_sms / 2));
-        cfg.blockDim = dim3(kThreads);
+        cfg.blockDim = dim3(C::THREADS);
         cfg.dynamicSmemBytes = C::SMEM_BYTES;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
@@ -988,7 +1120,7 @@ int launch(K kernel, const GemmGroup<G>& grp, int num_sms, cudaStream_t s) {
     if (total <= 0) return TERN_OK;
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[1];
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(C::THREADS);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = s;
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1015,7 +1147,14 @@ template <class C, int G>
 int group_set(GemmGroup<G>& g, int p, const void* A, int64_t a_inner, int64_t a_outer, const void* B0,
               const void* B1, int64_t b_inner, int64_t b_outer, const GemmArgs& a) {
     if (int st = map_operand<C>(&g.mA[p], A, a_inner, a_outer, C::A_MN, kBM)) return st;
-    if (int st = map_operand<C>(&g.mB0[p], B0, b_inner, b_outer, C::B_MN, C::B_ROWS)) return st;
+    if constexpr (C::PK) {   // B as 2-bit codes [Kg][Ng/16] words, copied per stage for the converters
+        if (int st = encode_2d(&g.mB0[p], MapKey{a.bpacked, a.Ng / 16, a.Kg, C::B_ROWS / 16, C::BK,
+                                                 static_cast<int>(CU_TENSOR_MAP_SWIZZLE_NONE),
+                                                 static_cast<int>(CU_TENSOR_MAP_DATA_TYPE_UINT32)}))
+            return st;
+    } else {
+        if (int st = map_operand<C>(&g.mB0[p], B0, b_inner, b_outer, C::B_MN, C::B_ROWS)) return st;
+    }
     if (B1) {
         if (int st = map_operand<C>(&g.mB1[p], B1, b_inner, b_outer, C::B_MN, C::B_ROWS)) return st;
     } else {
@@ -1037,13 +1176,14 @@ void group_close(GemmGroup<G>& g, int count) {
 }
 
 template <class C, class K>
-int run_fwd(K kernel, const uint16_t* X, const uint16_t* T, const float* scale, float* Y, int64_t M, int64_t K_,
-            int64_t N, int num_sms, cudaStream_t s) {
+int run_fwd(K kernel, const uint16_t* X, const uint16_t* T, const uint32_t* packed, const float* scale, float* Y,
+            int64_t M, int64_t K_, int64_t N, int num_sms, cudaStream_t s) {
     GemmGroup<1> g;
     GemmArgs a = make_args<C>(M, N, K_);
     a.out = Y;
     a.scale = scale;
-    if (int st = group_set<C>(g, 0, X, K_, M, T, nullptr, N, K_, a)) return st;
+    a.bpacked = C::PK ? packed : nullptr;
+    if (int st = group_set<C>(g, 0, X, K_, M, C::PK ? nullptr : T, nullptr, N, K_, a)) return st;
     group_close(g, 1);
     return launch<C>(kernel, g, num_sms, s);
 }
@@ -1162,16 +1302,22 @@ using namespace tern;
 
 extern "C" int tern_linear_fwd(const uint16_t* X, const tern_tiles* W, const float* scale, float* Y, int64_t M,
                                int64_t K, int64_t N, void* stream) {
-    if (!X || !W || !W->t_bf16 || !scale || !Y) return TERN_ERR_ARG;
+    if (!X || !W || (!W->t_bf16 && !W->packed) || !scale || !Y) return TERN_ERR_ARG;
     if (!dims_ok(M, K, N)) return TERN_ERR_ARG;
     if (K % 16 || N % 16) return TERN_ERR_ALIGN;
-    if (!aligned16(X) || !aligned16(W->t_bf16) || !aligned16(scale) || !aligned16(Y)) return TERN_ERR_ALIGN;
+    const void* b = W->t_bf16 ? static_cast<const void*>(W->t_bf16) : static_cast<const void*>(W->packed);
+    if (!aligned16(X) || !aligned16(b) || !aligned16(scale) || !aligned16(Y)) return TERN_ERR_ALIGN;
+    if (!W->t_bf16 && N % 64) return TERN_ERR_ALIGN;   // rows of 2-bit codes copied by TMA: 16-byte multiples
     int num_sms = 0;
     if (int st = check_device(&num_sms)) return st;
     if (int st = gemm_setup(num_sms)) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (use_pair(M)) return run_fwd<Fwd2>(tern_fwd_gemm<2, 1>, X, W->t_bf16, scale, Y, M, K, N, num_sms, s);
-    return run_fwd<Fwd1>(tern_fwd_gemm<1, 1>, X, W->t_bf16, scale, Y, M, K, N, num_sms, s);
+    if (W->t_bf16) {
+        if (use_pair(M)) return run_fwd<Fwd2>(tern_fwd_gemm<2, 1>, X, W->t_bf16, nullptr, scale, Y, M, K, N, num_sms, s);
+        return run_fwd<Fwd1>(tern_fwd_gemm<1, 1>, X, W->t_bf16, nullptr, scale, Y, M, K, N, num_sms, s);
+    }
+    if (use_pair(M)) return run_fwd<FwdP2>(tern_fwdp_gemm<2, 1>, X, nullptr, W->packed, scale, Y, M, K, N, num_sms, s);
+    return run_fwd<FwdP1>(tern_fwdp_gemm<1, 1>, X, nullptr, W->packed, scale, Y, M, K, N, num_sms, s);
 }
 
 // sgrad partials: one row per 32-row group of K, rounded up to 256 bytes.
@@ -1272,21 +1418,33 @@ int layer_align(const tern_layer& L) {
     return TERN_OK;
 }
 
-// Calls fn(idx, n) for the layers selected by `pick`, in order, kGroup at a time,
-// separately for layers whose rows (rows_of) need a CTA pair and those that do not.
-template <class Pick, class Rows, class Fn>
-int for_groups(const tern_layer* L, int count, Pick pick, Rows rows_of, Fn fn) {
+// Calls fn(pair, idx, n) (or fn(pair, variant, idx, n)) for the layers selected by
+// `pick`, in order, kGroup at a time, separately for layers whose rows (rows_of) need
+// a CTA pair and those that do not, and for the two kernel variants `variant` tells
+// apart (the forward's bf16 or 2-bit T).
+template <class Pick, class Rows, class Var, class Fn>
+int for_groups_v(const tern_layer* L, int count, Pick pick, Rows rows_of, Var variant, Fn fn) {
     for (int pair = 1; pair >= 0; --pair) {
-        int idx[kGroup], n = 0;
-        for (int i = 0; i <= count; ++i) {
-            if (i < count && pick(L[i]) && use_pair(rows_of(L[i])) == (pair == 1)) idx[n++] = i;
-            if (n == kGroup || (i == count && n > 0)) {
-                if (int st = fn(pair == 1, idx, n)) return st;
-                n = 0;
+        for (int v = 0; v < 2; ++v) {
+            int idx[kGroup], n = 0;
+            for (int i = 0; i <= count; ++i) {
+                if (i < count && pick(L[i]) && use_pair(rows_of(L[i])) == (pair == 1) && variant(L[i]) == (v == 1))
+                    idx[n++] = i;
+                if (n == kGroup || (i == count && n > 0)) {
+                    if (int st = fn(pair == 1, v == 1, idx, n)) return st;
+                    n = 0;
+                }
             }
         }
     }
     return TERN_OK;
+}
+
+template <class Pick, class Rows, class Fn>
+int for_groups(const tern_layer* L, int count, Pick pick, Rows rows_of, Fn fn) {
+    return for_groups_v(
+        L, count, pick, rows_of, [](const tern_layer&) { return false; },
+        [&](bool pair, bool, const int* idx, int n) { return fn(pair, idx, n); });
 }
 
 // The layers of a launch in descending order of k-blocks per tile (stable): the
@@ -1309,7 +1467,9 @@ int fwd_group(K kernel, const tern_layer* L, const int* idx_in, int n, int num_s
         a.out = l.Y;
         a.out_bf16 = l.Y_bf16;
         a.scale = l.scale;
-        if (int st = group_set<C>(g, i, l.X, l.K, l.M, l.W->t_bf16, nullptr, l.N, l.K, a)) return st;
+        a.bpacked = C::PK ? l.W->packed : nullptr;
+        if (int st = group_set<C>(g, i, l.X, l.K, l.M, C::PK ? nullptr : l.W->t_bf16, nullptr, l.N, l.K, a))
+            return st;
     }
     group_close(g, n);
     return launch<C>(kernel, g, num_sms, s);
@@ -1441,17 +1601,23 @@ extern "C" int tern_linear_fwd_grouped(const tern_layer* layers, int count, void
     if (!layers || count < 1) return TERN_ERR_ARG;
     for (int i = 0; i < count; ++i) {
         const tern_layer& l = layers[i];
-        if (!l.X || !l.W || !l.W->t_bf16 || !l.scale || (!l.Y && !l.Y_bf16) || !dims_ok(l.M, l.K, l.N))
+        if (!l.X || !l.W || (!l.W->t_bf16 && !l.W->packed) || !l.scale || (!l.Y && !l.Y_bf16) ||
+            !dims_ok(l.M, l.K, l.N))
             return TERN_ERR_ARG;
         if (int st = layer_align(l)) return st;
+        if (!l.W->t_bf16 && l.N % 64) return TERN_ERR_ALIGN;
     }
     int num_sms = 0;
     if (int st = check_device(&num_sms)) return st;
     if (int st = gemm_setup(num_sms)) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return for_groups(
+    return for_groups_v(
         layers, count, [](const tern_layer&) { return true; }, [](const tern_layer& l) { return l.M; },
-        [&](bool pair, const int* idx, int n) {
+        [](const tern_layer& l) { return l.W->t_bf16 == nullptr; },
+        [&](bool pair, bool packed, const int* idx, int n) {
+            if (packed)
+                return pair ? fwd_group<FwdP2>(tern_fwdp_gemm<2, kGroup>, layers, idx, n, num_sms, s)
+                            : fwd_group<FwdP1>(tern_fwdp_gemm<1, kGroup>, layers, idx, n, num_sms, s);
             return pair ? fwd_group<Fwd2>(tern_fwd_gemm<2, kGroup>, layers, idx, n, num_sms, s)
                         : fwd_group<Fwd1>(tern_fwd_gemm<1, kGroup>, layers, idx, n, num_sms, s);
         });
@@ -1585,6 +1751,10 @@ int gemm_setup(int num_sms) {
         gemm(persistent_units<Dx2>(tern_dx_gemm<2, kGroup>, num_sms, &u));
         gemm(persistent_units<Dw1>(tern_dw_gemm<1, kGroup>, num_sms, &u));
         gemm(persistent_units<Dw2>(tern_dw_gemm<2, kGroup>, num_sms, &u));
+        gemm(persistent_units<FwdP1>(tern_fwdp_gemm<1, 1>, num_sms, &u));
+        gemm(persistent_units<FwdP2>(tern_fwdp_gemm<2, 1>, num_sms, &u));
+        gemm(persistent_units<FwdP1>(tern_fwdp_gemm<1, kGroup>, num_sms, &u));
+        gemm(persistent_units<FwdP2>(tern_fwdp_gemm<2, kGroup>, num_sms, &u));
         cudaFuncAttributes fa;
         auto load = [&](cudaError_t e) {
             if (st == TERN_OK && e != cudaSuccess) st = TERN_ERR_CUDA;

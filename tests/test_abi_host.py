@@ -74,8 +74,10 @@ def test_forward_argument_checks(lib):
     assert f(*ok, 64, 24 + 16, 128, None) == lib.TERN_ERR_ALIGN    # K = 40
     assert f(*ok, 64, 128, 136, None) == lib.TERN_ERR_ALIGN        # N = 136
     assert f(P(0x20002), ctypes.byref(t), P(0x30000), P(0x40000), 64, 128, 128, None) == lib.TERN_ERR_ALIGN
-    nul = lib._Tiles(P(0x10000), None, None, None)                 # no bf16 T operand
+    nul = lib._Tiles(None, None, P(0x12000), P(0x13000))          # neither the bf16 T nor the 2-bit codes
     assert f(P(0x20000), ctypes.byref(nul), P(0x30000), P(0x40000), 64, 128, 128, None) == lib.TERN_ERR_ARG
+    mis = lib._Tiles(P(0x10004), None, None, None)                 # the 2-bit codes alone, misaligned
+    assert f(P(0x20000), ctypes.byref(mis), P(0x30000), P(0x40000), 64, 128, 128, None) == lib.TERN_ERR_ALIGN
 
 
 def test_backward_argument_checks(lib):

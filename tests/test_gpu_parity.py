@@ -250,3 +250,50 @@ def test_layer_with_negative_and_zero_scales(cuda_lib):
     inp.scale = sc
     layer = Layer(inp).run()
     full_oracle_check(layer)
+
+
+# ----------------------------------------------------------------- forward from the 2-bit codes
+
+@pytest.mark.parametrize("M,K,N", [(64, 128, 128), (130, 144, 320), (300, 528, 64), (257, 64, 768), (1000, 512, 2048),
+                                   (8, 80, 192), (513, 1040, 448)])
+def test_forward_from_packed_codes(cuda_lib, M, K, N):
+    """tern_linear_fwd with t_bf16 = NULL reads T as the 2-bit codes, expanded to bf16 in
+    the GEMM: the same Y bits as the bf16-plane forward, and within the oracle tolerance.
+    (This operand needs N % 64 == 0: its rows are copied by TMA in 16-byte multiples.)"""
+    bl = cuda_lib
+    inp = syn.linear_inputs(M, K, N, seed=M + 3 * K + N)
+    layer = Layer(inp).run()
+    packed_only = bl.Tiles(K, N, packed=layer.tiles.packed)
+    Y = torch.full((M, N), float("nan"), device="cuda")
+    bl.tern_linear_fwd(layer.X, packed_only, layer.scale, Y)
+    assert bl.tern_device_status() == bl.TERN_OK
+    assert torch.equal(Y, layer.Y)
+    Yr, Ya = oracle.fwd(inp.X, inp.q, inp.scale)
+    check_close("Y (2-bit T)", Y.cpu().numpy(), Yr, Ya)
+
+
+def test_grouped_forward_mixes_packed_and_bf16_layers(cuda_lib):
+    bl = cuda_lib
+    shapes = [(300, 256, 384), (64, 144, 272), (1000, 512, 512), (257, 128, 1008), (8, 64, 64)]
+    layers = [Layer(syn.linear_inputs(M, K, N, seed=900 + i)).run() for i, (M, K, N) in enumerate(shapes)]
+    outs = [torch.full_like(L.Y, float("nan")) for L in layers]
+    Yb = [torch.empty(L.Y.shape, dtype=torch.bfloat16, device="cuda") for L in layers]
+    dicts = []
+    for i, (L, Y, B) in enumerate(zip(layers, outs, Yb)):
+        tiles = bl.Tiles(L.K, L.N, packed=L.tiles.packed) if i % 2 == 0 else L.tiles
+        dicts.append(dict(X=L.X, tiles=tiles, scale=L.scale, Y=Y, Y_bf16=B))
+    bl.tern_linear_fwd_grouped(dicts)
+    assert bl.tern_device_status() == bl.TERN_OK
+    for L, Y, B in zip(layers, outs, Yb):
+        assert torch.equal(Y, L.Y)
+        assert torch.equal(B, L.Y.to(torch.bfloat16))
+
+
+def test_forward_from_packed_codes_needs_n_multiple_of_64(cuda_lib):
+    bl = cuda_lib
+    inp = syn.linear_inputs(64, 64, 48, seed=5)
+    layer = Layer(inp)
+    bl.tern_materialize(layer.q, layer.scale, layer.tiles, 2, 7)
+    with pytest.raises(bl.TernError) as e:
+        bl.tern_linear_fwd(layer.X, bl.Tiles(64, 48, packed=layer.tiles.packed), layer.scale, layer.Y)
+    assert e.value.status == bl.TERN_ERR_ALIGN
