@@ -45,6 +45,33 @@ def test_noalloc_matches_workspace_entry_point(cuda_lib, first, second):
         _within("sgrad", sgrad, ref.sgrad, sga)
 
 
+def test_noalloc_calls_back_to_back_on_one_stream(cuda_lib):
+    """Two no-workspace calls of different shapes enqueued on one stream with no
+    synchronisation between them (the second reuses the built-in scratch while the
+    first call's kernels may still be finishing), then both compared with the
+    workspace entry point."""
+    bl = cuda_lib
+    shapes = [(300, 528, 400), (517, 400, 528)]
+    inps = [syn.linear_inputs(M, K, N, seed=M * 5 + K + N) for M, K, N in shapes]
+    refs = [Layer(inp).run() for inp in inps]     # tern_linear_bwd with a caller workspace
+    nan = float("nan")
+    outs = []
+    for (M, K, N), ref in zip(shapes, refs):
+        o = (torch.full((M, K), nan, device="cuda"), torch.full((K, N), nan, device="cuda"),
+             torch.full((N,), nan, device="cuda"))
+        outs.append(o)
+    torch.cuda.synchronize()
+    for ref, (dX, gq, sgrad) in zip(refs, outs):
+        bl.tern_linear_bwd_noalloc(ref.X, ref.dY, ref.tiles, ref.scale, dX, gq, sgrad)
+    assert bl.tern_device_status() == bl.TERN_OK
+    for inp, ref, (dX, gq, sgrad) in zip(inps, refs, outs):
+        _, dXa = oracle.dx(inp.dY, inp.q, inp.scale)
+        _, gqa, _, sga = oracle.dw(inp.X, inp.dY, inp.q, inp.scale)
+        _within("dX", dX, ref.dX, dXa)
+        _within("gq", gq, ref.gq, gqa)
+        _within("sgrad", sgrad, ref.sgrad, sga)
+
+
 def test_noalloc_rejects_problems_beyond_its_scratch(cuda_lib):
     bl = cuda_lib
     K, N = 4096, 16400          # ceil(K/128) * 4 * N = 2,099,200 partials > 2^21
