@@ -67,11 +67,11 @@ __device__ int g_gemm_site[4];
 namespace {
 
 constexpr int kBM = 128;           // rows of A (and of D) per CTA
-constexpr int kThreads = 192;
-// Output staging of the epilogue: per epilogue warp two 32 x 32 fp32 buffers (4 KB each,
-// 128-byte swizzle), from which one lane issues the TMA store of each chunk.
+// Output staging of the epilogue: eight 32 x 32 fp32 buffers (4 KB each, 128-byte
+// swizzle) per CTA, one per epilogue warp (two per warp with four epilogue warps), from
+// which one lane issues the TMA store of each chunk.
 constexpr int kStageBuf = 32 * 32 * 4;
-constexpr int kStagingBytes = 4 * 2 * kStageBuf;
+constexpr int kStagingBytes = 8 * kStageBuf;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait; a healthy wait takes microseconds
 
 enum { EPI_FWD = 0, EPI_DX = 1, EPI_DW = 2 };
@@ -129,7 +129,11 @@ template <int CG_, int BN_, int BK_, bool A_MN_, bool B_MN_, int NB_, int EPI_, 
 struct Cfg {
     static constexpr int CG = CG_, BN = BN_, BK = BK_, NB = NB_, EPI = EPI_, STAGES = STAGES_;
     static constexpr bool A_MN = A_MN_, B_MN = B_MN_, PK = PK_;
-    static constexpr int THREADS = PK ? 448 : kThreads;   // PK: two teams of four converter warps
+    // warps: producer, MMA, EPI_WARPS epilogue warps (two per TMEM lane quarter, each taking
+    // half the columns; four when PK), and for PK two teams of four converter warps
+    static constexpr int EPI_WARPS = PK ? 4 : 8;
+    static constexpr int NBUF = 8 / EPI_WARPS;   // staging buffers per epilogue warp
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS + (PK ? 256 : 0);
     static constexpr int TILE_M = kBM * CG;
     static constexpr int B_ROWS = BN / CG;
     static constexpr int A_BYTES = kBM * BK * 2;
@@ -262,12 +266,13 @@ __device__ __forceinline__ float warp_column_sums(float (&v)[32], int lane) {
 // Stage one 32 x 32 fp32 chunk of a warp (lane = row, v = its 32 columns) in shared
 // memory with the 128-byte swizzle of the output tensor map, then let one lane issue
 // the chunk's TMA store (or fp32 add) at column x, row y; rows and columns past the
-// tensor's edge are clipped by the copy.  Two buffers per warp: before one is
-// rewritten, the store issued from it two chunks earlier must have read it.
+// tensor's edge are clipped by the copy.  NBUF buffers per warp: before one is
+// rewritten, the store issued from it NBUF chunks earlier must have read it.
+template <int NBUF>
 __device__ __forceinline__ void store_chunk(const CUtensorMap* map, uint32_t stage, int& nchunk, const float (&v)[32],
                                             int x, int y, bool add, int lane) {
-    const uint32_t buf = stage + static_cast<uint32_t>(nchunk & 1) * kStageBuf;
-    if (nchunk >= 2 && lane == 0) ptx::bulk_wait_read<1>();
+    const uint32_t buf = stage + static_cast<uint32_t>(nchunk % NBUF) * kStageBuf;
+    if (nchunk >= NBUF && lane == 0) ptx::bulk_wait_read<NBUF - 1>();
     __syncwarp();
     const uint32_t row = buf + static_cast<uint32_t>(lane) * 128u;
 #pragma unroll
@@ -334,7 +339,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const CUtensor
     // fp32 output through shared memory and TMA (gq += ... with accumulate: a TMA add);
     // the condition is the same for the whole warp
     if (a.out != nullptr && wrow < a.Mg)
-        store_chunk(omap, stage, nchunk, v, c0, wrow, C::EPI == EPI_DW && a.accumulate != 0, lane);
+        store_chunk<C::NBUF>(omap, stage, nchunk, v, c0, wrow, C::EPI == EPI_DW && a.accumulate != 0, lane);
     if constexpr (C::EPI != EPI_DW) {
         if (a.out_bf16 != nullptr && row_ok) {   // 16 columns -> 32 bytes, round to nearest even
             const int64_t at = static_cast<int64_t>(row) * a.Ng + c0;
@@ -411,7 +416,7 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(TFULL0 + 8u * b, 1);
-            ptx::mbar_init(TEMPTY0 + 8u * b, 4 * CG);   // every epilogue warp of the group
+            ptx::mbar_init(TEMPTY0 + 8u * b, C::EPI_WARPS * CG);   // every epilogue warp of the group
         }
         ptx::mbar_init(DRAIN, 1);
         if constexpr (C::PK) {
@@ -587,7 +592,7 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
                 wait_bounded(TEMPTY0 + 8u * acc, static_cast<uint32_t>(last >> 1) & 1u, abort_flag, true, SITE + 6);
             }
         }
-    } else if (C::PK && warp >= 6) {
+    } else if (C::PK && warp >= 2 + C::EPI_WARPS) {
         // ------------------------------------------------------------ operand converters
         // The producer copies each stage's B rows as 2-bit codes (TMA, P_BYTES) into this
         // CTA's ring; thread ct takes k-row ct/2 and half ct&1 of those rows (WPT words of 16
@@ -596,8 +601,8 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
         // the MMA issuer.  The stage is free when its codes land: the producer copies them
         // only after the stage's release.
         constexpr int WPT = C::B_ROWS / 32;
-        const int team = (warp - 6) >> 2;   // team t takes the k-blocks whose running index is t mod 2
-        const int ct = static_cast<int>(threadIdx.x) - 192 - 128 * team;
+        const int team = (warp - 2 - C::EPI_WARPS) >> 2;   // team t takes the k-blocks of running index t mod 2
+        const int ct = static_cast<int>(threadIdx.x) - 32 * (2 + C::EPI_WARPS) - 128 * team;
         const int kr = ct >> 1, half = ct & 1;
         const uint32_t bready_peer = CG == 2 ? ptx::mapa_shared(BREADY0, 0) : BREADY0;
         int stage = 0;
@@ -663,11 +668,14 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
             }
             if (!ok) break;
         }
-    } else if (warp >= 2 && warp < 6) {
+    } else if (warp >= 2 && warp < 2 + C::EPI_WARPS) {
         // ------------------------------------------------------------ epilogue
         const int quad = warp & 3;   // a warp may touch TMEM lanes 32*(warp%4) .. +31
         const uint32_t tempty_leader = CG == 2 ? ptx::mapa_shared(TEMPTY0, 0) : TEMPTY0;
-        const uint32_t stage = staging0 + static_cast<uint32_t>(warp - 2) * 2u * kStageBuf;
+        const uint32_t stage = staging0 + static_cast<uint32_t>(warp - 2) * C::NBUF * kStageBuf;
+        // with eight epilogue warps, warps 2-5 take the tile's first BN/2 columns and 6-9 the rest
+        constexpr int JPW = C::BN / 32 / (C::EPI_WARPS / 4);   // 32-column chunks per warp and tile
+        const int j0 = ((warp - 2) / 4) * JPW;
         int nchunk = 0;   // chunks this warp has staged (its buffer parity)
         int local = 0;
         // the column scales of a unit's tile (none for dX and for split units' raw tiles)
@@ -711,20 +719,20 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
                 // partial_g, which omap describes) for the reduce kernel
                 const int prow = u * C::TILE_M + static_cast<int>(rank) * kBM + quad * 32;
 #pragma unroll 1
-                for (int j = 0; j < C::BN / 32; ++j) {
+                for (int j = j0; j < j0 + JPW; ++j) {
                     uint32_t r[32];
                     ptx::tmem_ld_32x32b_x32(trow + j * 32, r);
                     ptx::tmem_wait_ld();
                     float v[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-                    store_chunk(omap, stage, nchunk, v, j * 32, prow, false, lane);
+                    store_chunk<C::NBUF>(omap, stage, nchunk, v, j * 32, prow, false, lane);
                 }
             } else if (row0 < a.Mg) {   // a pair's second half may lie wholly past the last row
                 const int tile128 = mt * CG + static_cast<int>(rank);
                 const int wrow = row0 + quad * 32;
 #pragma unroll 1
-                for (int j = 0; j < C::BN / 32; ++j) {
+                for (int j = j0; j < j0 + JPW; ++j) {
                     const int c0 = nt * C::BN + j * 32;
                     if (c0 >= a.Ng) break;
                     uint32_t r[32];
@@ -780,7 +788,7 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
 // One launch runs the work units of a group of G problems (G = 1: a single
 // layer); the tensor maps live in the kernel's parameter space.
 template <int CG, int G>
-__global__ void __launch_bounds__(kThreads, 1) tern_fwd_gemm(const __grid_constant__ GemmGroup<G> grp) {
+__global__ void __launch_bounds__(320, 1) tern_fwd_gemm(const __grid_constant__ GemmGroup<G> grp) {
     gemm_body<std::conditional_t<CG == 2, Fwd2, Fwd1>, G>(grp);
 }
 
@@ -791,12 +799,12 @@ __global__ void __launch_bounds__(448, 1) tern_fwdp_gemm(const __grid_constant__
 }
 
 template <int CG, int G>
-__global__ void __launch_bounds__(kThreads, 1) tern_dx_gemm(const __grid_constant__ GemmGroup<G> grp) {
+__global__ void __launch_bounds__(320, 1) tern_dx_gemm(const __grid_constant__ GemmGroup<G> grp) {
     gemm_body<std::conditional_t<CG == 2, Dx2, Dx1>, G>(grp);
 }
 
 template <int CG, int G>
-__global__ void __launch_bounds__(kThreads, 1) tern_dw_gemm(const __grid_constant__ GemmGroup<G> grp) {
+__global__ void __launch_bounds__(320, 1) tern_dw_gemm(const __grid_constant__ GemmGroup<G> grp) {
     gemm_body<std::conditional_t<CG == 2, Dw2, Dw1>, G>(grp);
 }
 
