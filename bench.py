@@ -392,7 +392,8 @@ def rwkv_block(bl, dev, stream, steps):
     adam_scalars = torch.tensor([ADAM_HP["lr"], 1 - ADAM_HP["b1"], 1 - ADAM_HP["b2"], 1.0], device=dev)
 
     # the grouped schedules call the library through prepared calls (arguments marshalled
-    # once), as a training loop repeating the step on the same buffers does
+    # once), as a training loop repeating the step on the same buffers does, and materialise
+    # the six weights in one grouped call
     adam_all = bl.MultiAdamW([L["scale"] for L in layers], [L["sgrad"] for L in layers], [L["m"] for L in layers],
                              [L["v"] for L in layers], adam_scalars, ADAM_HP["b1"], ADAM_HP["b2"], ADAM_HP["eps"],
                              ADAM_HP["wd"])
@@ -408,7 +409,8 @@ def rwkv_block(bl, dev, stream, steps):
         # packed_t: the forward reads T as the 2-bit codes and materialise skips the bf16 T plane
         tl = [bl.Tiles(L["K"], L["N"], packed=L["tiles"].packed, whi_bf16=L["tiles"].whi_bf16,
                        wlo_bf16=L["tiles"].wlo_bf16) if packed_t else L["tiles"] for L in layers]
-        mats_ = [bl.Materialize(L["q"], L["scale"], t_, 2, 7) for L, t_ in zip(layers, tl)]
+        mat_all = bl.MaterializeGrouped([dict(q=L["q"], scale=L["scale"], tiles=t_) for L, t_ in zip(layers, tl)],
+                                        2, 7)
         fwds = [bl.GroupedForward([dict(X=layers[i]["X"], tiles=tl[i], scale=layers[i]["scale"],
                                         Y=layers[i]["Y"]) for i in gr]) for gr in fwd_groups]
         bwds = []
@@ -420,8 +422,7 @@ def rwkv_block(bl, dev, stream, steps):
                                                  sgrad=layers[i]["sgrad"]) for i in gr], ws_))
 
         def step():
-            for m_ in mats_:
-                m_()
+            mat_all()
             for f_ in fwds:
                 f_()
             for b_ in bwds:
@@ -435,7 +436,7 @@ def rwkv_block(bl, dev, stream, steps):
         "dependency": grouped([[0, 1, 2], [3], [4], [5]], [[5], [4], [3], [0, 1, 2]]),
         "per_layer": per_layer,
     }
-    launches = {"independent": 6 + 1 + 4 + 1, "independent_2bit_T": 6 + 1 + 4 + 1, "dependency": 6 + 4 + 4 * 3 + 1,
+    launches = {"independent": 1 + 1 + 4 + 1, "independent_2bit_T": 1 + 1 + 4 + 1, "dependency": 1 + 4 + 4 * 3 + 1,
                 "per_layer": 6 * 6}
     flops = 6.0 * M * sum(K * N for K, N in shapes)
     reps = max(20, min(steps, 200))
@@ -500,7 +501,7 @@ def rwkv_block(bl, dev, stream, steps):
 
 def wide_chain(bl, dev, stream, steps):
     """Two chained projections, (M, K1, N1) = (16384, 2048, 6144) then (16384, 6144, 2048),
-    40% of q forced to zero: materialise both, fwd 1 writes its output in bf16 only
+    40% of q forced to zero: materialise both (one grouped call), fwd 1 writes its output in bf16 only
     (layer 2's input), fwd 2, bwd 2 writes its input gradient in bf16 only (layer 1's
     dY), bwd 1, then AdamW of both scales in one launch."""
     import torch
@@ -530,14 +531,14 @@ def wide_chain(bl, dev, stream, steps):
     ws2 = torch.empty(bl.tern_linear_bwd_grouped_workspace([(M, N1, K1)]) // 4, device=dev)
     adam_scalars = torch.tensor([ADAM_HP["lr"], 1 - ADAM_HP["b1"], 1 - ADAM_HP["b2"], 1.0], device=dev)
     names = ["materialize", "fwd1", "fwd2", "bwd2", "bwd1", "adamw"]
+    mat = bl.MaterializeGrouped([dict(q=q1, scale=s1, tiles=t1), dict(q=q2, scale=s2, tiles=t2)], 2, 7)
 
     def step(ev=None):
         def mark(i):
             if ev is not None:
                 ev[i].record(stream)
         mark(0)
-        bl.tern_materialize(q1, s1, t1, 2, 7)
-        bl.tern_materialize(q2, s2, t2, 2, 7)
+        mat()
         mark(1)
         bl.tern_linear_fwd_grouped([dict(X=X, tiles=t1, scale=s1, Y_bf16=X2)])
         mark(2)

@@ -9,7 +9,7 @@ current stream.  The functions carry the C names:
     tern_linear_bwd(X, dY, tiles, scale, dX, gq, sgrad, workspace)
     adamw_step(w, g, m, v, t, lr, b1, b2, eps, wd, gmul=1.0, decoupled=True)
 
-Materialize, GroupedForward, GroupedBackward and MultiAdamW are the same calls with
+Materialize, MaterializeGrouped, GroupedForward, GroupedBackward and MultiAdamW are the same calls with
 their arguments checked and marshalled once, for loops that repeat them on the
 same buffers.
 
@@ -42,7 +42,7 @@ TERN_ADAM_MAX_TENSORS = 64
 TERN_BWD_ACCUMULATE = 1
 
 # the C ABI's exported symbols (tests check the library exports every one)
-ABI_SYMBOLS = ("tern_tiles_bytes", "tern_materialize", "tern_linear_fwd", "tern_linear_bwd_workspace_min",
+ABI_SYMBOLS = ("tern_tiles_bytes", "tern_materialize", "tern_materialize_grouped", "tern_linear_fwd", "tern_linear_bwd_workspace_min",
                "tern_linear_bwd_workspace",
                "tern_linear_bwd", "tern_linear_bwd_ex", "tern_linear_bwd_noalloc", "tern_linear_fwd_grouped",
                "tern_linear_bwd_grouped_workspace", "tern_linear_bwd_grouped", "adamw_step", "tern_grad_sumsq_workspace",
@@ -59,6 +59,11 @@ class TernError(RuntimeError):
 class _Tiles(ctypes.Structure):
     _fields_ = [("packed", ctypes.c_void_p), ("t_bf16", ctypes.c_void_p),
                 ("whi_bf16", ctypes.c_void_p), ("wlo_bf16", ctypes.c_void_p)]
+
+
+class _MatLayer(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("q_clamped", ctypes.c_void_p), ("scale", ctypes.c_void_p),
+                ("out", ctypes.POINTER(_Tiles)), ("K", ctypes.c_int64), ("N", ctypes.c_int64)]
 
 
 class _Layer(ctypes.Structure):
@@ -78,6 +83,7 @@ def _load():
     sigs = {
         "tern_tiles_bytes": ([i64, i64, ci], sz),
         "tern_materialize": ([vp, vp, vp, i64, i64, ci, ci, tp, vp], ci),
+        "tern_materialize_grouped": ([ctypes.POINTER(_MatLayer), ci, ci, ci, vp], ci),
         "tern_linear_fwd": ([vp, tp, vp, vp, i64, i64, i64, vp], ci),
         "tern_linear_bwd_workspace_min": ([i64, i64, i64], sz),
         "tern_linear_bwd_workspace": ([i64, i64, i64], sz),
@@ -194,6 +200,39 @@ class Materialize:
 
 def tern_materialize(q, scale, tiles: Tiles, theta=2, q_clamp=7, q_clamped=None, stream=None):
     Materialize(q, scale, tiles, theta, q_clamp, q_clamped)(stream)
+
+
+class MaterializeGrouped:
+    """tern_materialize_grouped over weights given as dicts with q, scale, tiles and
+    optionally q_clamped, arguments marshalled once; see GroupedForward."""
+
+    def __init__(self, weights, theta=2, q_clamp=7):
+        self._arr = (_MatLayer * len(weights))()
+        self._keep = []
+        for i, w in enumerate(weights):
+            q, tiles = w["q"], w["tiles"]
+            K, N = q.shape
+            if (tiles.K, tiles.N) != (K, N):
+                raise ValueError("tiles shape does not match q")
+            ct = tiles._c()
+            self._keep.append(ct)
+            c = self._arr[i]
+            c.q = _ptr(q, torch.int8, (K, N), "q")
+            c.q_clamped = _ptr(w.get("q_clamped"), torch.int8, (K, N), "q_clamped")
+            c.scale = _ptr(w.get("scale"), torch.float32, (N,), "scale")
+            c.out = ctypes.pointer(ct)
+            c.K, c.N = K, N
+        self._n = len(weights)
+        self._theta, self._clamp = int(theta), int(q_clamp)
+        self._refs = list(weights)
+
+    def __call__(self, stream=None):
+        _check(lib.tern_materialize_grouped(self._arr, self._n, self._theta, self._clamp, _stream(stream)),
+               "tern_materialize_grouped")
+
+
+def tern_materialize_grouped(weights, theta=2, q_clamp=7, stream=None):
+    MaterializeGrouped(weights, theta, q_clamp)(stream)
 
 
 def tern_linear_fwd(X, tiles: Tiles, scale, Y, stream=None):

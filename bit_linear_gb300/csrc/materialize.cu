@@ -14,6 +14,9 @@
 // take 16-weight groups (one packed word, a 16-byte q load); launches that write
 // the bf16 planes take 8-weight halves, so every plane store is one 16-byte
 // store per thread and a warp covers 512 contiguous bytes.
+#include <algorithm>
+#include <vector>
+
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -204,15 +207,11 @@ __device__ __forceinline__ void encode_half(const MatArgs& a, int2 raw, int64_t 
 
 }  // namespace
 
-// Which encodings a launch writes is a template choice, so the packed-only
-// ternarisation carries no registers for the bf16 planes.
+// One weight's pass: thread tid of nth walks the weight's items (grid-stride), eight
+// loads in flight before their encodes.
 template <bool QC, bool PK, bool TT, bool HL>
-__global__ void __launch_bounds__(256) tern_materialize_kernel(const MatArgs a) {
-    ptx::pdl_trigger();
-    ptx::pdl_wait();
+__device__ __forceinline__ void materialize_body(const MatArgs& a, int64_t tid, int64_t nth) {
     constexpr int U = 8;
-    const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if constexpr (TT || HL) {
         const int64_t halves = a.groups * 2;
         const int2* q2 = reinterpret_cast<const int2*>(a.q);
@@ -239,6 +238,38 @@ __global__ void __launch_bounds__(256) tern_materialize_kernel(const MatArgs a) 
     }
 }
 
+// Weights of a grouped call that request the same encodings: job j owns the blocks
+// [block_begin[j], block_begin[j+1]) of the launch.
+constexpr int kMatGroup = 16;
+struct MatGroup {
+    MatArgs job[kMatGroup];
+    int block_begin[kMatGroup + 1];
+    int count;
+};
+
+// Which encodings a launch writes is a template choice, so the packed-only
+// ternarisation carries no registers for the bf16 planes.
+template <bool QC, bool PK, bool TT, bool HL>
+__global__ void __launch_bounds__(256) tern_materialize_kernel(const MatArgs a) {
+    ptx::pdl_trigger();
+    ptx::pdl_wait();
+    materialize_body<QC, PK, TT, HL>(a, static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x,
+                                     static_cast<int64_t>(gridDim.x) * blockDim.x);
+}
+
+// Several weights in one launch, each on its own range of blocks.
+template <bool QC, bool PK, bool TT, bool HL>
+__global__ void __launch_bounds__(256) tern_materialize_group_kernel(const __grid_constant__ MatGroup g) {
+    ptx::pdl_trigger();
+    ptx::pdl_wait();
+    int j = 0;
+    while (j + 1 < g.count && static_cast<int>(blockIdx.x) >= g.block_begin[j + 1]) ++j;
+    const int b = static_cast<int>(blockIdx.x) - g.block_begin[j];
+    const int nb = g.block_begin[j + 1] - g.block_begin[j];
+    materialize_body<QC, PK, TT, HL>(g.job[j], static_cast<int64_t>(b) * blockDim.x + threadIdx.x,
+                                     static_cast<int64_t>(nb) * blockDim.x);
+}
+
 namespace {
 
 template <bool QC, bool PK, bool TT, bool HL>
@@ -255,6 +286,49 @@ int launch_materialize(const MatArgs& a, int num_sms, cudaStream_t s) {
     const int64_t cap = static_cast<int64_t>(num_sms) * per_sm;
     const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
     return launch_pdl(kernel, dim3(grid), dim3(256), 0, s, a);
+}
+
+// A grouped launch: each job gets blocks in proportion to its items (about eight items per
+// thread), within the resident-CTA budget of the GPU.
+template <bool QC, bool PK, bool TT, bool HL>
+int launch_materialize_group(MatGroup& g, int num_sms, cudaStream_t s) {
+    auto kernel = tern_materialize_group_kernel<QC, PK, TT, HL>;
+    static int per_sm = 0;
+    if (per_sm == 0) {
+        int b = 0;
+        TERN_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, 256, 0));
+        per_sm = b > 0 ? b : 1;
+    }
+    const int64_t cap = static_cast<int64_t>(num_sms) * per_sm;
+    int64_t want[kMatGroup], total = 0;
+    for (int j = 0; j < g.count; ++j) {
+        const int64_t items = (TT || HL) ? 2 * g.job[j].groups : g.job[j].groups;
+        want[j] = (items + 256 * 8 - 1) / (256 * 8);
+        total += want[j];
+    }
+    g.block_begin[0] = 0;
+    for (int j = 0; j < g.count; ++j) {
+        int64_t nb = total <= cap ? want[j] : std::max<int64_t>(1, want[j] * cap / total);
+        g.block_begin[j + 1] = g.block_begin[j] + static_cast<int>(nb);
+    }
+    return launch_pdl(kernel, dim3(static_cast<unsigned>(g.block_begin[g.count])), dim3(256), 0, s, g);
+}
+
+template <int QCv, int PKv, int TTv, int HLv>
+int launch_group_sig(MatGroup& g, int n, cudaStream_t s) {
+    return launch_materialize_group<QCv != 0, PKv != 0, TTv != 0, HLv != 0>(g, n, s);
+}
+
+// signature bits: 8 = clamp write-back, 4 = packed, 2 = bf16 T, 1 = hi/lo planes
+int launch_group_by_sig(int sig, MatGroup& g, int n, cudaStream_t s) {
+    switch (sig) {
+#define TERN_SIG(v) \
+    case v: return launch_group_sig<(v >> 3) & 1, (v >> 2) & 1, (v >> 1) & 1, v & 1>(g, n, s);
+        TERN_SIG(1) TERN_SIG(2) TERN_SIG(3) TERN_SIG(4) TERN_SIG(5) TERN_SIG(6) TERN_SIG(7) TERN_SIG(8)
+        TERN_SIG(9) TERN_SIG(10) TERN_SIG(11) TERN_SIG(12) TERN_SIG(13) TERN_SIG(14) TERN_SIG(15)
+#undef TERN_SIG
+    default: return TERN_OK;
+    }
 }
 
 template <bool QC, bool PK, bool TT>
@@ -275,6 +349,71 @@ int dispatch_pk(const MatArgs& a, bool pk, bool tt, bool hl, int n, cudaStream_t
 }  // namespace tern
 
 using namespace tern;
+
+namespace tern {
+namespace {
+
+// Checks one weight's arguments and fills its launch arguments; the encodings it asks for
+// come back as signature bits (8 clamp, 4 packed, 2 bf16 T, 1 hi/lo; 0 = nothing).
+int mat_args(const int8_t* q, int8_t* q_clamped, const float* scale, int64_t K, int64_t N, int theta, int q_clamp,
+             const tern_tiles* out, MatArgs* a, int* sig) {
+    if (!q || !out) return TERN_ERR_ARG;
+    if (K < 1 || N < 16 || K >= (1ll << 31) || N >= (1ll << 31) || K * N >= (1ll << 40)) return TERN_ERR_ARG;
+    if (theta < 1 || q_clamp < theta || q_clamp > 127) return TERN_ERR_ARG;
+    if ((out->whi_bf16 || out->wlo_bf16) && !scale) return TERN_ERR_ARG;
+    if (N % 16) return TERN_ERR_ALIGN;
+    const void* ptrs[] = {q, q_clamped, scale, out->packed, out->t_bf16, out->whi_bf16, out->wlo_bf16};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return TERN_ERR_ALIGN;
+    a->q = q;
+    a->qc = q_clamped;
+    a->scale = scale;
+    a->packed = out->packed;
+    a->t = out->t_bf16;
+    a->whi = out->whi_bf16;
+    a->wlo = out->wlo_bf16;
+    a->groups = K * N / 16;
+    a->ngroups_row = static_cast<uint32_t>(N / 16);
+    const uint32_t tb = static_cast<uint8_t>(theta), tn = static_cast<uint8_t>(-theta);
+    const uint32_t cb = static_cast<uint8_t>(q_clamp), cn = static_cast<uint8_t>(-q_clamp);
+    a->th_pos = tb * 0x01010101u;
+    a->th_neg = tn * 0x01010101u;
+    a->cl_pos = cb * 0x01010101u;
+    a->cl_neg = cn * 0x01010101u;
+    *sig = (q_clamped ? 8 : 0) | (out->packed ? 4 : 0) | (out->t_bf16 ? 2 : 0) |
+           ((out->whi_bf16 || out->wlo_bf16) ? 1 : 0);
+    return TERN_OK;
+}
+
+}  // namespace
+}  // namespace tern
+
+extern "C" int tern_materialize_grouped(const tern_mat_layer* layers, int count, int theta, int q_clamp,
+                                        void* stream) {
+    if (!layers || count < 1) return TERN_ERR_ARG;
+    std::vector<MatArgs> args(static_cast<size_t>(count));
+    std::vector<int> sigs(static_cast<size_t>(count));
+    for (int i = 0; i < count; ++i) {
+        const tern_mat_layer& l = layers[i];
+        if (int st = mat_args(l.q, l.q_clamped, l.scale, l.K, l.N, theta, q_clamp, l.out, &args[i], &sigs[i]))
+            return st;
+    }
+    int num_sms = 0;
+    if (int st = check_device(&num_sms)) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    for (int sig = 1; sig < 16; ++sig) {   // one launch per set of requested encodings (16 weights at a time)
+        MatGroup g;
+        g.count = 0;
+        for (int i = 0; i <= count; ++i) {
+            if (i < count && sigs[i] == sig) g.job[g.count++] = args[i];
+            if (g.count == kMatGroup || (i == count && g.count > 0)) {
+                if (int st = launch_group_by_sig(sig, g, num_sms, s)) return st;
+                g.count = 0;
+            }
+        }
+    }
+    return TERN_OK;
+}
 
 extern "C" int tern_materialize(const int8_t* q, int8_t* q_clamped, const float* scale, int64_t K, int64_t N,
                                 int theta, int q_clamp, const tern_tiles* out, void* stream) {

@@ -91,6 +91,23 @@ int tern_materialize(const int8_t* q, int8_t* q_clamped, const float* scale, int
                      int theta, int q_clamp, const tern_tiles* out, void* stream);
 
 /*
+ * tern_materialize for several weights in one call: one launch per set of requested
+ * encodings (16 weights at a time), each weight on its own range of blocks, so that
+ * the small weights of one block do not each pay a launch.  Same results, rules and
+ * errors as the single-weight call, weight by weight; nothing is enqueued if any
+ * weight's arguments are bad.  theta and q_clamp are shared by every weight.  The
+ * pages materialise each weight in its own passes; the grouping is this library's.
+ */
+typedef struct tern_mat_layer {
+    const int8_t* q;         /* [K][N] int8 accumulator (device, read) */
+    int8_t* q_clamped;       /* [K][N] clamped q (device, written; NULL to skip; may equal q) */
+    const float* scale;      /* [N] fp32 (device; may be NULL without hi/lo planes) */
+    const tern_tiles* out;   /* tiles to write (host struct of device pointers) */
+    int64_t K, N;
+} tern_mat_layer;
+int tern_materialize_grouped(const tern_mat_layer* layers, int count, int theta, int q_clamp, void* stream);
+
+/*
  * Forward: Y[m][c] = scale[c] * sum_r X[m][r] * T[r][c] (page "train_gpu.cu",
  * header comment: W_eff = scale[c]*ternary(q); the forward GEMM itself is the
  * off-page fm_forward).  The scale is applied in the epilogue, so W_eff is never

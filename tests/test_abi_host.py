@@ -171,3 +171,19 @@ def test_multi_tensor_calls_take_at_most_the_table_size(lib):
     assert lib.lib.tern_grad_sumsq(ptrs, ns, k, P(0x20000), P(0x30000), 1 << 20, None) == lib.TERN_ERR_ARG
     assert lib.lib.tern_grad_sumsq_workspace(ns, k) == 0
     assert lib.TERN_ADAM_MAX_TENSORS == 64
+
+
+def test_grouped_materialize_argument_checks(lib):
+    f = lib.lib.tern_materialize_grouped
+    t = _tiles(lib)
+    arr = (lib._MatLayer * 2)()
+    for i in range(2):
+        arr[i] = lib._MatLayer(P(0x20000), None, P(0x30000), ctypes.pointer(t), 64, 128)
+    assert f(None, 2, 2, 7, None) == lib.TERN_ERR_ARG
+    assert f(arr, 0, 2, 7, None) == lib.TERN_ERR_ARG
+    assert f(arr, 2, 3, 2, None) == lib.TERN_ERR_ARG          # clamp < theta
+    arr[1].N = 136                                             # not a multiple of 16
+    assert f(arr, 2, 2, 7, None) == lib.TERN_ERR_ALIGN
+    arr[1].N = 128
+    arr[0].q = P(0x20004)                                      # misaligned
+    assert f(arr, 2, 2, 7, None) == lib.TERN_ERR_ALIGN

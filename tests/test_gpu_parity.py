@@ -297,3 +297,38 @@ def test_forward_from_packed_codes_needs_n_multiple_of_64(cuda_lib):
     with pytest.raises(bl.TernError) as e:
         bl.tern_linear_fwd(layer.X, bl.Tiles(64, 48, packed=layer.tiles.packed), layer.scale, layer.Y)
     assert e.value.status == bl.TERN_ERR_ALIGN
+
+
+def test_grouped_materialize_matches_single_calls(cuda_lib):
+    """Several weights in one tern_materialize_grouped call, with different sets of
+    encodings (all planes; packed only; packed and hi/lo with the clamp written back):
+    every output bit-equal to the oracle."""
+    bl = cuda_lib
+    shapes = [(512, 512), (129, 4112), (40, 80), (2048, 512), (1, 16)]
+    ws, refs = [], []
+    for i, (K, N) in enumerate(shapes):
+        q = syn.int8_uniform(40 + i, 3, K * N, -128, 127).reshape(K, N)
+        scale = syn.uniform_f32(40 + i, 4, N, -0.1, 0.1)
+        refs.append((oracle.materialize(q, scale, 2, 7), q))
+        if i % 3 == 0:
+            tiles = bl.Tiles.empty(K, N)
+        elif i % 3 == 1:
+            tiles = bl.Tiles(K, N, packed=torch.zeros((K, N // 16), dtype=torch.int32, device="cuda"))
+        else:
+            tiles = bl.Tiles.empty(K, N, t=False)
+        w = dict(q=dev(q), scale=dev(scale), tiles=tiles)
+        if i % 3 == 2:
+            w["q_clamped"] = torch.full((K, N), 99, dtype=torch.int8, device="cuda")
+        ws.append(w)
+    bl.tern_materialize_grouped(ws, 2, 7)
+    torch.cuda.synchronize()
+    for (ref, q), w in zip(refs, ws):
+        t = w["tiles"]
+        np.testing.assert_array_equal(t.packed.cpu().numpy().view(np.uint32), ref["packed"])
+        if t.t_bf16 is not None:
+            np.testing.assert_array_equal(host_bits(t.t_bf16), ref["t"])
+        if t.whi_bf16 is not None:
+            np.testing.assert_array_equal(host_bits(t.whi_bf16), ref["whi"])
+            np.testing.assert_array_equal(host_bits(t.wlo_bf16), ref["wlo"])
+        if "q_clamped" in w:
+            np.testing.assert_array_equal(w["q_clamped"].cpu().numpy(), ref["qc"])
