@@ -67,11 +67,10 @@ __device__ int g_gemm_site[4];
 namespace {
 
 constexpr int kBM = 128;           // rows of A (and of D) per CTA
-// Output staging of the epilogue: eight 32 x 32 fp32 buffers (4 KB each, 128-byte
-// swizzle) per CTA, one per epilogue warp (two per warp with four epilogue warps), from
-// which one lane issues the TMA store of each chunk.
+// Output staging of the epilogue: one 32 x 32 fp32 buffer (4 KB) per epilogue warp, in
+// which the warp turns its chunk (lane = row) around so that each store instruction writes
+// four whole 128-byte rows.
 constexpr int kStageBuf = 32 * 32 * 4;
-constexpr int kStagingBytes = 8 * kStageBuf;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait; a healthy wait takes microseconds
 
 enum { EPI_FWD = 0, EPI_DX = 1, EPI_DW = 2 };
@@ -102,14 +101,13 @@ struct GemmGroup {
     CUtensorMap mA[G];
     CUtensorMap mB0[G];
     CUtensorMap mB1[G];
-    CUtensorMap mOut[G];   // fp32 output in 32 x 32 boxes: out, or partial_g for split units
     GemmArgs args[G];
     int unit_begin[G + 1];
     int count;
 };
 
-// Problems per grouped launch: four tensor maps each keep the parameter block under 4 KB.
-constexpr int kGroup = 6;
+// Problems per grouped launch: with three tensor maps each the parameter block stays under 4 KB.
+constexpr int kGroup = 8;
 static_assert(sizeof(GemmGroup<kGroup>) <= 4096, "kernel parameter block over 4 KB");
 
 template <int G>
@@ -132,8 +130,8 @@ struct Cfg {
     // warps: producer, MMA, EPI_WARPS epilogue warps (two per TMEM lane quarter, each taking
     // half the columns; four when PK), and for PK two teams of four converter warps
     static constexpr int EPI_WARPS = PK ? 4 : 8;
-    static constexpr int NBUF = 8 / EPI_WARPS;   // staging buffers per epilogue warp
     static constexpr int THREADS = 64 + 32 * EPI_WARPS + (PK ? 256 : 0);
+    static constexpr int STAGING_BYTES = EPI_WARPS * kStageBuf;
     static constexpr int TILE_M = kBM * CG;
     static constexpr int B_ROWS = BN / CG;
     static constexpr int A_BYTES = kBM * BK * 2;
@@ -142,7 +140,7 @@ struct Cfg {
     static constexpr int TX_BYTES = CG * (PK ? A_BYTES : STAGE_BYTES);   // TMA bytes on the leader's barrier
     static constexpr int P_BYTES = PK ? BK * (B_ROWS / 16) * 4 : 0;     // 2-bit codes of a stage's B (PK)
     static constexpr int TMEM_COLS = 2 * BN;
-    static constexpr int SMEM_BYTES = STAGES * (STAGE_BYTES + P_BYTES) + kStagingBytes + 1024 + 256;
+    static constexpr int SMEM_BYTES = STAGES * (STAGE_BYTES + P_BYTES) + STAGING_BYTES + 1024 + 256;
     static_assert(CG == 1 || CG == 2, "CTA group");
     static_assert(BK == 64 || (BK == 32 && !A_MN && !B_MN), "MN-major operands use 64-deep k-blocks");
     static_assert(BN % 64 == 0 && BN <= 256 && B_ROWS % 64 == 0, "BN");
@@ -160,8 +158,8 @@ using Fwd2 = Cfg<2, 256, 64, false, true, 1, EPI_FWD, 6>;
 using Dx2 = Cfg<2, 256, 64, false, false, 2, EPI_DX, 4>;
 using Dw2 = Cfg<2, 256, 64, true, true, 1, EPI_DW, 6>;
 // The forward with T read as 2-bit codes.
-using FwdP1 = Cfg<1, 256, 64, false, true, 1, EPI_FWD, 3, true>;
-using FwdP2 = Cfg<2, 256, 64, false, true, 1, EPI_FWD, 5, true>;
+using FwdP1 = Cfg<1, 256, 64, false, true, 1, EPI_FWD, 4, true>;
+using FwdP2 = Cfg<2, 256, 64, false, true, 1, EPI_FWD, 6, true>;
 
 // tcgen05 instruction descriptor, kind::f16: bf16 A/B, fp32 D, M x N, operand majors.
 __host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool a_mn, bool b_mn) {
@@ -263,30 +261,35 @@ __device__ __forceinline__ float warp_column_sums(float (&v)[32], int lane) {
     return v[0];
 }
 
-// Stage one 32 x 32 fp32 chunk of a warp (lane = row, v = its 32 columns) in shared
-// memory with the 128-byte swizzle of the output tensor map, then let one lane issue
-// the chunk's TMA store (or fp32 add) at column x, row y; rows and columns past the
-// tensor's edge are clipped by the copy.  NBUF buffers per warp: before one is
-// rewritten, the store issued from it NBUF chunks earlier must have read it.
-template <int NBUF>
-__device__ __forceinline__ void store_chunk(const CUtensorMap* map, uint32_t stage, int& nchunk, const float (&v)[32],
-                                            int x, int y, bool add, int lane) {
-    const uint32_t buf = stage + static_cast<uint32_t>(nchunk % NBUF) * kStageBuf;
-    if (nchunk >= NBUF && lane == 0) ptx::bulk_wait_read<NBUF - 1>();
-    __syncwarp();
-    const uint32_t row = buf + static_cast<uint32_t>(lane) * 128u;
+// Store one 32 x 32 fp32 chunk of a warp (lane = row, v = its 32 columns) to global
+// memory at `base` (row stride ld), rows < rows and columns < cols only.  The warp turns
+// the chunk around in its 4 KB buffer (16-byte units XOR-swizzled by row, so neither side
+// has bank conflicts): afterwards lane l holds four consecutive columns of a row, and
+// each of the eight store instructions writes four whole 128-byte rows.  With add, the
+// stored values are added to what is in memory (gradient accumulation).
+__device__ __forceinline__ void store_chunk(float* base, int64_t ld, int rows, int cols, uint32_t buf,
+                                            const float (&v)[32], bool add, int lane) {
+    __syncwarp();   // every lane is done reading the previous chunk from buf
+    const uint32_t own = buf + static_cast<uint32_t>(lane) * 128u;
 #pragma unroll
     for (int c = 0; c < 8; ++c)
-        ptx::st_shared_v4(row + (static_cast<uint32_t>(c ^ (lane & 7)) << 4), v[4 * c], v[4 * c + 1], v[4 * c + 2],
+        ptx::st_shared_v4(own + (static_cast<uint32_t>(c ^ (lane & 7)) << 4), v[4 * c], v[4 * c + 1], v[4 * c + 2],
                           v[4 * c + 3]);
-    ptx::fence_proxy_async_smem();   // the generic-proxy writes above, before the async-proxy read
     __syncwarp();
-    if (lane == 0) {
-        if (add) ptx::tma_reduce_add_2d(map, buf, x, y);
-        else ptx::tma_store_2d(map, buf, x, y);
-        ptx::bulk_commit();
+    const int cq = lane & 7;   // this lane's 16-byte column group
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = 4 * i + (lane >> 3);
+        float4 x = ptx::ld_shared_v4(buf + static_cast<uint32_t>(r) * 128u + (static_cast<uint32_t>(cq ^ (r & 7)) << 4));
+        if (r < rows && 4 * cq < cols) {
+            float4* g = reinterpret_cast<float4*>(base + static_cast<int64_t>(r) * ld + 4 * cq);
+            if (add) {
+                const float4 o = *g;
+                x = make_float4(o.x + x.x, o.y + x.y, o.z + x.z, o.w + x.w);
+            }
+            *g = x;
+        }
     }
-    ++nchunk;
 }
 
 // Two weights of a packed word as one bf16 pair: t holds code i at bits 0-1 and code
@@ -314,9 +317,9 @@ __device__ __forceinline__ void load_tile_scales(const float* scale, int col0, i
 // scales as load_tile_scales spreads them.  tile128 is the index of the 128-row block
 // the rows lie in.
 template <class C>
-__device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const CUtensorMap* omap, uint32_t stage,
-                                               int& nchunk, const uint32_t (&r)[32], const float (&sc)[8], int j,
-                                               int row, int wrow, int c0, int tile128, int quad, int lane) {
+__device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, uint32_t stage, const uint32_t (&r)[32],
+                                               const float (&sc)[8], int j, int row, int wrow, int c0, int tile128,
+                                               int quad, int lane) {
     const bool row_ok = row < a.Mg;
     const bool hi_ok = c0 + 16 < a.Ng;   // N is a multiple of 16: the chunk's second half may lie past it
     float v[32];
@@ -336,10 +339,10 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const CUtensor
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] *= __shfl_sync(0xffffffffu, sc[i & 7], 4 * j + (i >> 3));
     }
-    // fp32 output through shared memory and TMA (gq += ... with accumulate: a TMA add);
-    // the condition is the same for the whole warp
+    // fp32 output (gq += ... with accumulate); the condition is the same for the whole warp
     if (a.out != nullptr && wrow < a.Mg)
-        store_chunk<C::NBUF>(omap, stage, nchunk, v, c0, wrow, C::EPI == EPI_DW && a.accumulate != 0, lane);
+        store_chunk(a.out + static_cast<int64_t>(wrow) * a.Ng + c0, a.Ng, a.Mg - wrow, a.Ng - c0, stage, v,
+                    C::EPI == EPI_DW && a.accumulate != 0, lane);
     if constexpr (C::EPI != EPI_DW) {
         if (a.out_bf16 != nullptr && row_ok) {   // 16 columns -> 32 bytes, round to nearest even
             const int64_t at = static_cast<int64_t>(row) * a.Ng + c0;
@@ -390,9 +393,9 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
     uint64_t* bars =
-        reinterpret_cast<uint64_t*>(gbase + C::STAGES * (C::STAGE_BYTES + C::P_BYTES) + kStagingBytes);
+        reinterpret_cast<uint64_t*>(gbase + C::STAGES * (C::STAGE_BYTES + C::P_BYTES) + C::STAGING_BYTES);
     const uint32_t staging0 = base + static_cast<uint32_t>(C::STAGES * C::STAGE_BYTES);
-    const uint32_t pring0 = staging0 + static_cast<uint32_t>(kStagingBytes);   // PK: codes of each stage
+    const uint32_t pring0 = staging0 + static_cast<uint32_t>(C::STAGING_BYTES);   // PK: codes of each stage
     // FULL, EMPTY (per stage), TFULL, TEMPTY (per accumulator), DRAIN, then (PK only) BREADY
     // (per stage: converters done with its B operand) and PFULL (per stage: its codes landed
     // in this CTA), then the TMEM address and abort flag
@@ -672,11 +675,10 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
         // ------------------------------------------------------------ epilogue
         const int quad = warp & 3;   // a warp may touch TMEM lanes 32*(warp%4) .. +31
         const uint32_t tempty_leader = CG == 2 ? ptx::mapa_shared(TEMPTY0, 0) : TEMPTY0;
-        const uint32_t stage = staging0 + static_cast<uint32_t>(warp - 2) * C::NBUF * kStageBuf;
+        const uint32_t stage = staging0 + static_cast<uint32_t>(warp - 2) * kStageBuf;
         // with eight epilogue warps, warps 2-5 take the tile's first BN/2 columns and 6-9 the rest
         constexpr int JPW = C::BN / 32 / (C::EPI_WARPS / 4);   // 32-column chunks per warp and tile
         const int j0 = ((warp - 2) / 4) * JPW;
-        int nchunk = 0;   // chunks this warp has staged (its buffer parity)
         int local = 0;
         // the column scales of a unit's tile (none for dX and for split units' raw tiles)
         auto unit_scales = [&](int ugn, float (&sc)[8]) {
@@ -713,11 +715,11 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
             tile_coords<16 / CG>(a.tile_begin + u / a.split, a.tiles_m, a.tiles_n, mt, nt);
             const int row0 = mt * C::TILE_M + static_cast<int>(rank) * kBM;
             const uint32_t trow = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * C::BN;
-            const CUtensorMap* omap = &grp.mOut[p];
             if (C::EPI == EPI_DW && a.partial_g != nullptr) {
                 // split unit: the raw partial tile (row-major TILE_M x BN, unit after unit in
-                // partial_g, which omap describes) for the reduce kernel
-                const int prow = u * C::TILE_M + static_cast<int>(rank) * kBM + quad * 32;
+                // partial_g) for the reduce kernel
+                float* pg = a.partial_g + (static_cast<int64_t>(u) * C::TILE_M + static_cast<int>(rank) * kBM + quad * 32) *
+                                              C::BN;
 #pragma unroll 1
                 for (int j = j0; j < j0 + JPW; ++j) {
                     uint32_t r[32];
@@ -726,7 +728,7 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
                     float v[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-                    store_chunk<C::NBUF>(omap, stage, nchunk, v, j * 32, prow, false, lane);
+                    store_chunk(pg + j * 32, C::BN, 32, 32, stage, v, false, lane);
                 }
             } else if (row0 < a.Mg) {   // a pair's second half may lie wholly past the last row
                 const int tile128 = mt * CG + static_cast<int>(rank);
@@ -738,8 +740,7 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
                     uint32_t r[32];
                     ptx::tmem_ld_32x32b_x32(trow + j * 32, r);
                     ptx::tmem_wait_ld();
-                    epilogue_chunk<C>(a, omap, stage, nchunk, r, sc_cur, j, wrow + lane, wrow, c0, tile128, quad,
-                                      lane);
+                    epilogue_chunk<C>(a, stage, r, sc_cur, j, wrow + lane, wrow, c0, tile128, quad, lane);
                 }
             }
 #pragma unroll
@@ -751,10 +752,6 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
                 else ptx::mbar_arrive(TEMPTY0 + 8u * acc);
             }
         }
-        // every TMA store of this warp has written its box before the CTA's shared
-        // memory goes away (the copies end by themselves: nothing they wait on)
-        if (lane == 0) ptx::bulk_wait_all();
-        __syncwarp();
     }
 
     ptx::tc_fence_before();
@@ -1049,13 +1046,6 @@ int map_bf16(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, int 
                                static_cast<int>(CU_TENSOR_MAP_DATA_TYPE_BFLOAT16)});
 }
 
-// Tensor map of a row-major fp32 output [rows][cols], written by the epilogues in boxes
-// of 32 x 32 with the 128-byte swizzle (cols % 4 == 0, base 16-byte aligned).
-int map_f32_out(CUtensorMap* m, const float* ptr, int64_t cols, int64_t rows) {
-    return encode_2d(m, MapKey{ptr, cols, rows, 32, 32, static_cast<int>(CU_TENSOR_MAP_SWIZZLE_128B),
-                               static_cast<int>(CU_TENSOR_MAP_DATA_TYPE_FLOAT32)});
-}
-
 // Boxes of one operand: K-major tiles are read as one box of BK x rows; MN-major
 // tiles as 64-wide boxes of BK k-rows.
 template <class C>
@@ -1169,9 +1159,6 @@ int group_set(GemmGroup<G>& g, int p, const void* A, int64_t a_inner, int64_t a_
         g.mB1[p] = g.mB0[p];
     }
     g.args[p] = a;
-    // the epilogue's fp32 output: out [Mg][Ng], or the split units' partial tiles
-    if (a.partial_g) return map_f32_out(&g.mOut[p], a.partial_g, C::BN, static_cast<int64_t>(a.num_units) * C::TILE_M);
-    if (a.out) return map_f32_out(&g.mOut[p], a.out, a.Ng, a.Mg);
     return TERN_OK;
 }
 
@@ -1268,8 +1255,6 @@ int run_dw(K kernel, const uint16_t* X, const uint16_t* dY, const float* scale, 
                 t.split = split;
                 t.kb_per = kb_per;
                 t.partial_g = tail;
-                if (int st = map_f32_out(&g.mOut[0], tail, C::BN, static_cast<int64_t>(t.num_units) * C::TILE_M))
-                    return st;
                 group_close(g, 1);
                 if (int st = launch<C>(kernel, g, num_sms, s)) return st;
                 ReduceGroup<1> r;
@@ -1570,8 +1555,6 @@ int dw_group(K kernel, const tern_layer* L, const int* idx, int n, float* const*
         a.kb_per = kb_per;
         a.num_units = a.num_tiles * a.split;
         a.partial_g = tail + off;
-        if (int st = map_f32_out(&g.mOut[i], a.partial_g, C::BN, static_cast<int64_t>(a.num_units) * C::TILE_M))
-            return st;
         off += static_cast<int64_t>(a.num_units) * C::TILE_M * C::BN;
         r.args[i] = a;
         r.block_begin[i + 1] = r.block_begin[i] + a.num_tiles * (C::TILE_M / 32) * (C::BN / 128);

@@ -195,7 +195,7 @@ typedef struct tern_layer {
  * Y_bf16, when given, receives Y rounded to bf16 from the same epilogue, so the
  * next layer of a chain reads its input without a separate cast; Y may then be
  * NULL.
- * Layers are launched up to six at a time; a layer's Y must not overlap
+ * Layers are launched up to eight at a time; a layer's Y must not overlap
  * another layer's inputs.
  * Known issue of an earlier build: with the GEMMs launched by programmatic
  * dependent launch (their set-up overlapping the previous kernel), a process that
