@@ -67,10 +67,6 @@ __device__ int g_gemm_site[4];
 namespace {
 
 constexpr int kBM = 128;           // rows of A (and of D) per CTA
-// Output staging of the epilogue: one 32 x 32 fp32 buffer (4 KB) per epilogue warp, in
-// which the warp turns its chunk (lane = row) around so that each store instruction writes
-// four whole 128-byte rows.
-constexpr int kStageBuf = 32 * 32 * 4;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait; a healthy wait takes microseconds
 
 enum { EPI_FWD = 0, EPI_DX = 1, EPI_DW = 2 };
@@ -131,7 +127,6 @@ struct Cfg {
     // half the columns; four when PK), and for PK two teams of four converter warps
     static constexpr int EPI_WARPS = PK ? 4 : 8;
     static constexpr int THREADS = 64 + 32 * EPI_WARPS + (PK ? 256 : 0);
-    static constexpr int STAGING_BYTES = EPI_WARPS * kStageBuf;
     static constexpr int TILE_M = kBM * CG;
     static constexpr int B_ROWS = BN / CG;
     static constexpr int A_BYTES = kBM * BK * 2;
@@ -140,7 +135,7 @@ struct Cfg {
     static constexpr int TX_BYTES = CG * (PK ? A_BYTES : STAGE_BYTES);   // TMA bytes on the leader's barrier
     static constexpr int P_BYTES = PK ? BK * (B_ROWS / 16) * 4 : 0;     // 2-bit codes of a stage's B (PK)
     static constexpr int TMEM_COLS = 2 * BN;
-    static constexpr int SMEM_BYTES = STAGES * (STAGE_BYTES + P_BYTES) + STAGING_BYTES + 1024 + 256;
+    static constexpr int SMEM_BYTES = STAGES * (STAGE_BYTES + P_BYTES) + 1024 + 256;
     static_assert(CG == 1 || CG == 2, "CTA group");
     static_assert(BK == 64 || (BK == 32 && !A_MN && !B_MN), "MN-major operands use 64-deep k-blocks");
     static_assert(BN % 64 == 0 && BN <= 256 && B_ROWS % 64 == 0, "BN");
@@ -151,12 +146,12 @@ struct Cfg {
 
 // One CTA per 128 x 256 tile (small problems).
 using Fwd1 = Cfg<1, 256, 64, false, true, 1, EPI_FWD, 4>;   // A = X (K-major), B = T [K][N] (MN-major)
-using Dx1 = Cfg<1, 256, 32, false, false, 2, EPI_DX, 4>;    // A = dY (K-major), B = W_hi, W_lo (K-major)
+using Dx1 = Cfg<1, 256, 32, false, false, 2, EPI_DX, 5>;    // A = dY (K-major), B = W_hi, W_lo (K-major)
 using Dw1 = Cfg<1, 256, 64, true, true, 1, EPI_DW, 4>;      // A = X^T, B = dY^T (both MN-major)
 // A CTA pair per 256 x 256 tile: half the shared-memory operand traffic per MMA.
-using Fwd2 = Cfg<2, 256, 64, false, true, 1, EPI_FWD, 6>;
+using Fwd2 = Cfg<2, 256, 64, false, true, 1, EPI_FWD, 7>;
 using Dx2 = Cfg<2, 256, 64, false, false, 2, EPI_DX, 4>;
-using Dw2 = Cfg<2, 256, 64, true, true, 1, EPI_DW, 6>;
+using Dw2 = Cfg<2, 256, 64, true, true, 1, EPI_DW, 7>;
 // The forward with T read as 2-bit codes.
 using FwdP1 = Cfg<1, 256, 64, false, true, 1, EPI_FWD, 4, true>;
 using FwdP2 = Cfg<2, 256, 64, false, true, 1, EPI_FWD, 6, true>;
@@ -262,26 +257,39 @@ __device__ __forceinline__ float warp_column_sums(float (&v)[32], int lane) {
 }
 
 // Store one 32 x 32 fp32 chunk of a warp (lane = row, v = its 32 columns) to global
-// memory at `base` (row stride ld), rows < rows and columns < cols only.  The warp turns
-// the chunk around in its 4 KB buffer (16-byte units XOR-swizzled by row, so neither side
-// has bank conflicts): afterwards lane l holds four consecutive columns of a row, and
-// each of the eight store instructions writes four whole 128-byte rows.  With add, the
-// stored values are added to what is in memory (gradient accumulation).
-__device__ __forceinline__ void store_chunk(float* base, int64_t ld, int rows, int cols, uint32_t buf,
-                                            const float (&v)[32], bool add, int lane) {
-    __syncwarp();   // every lane is done reading the previous chunk from buf
-    const uint32_t own = buf + static_cast<uint32_t>(lane) * 128u;
+// memory at `base` (row stride ld), rows < rows and columns < cols only.  Within each
+// group of eight lanes the 8 x 8 block of 16-byte units is transposed by three butterfly
+// stages of warp shuffles (no shared memory, which the operand pipeline keeps busy):
+// afterwards lane l holds unit l & 7 of the group's eight rows, and each of the eight
+// store instructions writes four whole 128-byte rows.  With add, the stored values are
+// added to what is in memory (gradient accumulation).
+__device__ __forceinline__ void store_chunk(float* base, int64_t ld, int rows, int cols, const float (&v)[32], bool add,
+                                            int lane) {
+    float4 u[8];
 #pragma unroll
-    for (int c = 0; c < 8; ++c)
-        ptx::st_shared_v4(own + (static_cast<uint32_t>(c ^ (lane & 7)) << 4), v[4 * c], v[4 * c + 1], v[4 * c + 2],
-                          v[4 * c + 3]);
-    __syncwarp();
+    for (int i = 0; i < 8; ++i) u[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+#pragma unroll
+    for (int d = 4; d >= 1; d >>= 1) {
+        const bool upper = (lane & d) != 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (i & d) continue;
+            const float4 send = upper ? u[i] : u[i | d];
+            float4 recv;
+            recv.x = __shfl_xor_sync(0xffffffffu, send.x, d);
+            recv.y = __shfl_xor_sync(0xffffffffu, send.y, d);
+            recv.z = __shfl_xor_sync(0xffffffffu, send.z, d);
+            recv.w = __shfl_xor_sync(0xffffffffu, send.w, d);
+            if (upper) u[i] = recv;
+            else u[i | d] = recv;
+        }
+    }
     const int cq = lane & 7;   // this lane's 16-byte column group
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const int r = 4 * i + (lane >> 3);
-        float4 x = ptx::ld_shared_v4(buf + static_cast<uint32_t>(r) * 128u + (static_cast<uint32_t>(cq ^ (r & 7)) << 4));
+        const int r = (lane & ~7) + i;
         if (r < rows && 4 * cq < cols) {
+            float4 x = u[i];
             float4* g = reinterpret_cast<float4*>(base + static_cast<int64_t>(r) * ld + 4 * cq);
             if (add) {
                 const float4 o = *g;
@@ -317,7 +325,7 @@ __device__ __forceinline__ void load_tile_scales(const float* scale, int col0, i
 // scales as load_tile_scales spreads them.  tile128 is the index of the 128-row block
 // the rows lie in.
 template <class C>
-__device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, uint32_t stage, const uint32_t (&r)[32],
+__device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const uint32_t (&r)[32],
                                                const float (&sc)[8], int j, int row, int wrow, int c0, int tile128,
                                                int quad, int lane) {
     const bool row_ok = row < a.Mg;
@@ -341,7 +349,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, uint32_t stage
     }
     // fp32 output (gq += ... with accumulate); the condition is the same for the whole warp
     if (a.out != nullptr && wrow < a.Mg)
-        store_chunk(a.out + static_cast<int64_t>(wrow) * a.Ng + c0, a.Ng, a.Mg - wrow, a.Ng - c0, stage, v,
+        store_chunk(a.out + static_cast<int64_t>(wrow) * a.Ng + c0, a.Ng, a.Mg - wrow, a.Ng - c0, v,
                     C::EPI == EPI_DW && a.accumulate != 0, lane);
     if constexpr (C::EPI != EPI_DW) {
         if (a.out_bf16 != nullptr && row_ok) {   // 16 columns -> 32 bytes, round to nearest even
@@ -392,10 +400,8 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    uint64_t* bars =
-        reinterpret_cast<uint64_t*>(gbase + C::STAGES * (C::STAGE_BYTES + C::P_BYTES) + C::STAGING_BYTES);
-    const uint32_t staging0 = base + static_cast<uint32_t>(C::STAGES * C::STAGE_BYTES);
-    const uint32_t pring0 = staging0 + static_cast<uint32_t>(C::STAGING_BYTES);   // PK: codes of each stage
+    uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + C::STAGES * (C::STAGE_BYTES + C::P_BYTES));
+    const uint32_t pring0 = base + static_cast<uint32_t>(C::STAGES * C::STAGE_BYTES);   // PK: codes of each stage
     // FULL, EMPTY (per stage), TFULL, TEMPTY (per accumulator), DRAIN, then (PK only) BREADY
     // (per stage: converters done with its B operand) and PFULL (per stage: its codes landed
     // in this CTA), then the TMEM address and abort flag
@@ -675,7 +681,6 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
         // ------------------------------------------------------------ epilogue
         const int quad = warp & 3;   // a warp may touch TMEM lanes 32*(warp%4) .. +31
         const uint32_t tempty_leader = CG == 2 ? ptx::mapa_shared(TEMPTY0, 0) : TEMPTY0;
-        const uint32_t stage = staging0 + static_cast<uint32_t>(warp - 2) * kStageBuf;
         // with eight epilogue warps, warps 2-5 take the tile's first BN/2 columns and 6-9 the rest
         constexpr int JPW = C::BN / 32 / (C::EPI_WARPS / 4);   // 32-column chunks per warp and tile
         const int j0 = ((warp - 2) / 4) * JPW;
@@ -728,7 +733,7 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
                     float v[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-                    store_chunk(pg + j * 32, C::BN, 32, 32, stage, v, false, lane);
+                    store_chunk(pg + j * 32, C::BN, 32, 32, v, false, lane);
                 }
             } else if (row0 < a.Mg) {   // a pair's second half may lie wholly past the last row
                 const int tile128 = mt * CG + static_cast<int>(rank);
@@ -740,7 +745,7 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
                     uint32_t r[32];
                     ptx::tmem_ld_32x32b_x32(trow + j * 32, r);
                     ptx::tmem_wait_ld();
-                    epilogue_chunk<C>(a, stage, r, sc_cur, j, wrow + lane, wrow, c0, tile128, quad, lane);
+                    epilogue_chunk<C>(a, r, sc_cur, j, wrow + lane, wrow, c0, tile128, quad, lane);
                 }
             }
 #pragma unroll
