@@ -963,6 +963,13 @@ def run_ours(args):
             del qt, tt
         extra["ternarise"] = dict(bytes_per_elem=1.25, **sweep[-1])
         extra["ternarise_sweep"] = sweep
+        # the step's own materialise (all four encodings, 7.25 B per weight) timed alone as
+        # graph-replayed calls: the in-step figure above also holds the launch and event gaps
+        ma = bl.Tiles.empty(K, N)
+        extra["materialise_all_planes_alone"] = dict(
+            bytes_per_elem=7.25, n=K * N, **bw_loop(lambda: bl.tern_materialize(q, scale, ma, 2, 7), 7.25 * K * N,
+                                                    reps=20))
+        del ma
         torch.cuda.empty_cache()
     dog.cancel()
 

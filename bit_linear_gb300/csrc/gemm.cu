@@ -26,7 +26,9 @@
 // independent problems (one layer is a group of one).
 //   warp 0     TMA producer (one thread): STAGES-deep ring of operand stages
 //   warp 1     TMEM allocator + MMA issuer (one thread, the pair's leader)
-//   warps 2-5  epilogue: TMEM -> registers -> global, one TMEM lane quarter each
+//   warps 2-9  epilogue: TMEM -> registers -> global, two warps per TMEM lane quarter,
+//              each taking half of a tile's columns (the 2-bit forward: warps 2-5, one per
+//              quarter, and warps 6-13 expand the 2-bit T codes into bf16 operand tiles)
 // Two TMEM accumulators (2 x BN columns) let the epilogue of tile i overlap the
 // main loop of tile i+1.  Before exit the producer waits for the release of every
 // stage it filled and the MMA thread for the release of the last accumulators, so

@@ -111,7 +111,10 @@ int tern_materialize_grouped(const tern_mat_layer* layers, int count, int theta,
  * Forward: Y[m][c] = scale[c] * sum_r X[m][r] * T[r][c] (page "train_gpu.cu",
  * header comment: W_eff = scale[c]*ternary(q); the forward GEMM itself is the
  * off-page fm_forward).  The scale is applied in the epilogue, so W_eff is never
- * formed.  Reads W->t_bf16.
+ * formed.  Reads W->t_bf16; with W->t_bf16 NULL it reads W->packed instead and
+ * expands the 2-bit codes into bf16 operand tiles inside the GEMM (same result,
+ * bit for bit; N must then be a multiple of 64, else TERN_ERR_ALIGN).  With neither
+ * plane given: TERN_ERR_ARG.
  *   X [M][K] bf16 (device), scale [N] fp32 (device), Y [M][N] fp32 (device, written).
  * M >= 1; K, N >= 16 and multiples of 16; pointers 16-byte aligned.
  * Tensor cores, bf16 x {-1,0,+1} products (exact), fp32 accumulation.
