@@ -63,6 +63,11 @@ def _bind(lib):
         "or_bf16_value": ([ctypes.c_uint16], dbl),
         "or_bf16_round": ([dbl], ctypes.c_uint16),
         "or_materialize": ([vp, vp, i64, i64, ci, ci, vp, vp, vp, vp, vp], None),
+        "or_f16_value": ([ctypes.c_uint16], dbl),
+        "or_f16_round": ([dbl], ctypes.c_uint16),
+        "or_e4m3_value": ([ctypes.c_uint8], dbl),
+        "or_e4m3_round": ([dbl], ctypes.c_uint8),
+        "or_split8_planes": ([vp, vp, i64, i64, ci, ci, vp, vp], None),
         "or_fwd": ([vp, vp, vp, i64, i64, i64, ci, vp, vp, ci], None),
         "or_dx": ([vp, vp, vp, i64, i64, i64, ci, vp, vp, ci], None),
         "or_dw": ([vp, vp, vp, vp, i64, i64, i64, ci, vp, vp, vp, vp, ci], None),
@@ -112,6 +117,34 @@ def bf16_value(bits: int) -> float:
 
 def bf16_round(x: float) -> int:
     return int(_L().or_bf16_round(float(x)))
+
+
+def f16_value(bits: int) -> float:
+    return _L().or_f16_value(int(bits))
+
+
+def f16_round(x: float) -> int:
+    return int(_L().or_f16_round(float(x)))
+
+
+def e4m3_value(bits: int) -> float:
+    return _L().or_e4m3_value(int(bits))
+
+
+def e4m3_round(x: float) -> int:
+    return int(_L().or_e4m3_round(float(x)))
+
+
+def split8_planes(q, scale, theta=SR4_THETA, q_clamp=SR4_Q_CLAMP):
+    """The fp16 + e4m3 dX operands: returns (wh16 [K,N] uint16 binary16 bits,
+    wl8 [K,N] uint8 e4m3 bits)."""
+    q = _c(q, np.int8)
+    K, N = q.shape
+    scale = _c(scale, np.float32)
+    wh16 = np.empty((K, N), np.uint16)
+    wl8 = np.empty((K, N), np.uint8)
+    _L().or_split8_planes(_p(q), _p(scale), K, N, int(theta), int(q_clamp), _p(wh16), _p(wl8))
+    return wh16, wl8
 
 
 def materialize(q, scale, theta=SR4_THETA, q_clamp=SR4_Q_CLAMP):

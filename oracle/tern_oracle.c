@@ -83,6 +83,67 @@ uint16_t or_bf16_round(double x) {
     return (uint16_t)(u >> 16);
 }
 
+/* x rounded to a binary floating-point grid of p significant bits whose smallest
+ * normal exponent is emin (below it the spacing stays 2^(emin-p+1): subnormals),
+ * ties to even, with unbounded exponent range above.  The caller handles overflow. */
+static double or_round_grid(double x, int p, int emin) {
+    if (x == 0.0 || !isfinite(x)) return x;
+    int e;
+    frexp(fabs(x), &e);                     /* floor(log2|x|) = e - 1 */
+    int lsb = (e - 1 > emin ? e - 1 : emin) - (p - 1);   /* exponent of one unit in the last place */
+    double r = ldexp(nearbyint(ldexp(fabs(x), -lsb)), lsb);   /* default rounding: ties to even */
+    return x < 0 ? -r : r;
+}
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits;
+ * normal values 2^-14 .. 65504, subnormals k * 2^-24.  Value of a bit pattern. */
+double or_f16_value(uint16_t h) {
+    int sgn = h >> 15, ex = (h >> 10) & 0x1F, fr = h & 0x3FF;
+    double v;
+    if (ex == 0x1F) v = fr ? NAN : INFINITY;
+    else if (ex == 0) v = ldexp((double)fr, -24);
+    else v = ldexp(1.0 + fr / 1024.0, ex - 15);
+    return sgn ? -v : v;
+}
+
+/* binary16 nearest to x, ties to even; beyond 65504 + half a unit it is infinity
+ * (IEEE 754 round to nearest).  Finite x; returned as its bit pattern. */
+uint16_t or_f16_round(double x) {
+    uint16_t sgn = signbit(x) ? 0x8000u : 0u;
+    double r = fabs(or_round_grid(x, 11, -14));
+    if (r == 0.0) return sgn;
+    if (r > 65504.0) return sgn | 0x7C00u;
+    int e;
+    frexp(r, &e);
+    if (e - 1 < -14) return sgn | (uint16_t)ldexp(r, 24);   /* subnormal: r / 2^-24 */
+    return sgn | (uint16_t)((e - 1 + 15) << 10) | (uint16_t)(ldexp(r, -(e - 1)) * 1024.0 - 1024.0);
+}
+
+/* 8-bit E4M3 (OCP 8-bit floating point, the tensor cores' e4m3): 1 sign bit, 4
+ * exponent bits (bias 7), 3 fraction bits, no infinities, S.1111.111 = NaN;
+ * normal values 2^-6 .. 448, subnormals k * 2^-9.  Value of a bit pattern. */
+double or_e4m3_value(uint8_t b) {
+    int sgn = b >> 7, ex = (b >> 3) & 0xF, fr = b & 7;
+    double v;
+    if (ex == 0xF && fr == 7) v = NAN;
+    else if (ex == 0) v = ldexp((double)fr, -9);
+    else v = ldexp(1.0 + fr / 8.0, ex - 7);
+    return sgn ? -v : v;
+}
+
+/* E4M3 nearest to x, ties to even, saturating: a magnitude that rounds above 448
+ * becomes 448 (the "satfinite" conversion).  Finite x; returned as its bit pattern. */
+uint8_t or_e4m3_round(double x) {
+    uint8_t sgn = signbit(x) ? 0x80u : 0u;
+    double r = fabs(or_round_grid(x, 4, -6));
+    if (r == 0.0) return sgn;
+    if (r > 448.0) r = 448.0;
+    int e;
+    frexp(r, &e);
+    if (e - 1 < -6) return sgn | (uint8_t)ldexp(r, 9);      /* subnormal: r / 2^-9 */
+    return sgn | (uint8_t)((e - 1 + 7) << 3) | (uint8_t)(ldexp(r, -(e - 1)) * 8.0 - 8.0);
+}
+
 /* ------------------------------------------------------------ materialise */
 
 /*
@@ -120,6 +181,36 @@ void or_materialize(const int8_t* q, const float* scale, int64_t K, int64_t N, i
                 if (whi) whi[i] = w == 0 ? 0x0000u : or_bf16_round(shi * w);
                 if (wlo) wlo[i] = w == 0 ? 0x0000u : or_bf16_round(slo * w);
             }
+        }
+    }
+}
+
+/*
+ * The dX operands of the fp16 + e4m3 split (this library's encoding; the pages
+ * form W_eff = scale[c]*T in fp32).  Per column, scale[c] = a_c * 2^e_c with
+ * e_c = floor(log2|scale[c]|) and a_c in +-[1, 2) (a_c = 0, e_c = 0 for a zero
+ * scale):
+ *   wh16 [K][N] binary16 of h_c * T,           h_c = f16(a_c)
+ *   wl8  [K][N] e4m3 of l_c * T,               l_c = e4m3(2^7 * (a_c - h_c))
+ * so that h_c + 2^-7 * l_c = a_c within 2^-15 |a_c|.  A zero weight is +0 in both
+ * planes; a negative one flips the sign bit (so l_c = +0 with T = -1 gives -0).
+ */
+void or_split8_planes(const int8_t* q, const float* scale, int64_t K, int64_t N, int theta, int clamp,
+                      uint16_t* wh16, uint8_t* wl8) {
+    for (int64_t c = 0; c < N; ++c) {
+        double s = (double)scale[c], a = 0.0;
+        if (s != 0.0) {
+            int e;
+            frexp(fabs(s), &e);
+            a = ldexp(s, -(e - 1));                 /* exact: a power-of-two rescale */
+        }
+        uint16_t h = or_f16_round(a);
+        uint8_t l = or_e4m3_round(ldexp(a - or_f16_value(h), 7));   /* a - h is exact in fp64 */
+        for (int64_t r = 0; r < K; ++r) {
+            int64_t i = r * N + c;
+            int w = or_ternary(or_clamp(q[i], clamp), theta);
+            if (wh16) wh16[i] = w == 0 ? 0x0000u : (uint16_t)(w < 0 ? h ^ 0x8000u : h);
+            if (wl8) wl8[i] = w == 0 ? 0x00u : (uint8_t)(w < 0 ? l ^ 0x80u : l);
         }
     }
 }

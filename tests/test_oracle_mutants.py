@@ -15,6 +15,7 @@ import pytest
 import oracle
 import test_oracle_pins as P
 import test_oracle_sr4 as S
+import test_oracle_split8 as S8
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "tern_oracle.c")
 
@@ -82,6 +83,24 @@ MUTANTS = [
      [lambda: P.test_abs_sums_are_products_of_absolute_values((12, 40, 32), 31), P.test_sampled_entries_equal_full_outputs]),
     ("sampled sgrad abs sum drops |T|", "sa += G[K + r] * (double)abs(w);", "sa += G[K + r];", 0,
      [lambda: P.test_abs_sums_are_products_of_absolute_values((12, 40, 32), 31), P.test_sampled_entries_equal_full_outputs]),
+    # binary16 / E4M3 rounding and the fp16 + e4m3 split of the dX operands
+    ("grid rounding ties away from zero", "double r = ldexp(nearbyint(ldexp(fabs(x), -lsb)), lsb);",
+     "double r = ldexp(round(ldexp(fabs(x), -lsb)), lsb);", 0,
+     [S8.test_f16_round_matches_numpy, S8.test_f16_golden_values, S8.test_e4m3_golden_values]),
+    ("binary16 subnormals start one binade low", "if (e - 1 < -14) return sgn | (uint16_t)ldexp(r, 24);",
+     "if (e - 1 < -15) return sgn | (uint16_t)ldexp(r, 24);", 0,
+     [S8.test_f16_round_matches_numpy, S8.test_f16_golden_values]),
+    ("e4m3 exponent bias 8", "return sgn | (uint8_t)((e - 1 + 7) << 3)", "return sgn | (uint8_t)((e - 1 + 8) << 3)", 0,
+     [S8.test_e4m3_round_matches_torch_in_range, S8.test_e4m3_golden_values]),
+    ("e4m3 without saturation", "if (r > 448.0) r = 448.0;", "if (r > 480.0) r = 480.0;", 0,
+     [lambda: S8.test_e4m3_saturates(470.0)]),
+    ("split mantissa in [0.5, 1)", "a = ldexp(s, -(e - 1));", "a = ldexp(s, -e);", 0,
+     [S8.test_split_reconstructs_the_scale, S8.test_split_planes_match_library_conversions]),
+    ("split low part scaled by 2^6", "or_e4m3_round(ldexp(a - or_f16_value(h), 7))",
+     "or_e4m3_round(ldexp(a - or_f16_value(h), 6))", 0,
+     [S8.test_split_reconstructs_the_scale, S8.test_split_planes_match_library_conversions]),
+    ("split drops the sign of T", "(uint16_t)(w < 0 ? h ^ 0x8000u : h)", "(uint16_t)h", 0,
+     [S8.test_split_reconstructs_the_scale, S8.test_split_planes_match_library_conversions]),
     ("clip inverted", "if (max_norm > 0.0 && norm > max_norm) return max_norm / norm;",
      "if (max_norm > 0.0 && norm > max_norm) return norm / max_norm;", 0,
      [P.test_sumsq_and_norm, P.test_clipped_gradient_has_the_clip_norm]),
