@@ -37,13 +37,14 @@ TERN_ERR_DEVICE = -6
 TERN_ERR_SCRATCH_LIMIT = -7
 TERN_NOALLOC_SCRATCH_BYTES = 8 << 20
 
-TERN_TILE_PACKED, TERN_TILE_T, TERN_TILE_WHI, TERN_TILE_WLO = 0, 1, 2, 3
+TERN_TILE_PACKED, TERN_TILE_T, TERN_TILE_WHI, TERN_TILE_WLO, TERN_TILE_WHI16, TERN_TILE_WLO8 = 0, 1, 2, 3, 4, 5
 TERN_ADAM_MAX_TENSORS = 64
 TERN_BWD_ACCUMULATE = 1
+TERN_BWD_DX_SPLIT8 = 2
 
 # the C ABI's exported symbols (tests check the library exports every one)
 ABI_SYMBOLS = ("tern_tiles_bytes", "tern_materialize", "tern_materialize_grouped", "tern_linear_fwd", "tern_linear_bwd_workspace_min",
-               "tern_linear_bwd_workspace",
+               "tern_linear_bwd_workspace", "tern_linear_bwd_workspace_ex",
                "tern_linear_bwd", "tern_linear_bwd_ex", "tern_linear_bwd_noalloc", "tern_linear_fwd_grouped",
                "tern_linear_bwd_grouped_workspace", "tern_linear_bwd_grouped", "adamw_step", "tern_grad_sumsq_workspace",
                "tern_grad_sumsq", "adamw_step_multi", "tern_sr4_workspace", "tern_sr4_step", "tern_sr4_panel", "tern_strerror",
@@ -58,7 +59,8 @@ class TernError(RuntimeError):
 
 class _Tiles(ctypes.Structure):
     _fields_ = [("packed", ctypes.c_void_p), ("t_bf16", ctypes.c_void_p),
-                ("whi_bf16", ctypes.c_void_p), ("wlo_bf16", ctypes.c_void_p)]
+                ("whi_bf16", ctypes.c_void_p), ("wlo_bf16", ctypes.c_void_p),
+                ("whi_f16", ctypes.c_void_p), ("wlo_e4m3", ctypes.c_void_p)]
 
 
 class _MatLayer(ctypes.Structure):
@@ -87,6 +89,7 @@ def _load():
         "tern_linear_fwd": ([vp, tp, vp, vp, i64, i64, i64, vp], ci),
         "tern_linear_bwd_workspace_min": ([i64, i64, i64], sz),
         "tern_linear_bwd_workspace": ([i64, i64, i64], sz),
+        "tern_linear_bwd_workspace_ex": ([i64, i64, i64, ctypes.c_uint], sz),
         "tern_linear_bwd": ([vp, vp, tp, vp, vp, vp, vp, vp, sz, i64, i64, i64, vp], ci),
         "tern_linear_bwd_ex": ([vp, vp, tp, vp, vp, vp, vp, vp, sz, i64, i64, i64, ctypes.c_uint, vp], ci),
         "tern_linear_bwd_noalloc": ([vp, vp, tp, vp, vp, vp, vp, i64, i64, i64, vp], ci),
@@ -151,22 +154,26 @@ def _ptr(t, dtype, shape=None, name="tensor"):
 class Tiles:
     """Caller-owned weight encodings of one K x N ternary matrix (see tern.h, tern_tiles).
 
-    packed int32 [K, N/16] (2-bit codes), t/whi/wlo bfloat16 [K, N].  Any member may be None.
+    packed int32 [K, N/16] (2-bit codes), t/whi/wlo bfloat16 [K, N]; the fp16 + e4m3 dX split
+    whi_f16 float16 [K, N] and wlo_e4m3 uint8 [K, N] (e4m3 bit patterns).  Any member may be None.
     """
 
-    def __init__(self, K, N, packed=None, t_bf16=None, whi_bf16=None, wlo_bf16=None):
+    def __init__(self, K, N, packed=None, t_bf16=None, whi_bf16=None, wlo_bf16=None, whi_f16=None, wlo_e4m3=None):
         self.K, self.N = int(K), int(N)
         self.packed, self.t_bf16, self.whi_bf16, self.wlo_bf16 = packed, t_bf16, whi_bf16, wlo_bf16
+        self.whi_f16, self.wlo_e4m3 = whi_f16, wlo_e4m3
 
     @classmethod
-    def empty(cls, K, N, device="cuda", packed=True, t=True, hi_lo=True):
+    def empty(cls, K, N, device="cuda", packed=True, t=True, hi_lo=True, split8=False):
         K, N = int(K), int(N)
         mk = lambda shape, dt: torch.empty(shape, dtype=dt, device=device)  # noqa: E731
         return cls(K, N,
                    mk((K, N // 16), torch.int32) if packed else None,
                    mk((K, N), torch.bfloat16) if t else None,
                    mk((K, N), torch.bfloat16) if hi_lo else None,
-                   mk((K, N), torch.bfloat16) if hi_lo else None)
+                   mk((K, N), torch.bfloat16) if hi_lo else None,
+                   mk((K, N), torch.float16) if split8 else None,
+                   mk((K, N), torch.uint8) if split8 else None)
 
     def _c(self) -> _Tiles:
         K, N = self.K, self.N
@@ -174,7 +181,9 @@ class Tiles:
             _ptr(self.packed, torch.int32, (K, N // 16), "tiles.packed"),
             _ptr(self.t_bf16, torch.bfloat16, (K, N), "tiles.t_bf16"),
             _ptr(self.whi_bf16, torch.bfloat16, (K, N), "tiles.whi_bf16"),
-            _ptr(self.wlo_bf16, torch.bfloat16, (K, N), "tiles.wlo_bf16"))
+            _ptr(self.wlo_bf16, torch.bfloat16, (K, N), "tiles.wlo_bf16"),
+            _ptr(self.whi_f16, torch.float16, (K, N), "tiles.whi_f16"),
+            _ptr(self.wlo_e4m3, torch.uint8, (K, N), "tiles.wlo_e4m3"))
 
 
 def tern_tiles_bytes(K, N, which) -> int:
@@ -253,8 +262,14 @@ def tern_linear_bwd_workspace_min(M, K, N) -> int:
     return int(lib.tern_linear_bwd_workspace_min(int(M), int(K), int(N)))
 
 
-def tern_linear_bwd(X, dY, tiles: Tiles, scale, dX, gq, sgrad, workspace, stream=None, accumulate=False):
-    """accumulate=True calls tern_linear_bwd_ex with TERN_BWD_ACCUMULATE (gq, sgrad +=)."""
+def tern_linear_bwd_workspace_ex(M, K, N, flags=0) -> int:
+    return int(lib.tern_linear_bwd_workspace_ex(int(M), int(K), int(N), int(flags)))
+
+
+def tern_linear_bwd(X, dY, tiles: Tiles, scale, dX, gq, sgrad, workspace, stream=None, accumulate=False,
+                    split8=False):
+    """accumulate=True adds TERN_BWD_ACCUMULATE (gq, sgrad +=), split8=True TERN_BWD_DX_SPLIT8 (dX from
+    the fp16 + e4m3 split); either calls tern_linear_bwd_ex."""
     M, K = X.shape
     N = tiles.N
     ct = tiles._c()
@@ -264,8 +279,9 @@ def tern_linear_bwd(X, dY, tiles: Tiles, scale, dX, gq, sgrad, workspace, stream
             _ptr(scale, torch.float32, (N,), "scale"), _ptr(dX, torch.float32, (M, K), "dX"),
             _ptr(gq, torch.float32, (K, N), "gq"), _ptr(sgrad, torch.float32, (N,), "sgrad"), ws_ptr, ws_bytes,
             M, K, N)
-    if accumulate:
-        _check(lib.tern_linear_bwd_ex(*args, TERN_BWD_ACCUMULATE, _stream(stream)), "tern_linear_bwd_ex")
+    flags = (TERN_BWD_ACCUMULATE if accumulate else 0) | (TERN_BWD_DX_SPLIT8 if split8 else 0)
+    if flags:
+        _check(lib.tern_linear_bwd_ex(*args, flags, _stream(stream)), "tern_linear_bwd_ex")
     else:
         _check(lib.tern_linear_bwd(*args, _stream(stream)), "tern_linear_bwd")
 

@@ -24,6 +24,15 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 // Host side of the device status word (defined in gemm.cu).
 int gemm_status_read(int clear);
 
+// The fp16 + e4m3 split of the dX operands (split8.cu): the weight planes h_c*T and
+// l_c*T from q and scale, and the per-call split of dY into the workspace (binary16 and
+// e4m3 copies and the per-row exponents, split8_dy_bytes in all).
+int split8_planes(const int8_t* q, const float* scale, int64_t K, int64_t N, int theta, uint16_t* wh16,
+                  uint8_t* wl8, int num_sms, cudaStream_t s);
+int64_t split8_dy_bytes(int64_t M, int64_t N);
+int split8_dy(const uint16_t* dY, const float* scale, int64_t M, int64_t N, void* ws, uint16_t** dy16, uint8_t** dy8,
+              int** row_exp, cudaStream_t s);
+
 }  // namespace tern
 
 #ifdef __CUDACC__
@@ -157,6 +166,16 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// The same with 8-bit floating-point operands (kind::f8f6f4; the formats come from idesc).
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 // Arrive once on `bar` when every tcgen05 op issued so far by this thread completes.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -226,6 +245,15 @@ __device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, u
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_f8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }

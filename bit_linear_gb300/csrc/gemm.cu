@@ -89,6 +89,7 @@ struct GemmArgs {
     float* partial_g;
     uint16_t* out_bf16;       // [Mg][Ng] bf16 (RNE) copy of out, or its only output (EPI_FWD, EPI_DX)
     const uint32_t* bpacked;  // forward from 2-bit codes: T as [Kg][Ng/16] words (the B operand)
+    const int* row_exp;       // dX from the fp16 + e4m3 split: dX row m is 2^row_exp[m] times the accumulator
 };
 
 // Up to G independent problems in one launch: their work units are concatenated
@@ -108,8 +109,21 @@ struct GemmGroup {
 constexpr int kGroup = 8;
 static_assert(sizeof(GemmGroup<kGroup>) <= 4096, "kernel parameter block over 4 KB");
 
+// The dX GEMM from the fp16 + e4m3 split reads four operands: A = dY16 (mA), B = h*T
+// (mB0), A8 = dY8 (mA1), B8 = l*T (mB1).
 template <int G>
-__device__ __forceinline__ int group_find(const GemmGroup<G>& g, int unit) {
+struct GemmGroup4 {
+    CUtensorMap mA[G];
+    CUtensorMap mB0[G];
+    CUtensorMap mB1[G];
+    CUtensorMap mA1[G];
+    GemmArgs args[G];
+    int unit_begin[G + 1];
+    int count;
+};
+
+template <class GRP>
+__device__ __forceinline__ int group_find(const GRP& g, int unit) {
     int p = 0;
     while (p + 1 < g.count && unit >= g.unit_begin[p + 1]) ++p;
     return p;
@@ -121,10 +135,13 @@ __device__ __forceinline__ int group_find(const GemmGroup<G>& g, int unit) {
 // PK: the B operand (the forward's T) is read as 2-bit codes and expanded to bf16 in
 // shared memory by converter warps (warps 6-13: two teams of four that take alternate
 // k-blocks) instead of being copied by TMA.
-template <int CG_, int BN_, int BK_, bool A_MN_, bool B_MN_, int NB_, int EPI_, int STAGES_, bool PK_ = false>
+// F8: the dX GEMM from the fp16 + e4m3 split: per k-block a binary16 A and B (rows of
+// BK*2 bytes, SW128) and an e4m3 A and B (rows of BK bytes, SW64), in that order.
+template <int CG_, int BN_, int BK_, bool A_MN_, bool B_MN_, int NB_, int EPI_, int STAGES_, bool PK_ = false,
+          bool F8_ = false>
 struct Cfg {
     static constexpr int CG = CG_, BN = BN_, BK = BK_, NB = NB_, EPI = EPI_, STAGES = STAGES_;
-    static constexpr bool A_MN = A_MN_, B_MN = B_MN_, PK = PK_;
+    static constexpr bool A_MN = A_MN_, B_MN = B_MN_, PK = PK_, F8 = F8_;
     // warps: producer, MMA, EPI_WARPS epilogue warps (two per TMEM lane quarter, each taking
     // half the columns; four when PK), and for PK two teams of four converter warps
     static constexpr int EPI_WARPS = PK ? 4 : 8;
@@ -133,7 +150,9 @@ struct Cfg {
     static constexpr int B_ROWS = BN / CG;
     static constexpr int A_BYTES = kBM * BK * 2;
     static constexpr int B_BYTES = B_ROWS * BK * 2;
-    static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES;   // per CTA
+    static constexpr int A8_BYTES = F8 ? kBM * BK : 0;
+    static constexpr int B8_BYTES = F8 ? B_ROWS * BK : 0;
+    static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES + A8_BYTES + B8_BYTES;   // per CTA
     static constexpr int TX_BYTES = CG * (PK ? A_BYTES : STAGE_BYTES);   // TMA bytes on the leader's barrier
     static constexpr int P_BYTES = PK ? BK * (B_ROWS / 16) * 4 : 0;     // 2-bit codes of a stage's B (PK)
     static constexpr int TMEM_COLS = 2 * BN;
@@ -144,6 +163,7 @@ struct Cfg {
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of two");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
     static_assert(!PK || (EPI == EPI_FWD && B_MN && NB == 1 && BK == 64), "packed operand: the forward's T");
+    static_assert(!F8 || (EPI == EPI_DX && !A_MN && !B_MN && NB == 1 && BK == 64 && !PK), "fp16 + e4m3 split: dX");
 };
 
 // One CTA per 128 x 256 tile (small problems).
@@ -157,12 +177,16 @@ using Dw2 = Cfg<2, 256, 64, true, true, 1, EPI_DW, 7>;
 // The forward with T read as 2-bit codes.
 using FwdP1 = Cfg<1, 256, 64, false, true, 1, EPI_FWD, 4, true>;
 using FwdP2 = Cfg<2, 256, 64, false, true, 1, EPI_FWD, 6, true>;
+// dX from the fp16 + e4m3 split.
+using Dx8_1 = Cfg<1, 256, 64, false, false, 1, EPI_DX, 3, false, true>;
+using Dx8_2 = Cfg<2, 256, 64, false, false, 1, EPI_DX, 4, false, true>;
 
-// tcgen05 instruction descriptor, kind::f16: bf16 A/B, fp32 D, M x N, operand majors.
-__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool a_mn, bool b_mn) {
+// tcgen05 instruction descriptor: fp32 D, M x N, operand majors and the A/B format code
+// (kind::f16: 0 = f16, 1 = bf16; kind::f8f6f4: 0 = e4m3).
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool a_mn, bool b_mn, uint32_t fmt = 1u) {
     return (1u << 4)                       // D format: f32
-           | (1u << 7)                     // A format: bf16
-           | (1u << 10)                    // B format: bf16
+           | (fmt << 7)                    // A format
+           | (fmt << 10)                   // B format
            | (static_cast<uint32_t>(a_mn) << 15)
            | (static_cast<uint32_t>(b_mn) << 16)
            | (static_cast<uint32_t>(N >> 3) << 17)
@@ -329,7 +353,7 @@ __device__ __forceinline__ void load_tile_scales(const float* scale, int col0, i
 template <class C>
 __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const uint32_t (&r)[32],
                                                const float (&sc)[8], int j, int row, int wrow, int c0, int tile128,
-                                               int quad, int lane) {
+                                               int quad, int lane, int rexp = 0) {
     const bool row_ok = row < a.Mg;
     const bool hi_ok = c0 + 16 < a.Ng;   // N is a multiple of 16: the chunk's second half may lie past it
     float v[32];
@@ -343,6 +367,10 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const uint32_t
     } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+    }
+    if constexpr (C::F8) {   // the dY row's exponent, taken out by the split
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = ldexpf(v[i], rexp);
     }
     if (C::EPI == EPI_FWD || (C::EPI == EPI_DW && a.out != nullptr)) {
         // column c0 + i of the chunk is register i % 8 of lane 4j + i / 8
@@ -393,8 +421,8 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const uint32_t
     }
 }
 
-template <class C, int G>
-__device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
+template <class C, class GRP>
+__device__ __forceinline__ void gemm_body(const GRP& grp) {
     constexpr int CG = C::CG;
     constexpr int SITE = (C::EPI + 1) * 100 + CG * 10;
     const int total_units = grp.unit_begin[grp.count];
@@ -467,7 +495,8 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
         for (int p = 0; p < grp.count; ++p) {
             ptx::tma_prefetch_desc(&grp.mA[p]);
             ptx::tma_prefetch_desc(&grp.mB0[p]);
-            if (C::NB == 2) ptx::tma_prefetch_desc(&grp.mB1[p]);
+            if (C::NB == 2 || C::F8) ptx::tma_prefetch_desc(&grp.mB1[p]);
+            if constexpr (C::F8) ptx::tma_prefetch_desc(&grp.mA1[p]);
         }
         int stage = 0;
         uint32_t phase = 0;
@@ -522,6 +551,11 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
                         load(sB, tmB, k0, brow);
                     }
                 }
+                if constexpr (C::F8) {   // the e4m3 halves: A8 rows of BK bytes, then B8
+                    const uint32_t sA8 = sB0 + C::B_BYTES;
+                    load(sA8, &grp.mA1[p], k0, arow);
+                    load(sA8 + C::A8_BYTES, tmB1, k0, brow);
+                }
                 issued |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                 if (++stage == C::STAGES) {
@@ -541,10 +575,16 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
         }
     } else if (warp == 1 && lane == 0 && rank == 0) {
         // ------------------------------------------------------------ MMA issuer (leader only)
-        constexpr uint32_t IDESC = make_idesc(C::TILE_M, C::BN, C::A_MN, C::B_MN);
+        // bf16 operands, or binary16 (F8's first pass: kind::f16 with format code 0)
+        constexpr uint32_t IDESC = make_idesc(C::TILE_M, C::BN, C::A_MN, C::B_MN, C::F8 ? 0u : 1u);
+        constexpr uint32_t IDESC8 = make_idesc(C::TILE_M, C::BN, false, false, 0u);   // kind::f8f6f4, e4m3 x e4m3
         auto mma = [&](uint32_t d, uint64_t da, uint64_t db, uint32_t acc) {
             if constexpr (CG == 2) ptx::mma_bf16_pair(d, da, db, IDESC, acc);
             else ptx::mma_bf16(d, da, db, IDESC, acc);
+        };
+        auto mma8 = [&](uint32_t d, uint64_t da, uint64_t db) {
+            if constexpr (CG == 2) ptx::mma_f8_pair(d, da, db, IDESC8, 1u);
+            else ptx::mma_f8(d, da, db, IDESC8, 1u);
         };
         auto commit_all = [&](uint32_t bar) {   // arrive on `bar` in every CTA of the group
             if constexpr (CG == 2) ptx::mma_commit_pair_mc(bar, 0x3);
@@ -581,6 +621,14 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
                     const uint64_t da = op_desc<C::A_MN, C::BK>(sA, kk);
                     mma(d_tmem, da, op_desc<C::B_MN, C::BK>(sB0, kk), (kb != kb0 || kk != 0) ? 1u : 0u);
                     if constexpr (C::NB == 2) mma(d_tmem, da, op_desc<C::B_MN, C::BK>(sB0 + C::B_BYTES, kk), 1u);
+                }
+                if constexpr (C::F8) {
+                    // the e4m3 pass: rows of 64 bytes (SW64), 32-deep k-slices 32 bytes apart,
+                    // into the same accumulator
+                    const uint32_t sA8 = sB0 + C::B_BYTES, sB8 = sA8 + C::A8_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < C::BK / 32; ++kk)
+                        mma8(d_tmem, make_sdesc(sA8 + kk * 32u, 16u, 512u, SW64), make_sdesc(sB8 + kk * 32u, 16u, 512u, SW64));
                 }
                 commit_all(EMPTY0 + 8u * stage);   // frees the stage once these MMAs are done
                 if (++stage == C::STAGES) {
@@ -740,6 +788,7 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
             } else if (row0 < a.Mg) {   // a pair's second half may lie wholly past the last row
                 const int tile128 = mt * CG + static_cast<int>(rank);
                 const int wrow = row0 + quad * 32;
+                const int rexp = C::F8 && wrow + lane < a.Mg ? __ldg(a.row_exp + wrow + lane) : 0;
 #pragma unroll 1
                 for (int j = j0; j < j0 + JPW; ++j) {
                     const int c0 = nt * C::BN + j * 32;
@@ -747,7 +796,7 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
                     uint32_t r[32];
                     ptx::tmem_ld_32x32b_x32(trow + j * 32, r);
                     ptx::tmem_wait_ld();
-                    epilogue_chunk<C>(a, r, sc_cur, j, wrow + lane, wrow, c0, tile128, quad, lane);
+                    epilogue_chunk<C>(a, r, sc_cur, j, wrow + lane, wrow, c0, tile128, quad, lane, rexp);
                 }
             }
 #pragma unroll
@@ -793,23 +842,30 @@ __device__ __forceinline__ void gemm_body(const GemmGroup<G>& grp) {
 // layer); the tensor maps live in the kernel's parameter space.
 template <int CG, int G>
 __global__ void __launch_bounds__(320, 1) tern_fwd_gemm(const __grid_constant__ GemmGroup<G> grp) {
-    gemm_body<std::conditional_t<CG == 2, Fwd2, Fwd1>, G>(grp);
+    gemm_body<std::conditional_t<CG == 2, Fwd2, Fwd1>>(grp);
 }
 
 // The forward with T read as 2-bit codes (expanded in shared memory by converter warps).
 template <int CG, int G>
 __global__ void __launch_bounds__(448, 1) tern_fwdp_gemm(const __grid_constant__ GemmGroup<G> grp) {
-    gemm_body<std::conditional_t<CG == 2, FwdP2, FwdP1>, G>(grp);
+    gemm_body<std::conditional_t<CG == 2, FwdP2, FwdP1>>(grp);
 }
 
 template <int CG, int G>
 __global__ void __launch_bounds__(320, 1) tern_dx_gemm(const __grid_constant__ GemmGroup<G> grp) {
-    gemm_body<std::conditional_t<CG == 2, Dx2, Dx1>, G>(grp);
+    gemm_body<std::conditional_t<CG == 2, Dx2, Dx1>>(grp);
 }
 
 template <int CG, int G>
 __global__ void __launch_bounds__(320, 1) tern_dw_gemm(const __grid_constant__ GemmGroup<G> grp) {
-    gemm_body<std::conditional_t<CG == 2, Dw2, Dw1>, G>(grp);
+    gemm_body<std::conditional_t<CG == 2, Dw2, Dw1>>(grp);
+}
+
+// dX from the fp16 + e4m3 split (split8.cu): a binary16 pass and an e4m3 pass into one
+// accumulator, the dY row exponent applied in the epilogue.
+template <int CG, int G>
+__global__ void __launch_bounds__(320, 1) tern_dx8_gemm(const __grid_constant__ GemmGroup4<G> grp) {
+    gemm_body<std::conditional_t<CG == 2, Dx8_2, Dx8_1>>(grp);
 }
 
 // Self-test of the bounded wait: one warp waits on an mbarrier that nothing
@@ -1027,7 +1083,9 @@ int encode_2d(CUtensorMap* m, const MapKey& k) {
     }
     EncodeTiledFn enc = encode_fn();
     if (!enc) return TERN_ERR_CUDA;
-    const int esize = k.dtype == CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 ? 2 : 4;
+    const int esize = (k.dtype == CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 || k.dtype == CU_TENSOR_MAP_DATA_TYPE_FLOAT16) ? 2
+                      : k.dtype == CU_TENSOR_MAP_DATA_TYPE_UINT8                                              ? 1
+                                                                                                              : 4;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(k.inner), static_cast<cuuint64_t>(k.outer)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(k.inner) * esize};
     cuuint32_t box[2] = {static_cast<cuuint32_t>(k.box_inner), static_cast<cuuint32_t>(k.box_outer)};
@@ -1117,8 +1175,8 @@ int persistent_units(K kernel, int num_sms, int* units) {
 // SMs), at most one per work unit.  No programmatic stream serialization: the grid
 // starts once every earlier kernel on the stream has completed, so its TMEM
 // allocation and cluster barrier (waits without a bound) never wait on another grid.
-template <class C, class K, int G>
-int launch(K kernel, const GemmGroup<G>& grp, int num_sms, cudaStream_t s) {
+template <class C, class K, class GRP>
+int launch(K kernel, const GRP& grp, int num_sms, cudaStream_t s) {
     int units = 0;
     if (int st = persistent_units<C>(kernel, num_sms, &units)) return st;
     const int total = grp.unit_begin[grp.count];
@@ -1170,8 +1228,8 @@ int group_set(GemmGroup<G>& g, int p, const void* A, int64_t a_inner, int64_t a_
 }
 
 // Unit ranges of the first `count` problems, from their num_units.
-template <int G>
-void group_close(GemmGroup<G>& g, int count) {
+template <class GRP>
+void group_close(GRP& g, int count) {
     g.count = count;
     g.unit_begin[0] = 0;
     for (int p = 0; p < count; ++p) g.unit_begin[p + 1] = g.unit_begin[p] + g.args[p].num_units;
@@ -1197,6 +1255,28 @@ int run_dx(K kernel, const uint16_t* dY, const uint16_t* whi, const uint16_t* wl
     GemmArgs a = make_args<C>(M, K_, N);
     a.out = dX;
     if (int st = group_set<C>(g, 0, dY, N, M, whi, wlo, N, K_, a)) return st;
+    group_close(g, 1);
+    return launch<C>(kernel, g, num_sms, s);
+}
+
+// dX from the fp16 + e4m3 split: dY16 / dY8 [M][N] and the weight planes h*T / l*T [K][N].
+template <class C, class K>
+int run_dx8(K kernel, const uint16_t* dy16, const uint8_t* dy8, const int* row_exp, const uint16_t* wh16,
+            const uint8_t* wl8, float* dX, int64_t M, int64_t K_, int64_t N, int num_sms, cudaStream_t s) {
+    GemmGroup4<1> g;
+    GemmArgs a = make_args<C>(M, K_, N);
+    a.out = dX;
+    a.row_exp = row_exp;
+    auto map = [&](CUtensorMap* m, const void* ptr, int64_t outer, int rows, bool f16) {
+        return encode_2d(m, MapKey{ptr, N, outer, 64, rows,
+                                   static_cast<int>(f16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B),
+                                   static_cast<int>(f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8)});
+    };
+    if (int st = map(&g.mA[0], dy16, M, kBM, true)) return st;
+    if (int st = map(&g.mB0[0], wh16, K_, C::B_ROWS, true)) return st;
+    if (int st = map(&g.mA1[0], dy8, M, kBM, false)) return st;
+    if (int st = map(&g.mB1[0], wl8, K_, C::B_ROWS, false)) return st;
+    g.args[0] = a;
     group_close(g, 1);
     return launch<C>(kernel, g, num_sms, s);
 }
@@ -1338,13 +1418,22 @@ extern "C" size_t tern_linear_bwd_workspace(int64_t M, int64_t K, int64_t N) {
     return static_cast<size_t>(bwd_partials_bytes(K, N) + tail);
 }
 
+extern "C" size_t tern_linear_bwd_workspace_ex(int64_t M, int64_t K, int64_t N, unsigned flags) {
+    if (!dims_ok(M, K, N) || (flags & ~static_cast<unsigned>(TERN_BWD_ACCUMULATE | TERN_BWD_DX_SPLIT8))) return 0;
+    const size_t base = tern_linear_bwd_workspace(M, K, N);
+    if (!(flags & TERN_BWD_DX_SPLIT8)) return base;
+    return std::max(base, static_cast<size_t>(split8_dy_bytes(M, N)));
+}
+
 extern "C" int tern_linear_bwd_ex(const uint16_t* X, const uint16_t* dY, const tern_tiles* W, const float* scale,
                                   float* dX, float* gq, float* sgrad, void* workspace, size_t ws_bytes, int64_t M,
                                   int64_t K, int64_t N, unsigned flags, void* stream) {
-    if (flags & ~static_cast<unsigned>(TERN_BWD_ACCUMULATE)) return TERN_ERR_ARG;
+    if (flags & ~static_cast<unsigned>(TERN_BWD_ACCUMULATE | TERN_BWD_DX_SPLIT8)) return TERN_ERR_ARG;
     const int accumulate = (flags & TERN_BWD_ACCUMULATE) ? 1 : 0;
     if (!X || !dY || !W || !scale) return TERN_ERR_ARG;
-    if (dX && (!W->whi_bf16 || !W->wlo_bf16)) return TERN_ERR_ARG;
+    const bool split8 = dX != nullptr && (flags & TERN_BWD_DX_SPLIT8) != 0;
+    if (dX && !split8 && (!W->whi_bf16 || !W->wlo_bf16)) return TERN_ERR_ARG;
+    if (split8 && (!W->whi_f16 || !W->wlo_e4m3)) return TERN_ERR_ARG;
     if (sgrad && !W->packed) return TERN_ERR_ARG;
     if (!dX && !gq && !sgrad) return TERN_ERR_ARG;
     if (!dims_ok(M, K, N)) return TERN_ERR_ARG;
@@ -1352,14 +1441,30 @@ extern "C" int tern_linear_bwd_ex(const uint16_t* X, const uint16_t* dY, const t
     if (!aligned16(X) || !aligned16(dY) || !aligned16(scale)) return TERN_ERR_ALIGN;
     if (sgrad && (!aligned16(sgrad) || !aligned16(W->packed) || !aligned16(workspace))) return TERN_ERR_ALIGN;
     if (gq && !aligned16(gq)) return TERN_ERR_ALIGN;
-    if (dX && (!aligned16(dX) || !aligned16(W->whi_bf16) || !aligned16(W->wlo_bf16))) return TERN_ERR_ALIGN;
+    if (dX && !split8 && (!aligned16(dX) || !aligned16(W->whi_bf16) || !aligned16(W->wlo_bf16))) return TERN_ERR_ALIGN;
+    if (split8 && (!aligned16(dX) || !aligned16(W->whi_f16) || !aligned16(W->wlo_e4m3) ||
+                   (workspace && !aligned16(workspace))))
+        return TERN_ERR_ALIGN;
     if (sgrad && (!workspace || ws_bytes < tern_linear_bwd_workspace_min(M, K, N))) return TERN_ERR_WORKSPACE;
+    if (split8 && (!workspace || static_cast<int64_t>(ws_bytes) < split8_dy_bytes(M, N))) return TERN_ERR_WORKSPACE;
     int num_sms = 0;
     if (int st = check_device(&num_sms)) return st;
     if (int st = gemm_setup(num_sms)) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    if (dX) {
+    if (split8) {
+        // dY's split into the workspace, read only by this dX GEMM (the G GEMM below
+        // reuses the bytes after it on the same stream)
+        uint16_t* dy16 = nullptr;
+        uint8_t* dy8 = nullptr;
+        int* rexp = nullptr;
+        if (int st = split8_dy(dY, scale, M, N, workspace, &dy16, &dy8, &rexp, s)) return st;
+        const int st = use_pair(M) ? run_dx8<Dx8_2>(tern_dx8_gemm<2, 1>, dy16, dy8, rexp, W->whi_f16, W->wlo_e4m3, dX,
+                                                    M, K, N, num_sms, s)
+                                   : run_dx8<Dx8_1>(tern_dx8_gemm<1, 1>, dy16, dy8, rexp, W->whi_f16, W->wlo_e4m3, dX,
+                                                    M, K, N, num_sms, s);
+        if (st) return st;
+    } else if (dX) {
         const int st = use_pair(M)
                            ? run_dx<Dx2>(tern_dx_gemm<2, 1>, dY, W->whi_bf16, W->wlo_bf16, dX, M, K, N, num_sms, s)
                            : run_dx<Dx1>(tern_dx_gemm<1, 1>, dY, W->whi_bf16, W->wlo_bf16, dX, M, K, N, num_sms, s);
@@ -1753,6 +1858,8 @@ int gemm_setup(int num_sms) {
         gemm(persistent_units<FwdP2>(tern_fwdp_gemm<2, 1>, num_sms, &u));
         gemm(persistent_units<FwdP1>(tern_fwdp_gemm<1, kGroup>, num_sms, &u));
         gemm(persistent_units<FwdP2>(tern_fwdp_gemm<2, kGroup>, num_sms, &u));
+        gemm(persistent_units<Dx8_1>(tern_dx8_gemm<1, 1>, num_sms, &u));
+        gemm(persistent_units<Dx8_2>(tern_dx8_gemm<2, 1>, num_sms, &u));
         cudaFuncAttributes fa;
         auto load = [&](cudaError_t e) {
             if (st == TERN_OK && e != cudaSuccess) st = TERN_ERR_CUDA;

@@ -362,9 +362,10 @@ int mat_args(const int8_t* q, int8_t* q_clamped, const float* scale, int64_t K, 
     if (!q || !out) return TERN_ERR_ARG;
     if (K < 1 || N < 16 || K >= (1ll << 31) || N >= (1ll << 31) || K * N >= (1ll << 40)) return TERN_ERR_ARG;
     if (theta < 1 || q_clamp < theta || q_clamp > 127) return TERN_ERR_ARG;
-    if ((out->whi_bf16 || out->wlo_bf16) && !scale) return TERN_ERR_ARG;
+    if ((out->whi_bf16 || out->wlo_bf16 || out->whi_f16 || out->wlo_e4m3) && !scale) return TERN_ERR_ARG;
     if (N % 16) return TERN_ERR_ALIGN;
-    const void* ptrs[] = {q, q_clamped, scale, out->packed, out->t_bf16, out->whi_bf16, out->wlo_bf16};
+    const void* ptrs[] = {q,           q_clamped,    scale,         out->packed, out->t_bf16,
+                          out->whi_bf16, out->wlo_bf16, out->whi_f16, out->wlo_e4m3};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return TERN_ERR_ALIGN;
     a->q = q;
@@ -414,6 +415,12 @@ extern "C" int tern_materialize_grouped(const tern_mat_layer* layers, int count,
             }
         }
     }
+    for (int i = 0; i < count; ++i) {   // the fp16 + e4m3 dX planes, weight by weight
+        const tern_mat_layer& l = layers[i];
+        if (l.out->whi_f16 || l.out->wlo_e4m3)
+            if (int st = split8_planes(l.q, l.scale, l.K, l.N, theta, l.out->whi_f16, l.out->wlo_e4m3, num_sms, s))
+                return st;
+    }
     return TERN_OK;
 }
 
@@ -422,9 +429,11 @@ extern "C" int tern_materialize(const int8_t* q, int8_t* q_clamped, const float*
     if (!q || !out) return TERN_ERR_ARG;
     if (K < 1 || N < 16 || K >= (1ll << 31) || N >= (1ll << 31) || K * N >= (1ll << 40)) return TERN_ERR_ARG;
     if (theta < 1 || q_clamp < theta || q_clamp > 127) return TERN_ERR_ARG;
-    if ((out->whi_bf16 || out->wlo_bf16) && !scale) return TERN_ERR_ARG;
+    const bool s8 = out->whi_f16 != nullptr || out->wlo_e4m3 != nullptr;
+    if ((out->whi_bf16 || out->wlo_bf16 || s8) && !scale) return TERN_ERR_ARG;
     if (N % 16) return TERN_ERR_ALIGN;
-    const void* ptrs[] = {q, q_clamped, scale, out->packed, out->t_bf16, out->whi_bf16, out->wlo_bf16};
+    const void* ptrs[] = {q,           q_clamped,    scale,         out->packed, out->t_bf16,
+                          out->whi_bf16, out->wlo_bf16, out->whi_f16, out->wlo_e4m3};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return TERN_ERR_ALIGN;
     int num_sms = 0;
@@ -448,8 +457,14 @@ extern "C" int tern_materialize(const int8_t* q, int8_t* q_clamped, const float*
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool qc = q_clamped != nullptr, pk = out->packed != nullptr, tt = out->t_bf16 != nullptr;
     const bool hl = out->whi_bf16 != nullptr || out->wlo_bf16 != nullptr;
-    if (!qc && !pk && !tt && !hl) return TERN_OK;   // nothing requested
-    return qc ? dispatch_pk<true>(a, pk, tt, hl, num_sms, s) : dispatch_pk<false>(a, pk, tt, hl, num_sms, s);
+    if (qc || pk || tt || hl) {
+        if (int st = qc ? dispatch_pk<true>(a, pk, tt, hl, num_sms, s) : dispatch_pk<false>(a, pk, tt, hl, num_sms, s))
+            return st;
+    }
+    // the fp16 + e4m3 dX planes: a pass of their own (ternary(clamp(q)) = ternary(q), so an
+    // in-place clamp before it changes nothing)
+    if (s8) return split8_planes(q, scale, K, N, theta, out->whi_f16, out->wlo_e4m3, num_sms, s);
+    return TERN_OK;
 }
 
 extern "C" size_t tern_tiles_bytes(int64_t K, int64_t N, int which) {
@@ -458,7 +473,9 @@ extern "C" size_t tern_tiles_bytes(int64_t K, int64_t N, int which) {
     case TERN_TILE_PACKED: return static_cast<size_t>(K * (N / 16)) * 4;
     case TERN_TILE_T:
     case TERN_TILE_WHI:
-    case TERN_TILE_WLO: return static_cast<size_t>(K * N) * 2;
+    case TERN_TILE_WLO:
+    case TERN_TILE_WHI16: return static_cast<size_t>(K * N) * 2;
+    case TERN_TILE_WLO8: return static_cast<size_t>(K * N);
     default: return 0;
     }
 }

@@ -66,12 +66,22 @@ typedef struct tern_tiles {
     uint16_t* t_bf16;   /* [K][N] bf16 of ternary(q): 0x0000, 0x3F80, 0xBF80 (forward operand) */
     uint16_t* whi_bf16; /* [K][N] bf16 of s_hi[c]*ternary(q), s_hi = bf16_rne(scale[c]) */
     uint16_t* wlo_bf16; /* [K][N] bf16 of s_lo[c]*ternary(q), s_lo = bf16_rne(scale[c]-s_hi) */
+    /* The fp16 + e4m3 split of the dX operand (read by tern_linear_bwd_ex with
+     * TERN_BWD_DX_SPLIT8).  scale[c] = a_c * 2^e_c, e_c = floor(log2|scale[c]|), a_c in
+     * +-[1,2) (a_c = 0 for a zero scale); h_c = binary16_rne(a_c), l_c =
+     * e4m3_rne_satfinite(2^7 * (a_c - h_c)) (OCP E4M3: bias 7, largest 448), so that
+     * h_c + 2^-7 l_c = a_c within 2^-15 |a_c|.  A zero weight is +0 in both planes; a
+     * negative one flips the sign bit. */
+    uint16_t* whi_f16;  /* [K][N] binary16 of h_c*ternary(q) */
+    uint8_t* wlo_e4m3;  /* [K][N] e4m3 of l_c*ternary(q) */
 } tern_tiles;
 
 #define TERN_TILE_PACKED 0
 #define TERN_TILE_T 1
 #define TERN_TILE_WHI 2
 #define TERN_TILE_WLO 3
+#define TERN_TILE_WHI16 4
+#define TERN_TILE_WLO8 5
 
 /* Bytes of one tern_tiles buffer (`which` = TERN_TILE_*) for a K x N weight; 0 on bad args. */
 size_t tern_tiles_bytes(int64_t K, int64_t N, int which);
@@ -82,7 +92,7 @@ size_t tern_tiles_bytes(int64_t K, int64_t N, int which);
  *   q         [K][N] int8 accumulator (device, read)
  *   q_clamped [K][N] int8, min(max(q,-q_clamp),q_clamp) (device, written; NULL to skip;
  *             may equal q for an in-place clamp)
- *   scale     [N] fp32 (device, read; may be NULL when out->whi_bf16 and out->wlo_bf16 are NULL)
+ *   scale     [N] fp32 (device, read; may be NULL when out has no hi/lo or fp16/e4m3 planes)
  *   out       tiles to write (host struct of device pointers; NULL members skipped)
  *   theta >= 1, q_clamp >= theta (clamping then keeps every ternary value).
  * K >= 1, N >= 16 with N % 16 == 0; every pointer 16-byte aligned.  Bit-exact.
@@ -164,8 +174,24 @@ int tern_linear_bwd(const uint16_t* X, const uint16_t* dY, const tern_tiles* W, 
  * "train_gpu.cu": the B > 1 path accumulates every gradient over micro-batches
  * before the optimizer step and scales by 1/B; here the 1/B goes into
  * tern_sr4_step's inv_bs and AdamW's gmul).  Unknown flag bits: TERN_ERR_ARG.
+ *
+ * TERN_BWD_DX_SPLIT8 computes dX from the fp16 + e4m3 split instead of the bf16
+ * hi/lo split: it reads W->whi_f16 and W->wlo_e4m3 (not whi_bf16 / wlo_bf16) and
+ * first splits dY, per row m, into binary16 dY[m][c]*2^(e_c-e_m) and e4m3
+ * dY[m][c]*2^(e_c-e_m-7) copies, e_m chosen so that the row's largest
+ * |dY[m][c]|*2^e_c lands in [2^14, 2^15); the GEMM is then one binary16 pass and one
+ * e4m3 pass (twice the bf16 rate) into one accumulator, times 2^e_m.  The workspace
+ * must hold the split: at least tern_linear_bwd_workspace_ex(M, K, N, flags) bytes
+ * (the copies are consumed before the G GEMM, which reuses the same bytes).
+ * Error of each dX[m][r] against the exact sum, besides fp32 accumulation:
+ *   <= 6.3e-5 * sum_c |dY[m][c] scale[c] T[r][c]|
+ *      + 4.3e-9 * max_c |dY[m][c] scale[c]| * #{c : T[r][c] != 0}
+ * (the second term from dY values more than 2^13 below the row's largest, whose e4m3
+ * copy loses bits).  The bf16 split's bound is 2^-16 of the first sum alone.
  */
 #define TERN_BWD_ACCUMULATE 1u
+#define TERN_BWD_DX_SPLIT8 2u
+size_t tern_linear_bwd_workspace_ex(int64_t M, int64_t K, int64_t N, unsigned flags);
 int tern_linear_bwd_ex(const uint16_t* X, const uint16_t* dY, const tern_tiles* W, const float* scale,
                        float* dX, float* gq, float* sgrad, void* workspace, size_t ws_bytes, int64_t M,
                        int64_t K, int64_t N, unsigned flags, void* stream);

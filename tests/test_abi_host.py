@@ -55,6 +55,16 @@ def test_sizes(lib):
     # K <= 128: single-CTA tiles (128 x 256), 1 tile x 1 k-block -> one split tile at most
     assert lib.tern_linear_bwd_workspace(64, 128, 16) == 256 * (-(-(1 * 4 * 16 * 4) // 256)) + 128 * 256 * 4
     assert lib.tern_linear_bwd_workspace(0, 16, 16) == 0
+    # the fp16 + e4m3 dX planes and the split of dY (binary16, e4m3, the row and column
+    # exponents, each rounded up to 256 bytes), which the G GEMM's workspace shares
+    assert lib.tern_tiles_bytes(4096, 12288, lib.TERN_TILE_WHI16) == 4096 * 12288 * 2
+    assert lib.tern_tiles_bytes(4096, 12288, lib.TERN_TILE_WLO8) == 4096 * 12288
+    assert lib.tern_linear_bwd_workspace_ex(32768, 4096, 12288, 0) == lib.tern_linear_bwd_workspace(32768, 4096, 12288)
+    split = 32768 * 12288 * 3 + 32768 * 4 + 12288 * 4     # ... and the column exponents
+    assert lib.tern_linear_bwd_workspace_ex(32768, 4096, 12288, lib.TERN_BWD_DX_SPLIT8) == split
+    assert lib.tern_linear_bwd_workspace_ex(64, 4096, 16, lib.TERN_BWD_DX_SPLIT8) == \
+        lib.tern_linear_bwd_workspace(64, 4096, 16)       # the G workspace is the larger here
+    assert lib.tern_linear_bwd_workspace_ex(64, 128, 128, 8) == 0      # unknown flag
 
 
 P = ctypes.c_void_p
@@ -100,6 +110,26 @@ def test_backward_argument_checks(lib):
              P(0x70000), need, 64, 128, 128, None) == lib.TERN_ERR_ARG
 
 
+def test_split8_backward_argument_checks(lib):
+    f = lib.lib.tern_linear_bwd_ex
+    M, K, N = 64, 128, 128
+    split8 = lib._Tiles(P(0x10000), None, None, None, P(0x14000), P(0x15000))
+    need = lib.tern_linear_bwd_workspace_ex(M, K, N, lib.TERN_BWD_DX_SPLIT8)
+    call = lambda t, dX, ws, n, flags: f(P(0x20000), P(0x21000), ctypes.byref(t), P(0x30000), dX, None,  # noqa
+                                         None, ws, n, M, K, N, flags, None)
+    bf = _tiles(lib)                                                   # bf16 planes, no split planes
+    assert call(bf, P(0x40000), P(0x70000), need, lib.TERN_BWD_DX_SPLIT8) == lib.TERN_ERR_ARG
+    split_bytes = M * N * 2 + M * N + 256 + 512   # copies of dY, row and column exponents (256-byte units)
+    assert split_bytes <= need
+    assert call(split8, P(0x40000), P(0x70000), split_bytes - 16, lib.TERN_BWD_DX_SPLIT8) == lib.TERN_ERR_WORKSPACE
+    assert call(split8, P(0x40000), None, 0, lib.TERN_BWD_DX_SPLIT8) == lib.TERN_ERR_WORKSPACE
+    assert call(split8, P(0x40000), P(0x70008), need, lib.TERN_BWD_DX_SPLIT8) == lib.TERN_ERR_ALIGN
+    bad = lib._Tiles(P(0x10000), None, None, None, P(0x14000), P(0x15001))
+    assert call(bad, P(0x40000), P(0x70000), need, lib.TERN_BWD_DX_SPLIT8) == lib.TERN_ERR_ALIGN
+    assert call(split8, P(0x40000), P(0x70000), need, 4) == lib.TERN_ERR_ARG          # unknown flag
+    assert call(split8, P(0x40000), P(0x70000), need, 0) == lib.TERN_ERR_ARG          # bf16 planes needed
+
+
 def test_materialize_argument_checks(lib):
     f = lib.lib.tern_materialize
     t = _tiles(lib)
@@ -111,6 +141,10 @@ def test_materialize_argument_checks(lib):
     assert f(q, None, s, 16, 40, 2, 7, ctypes.byref(t), None) == lib.TERN_ERR_ALIGN
     assert f(P(0x20001), None, s, 16, 32, 2, 7, ctypes.byref(t), None) == lib.TERN_ERR_ALIGN
     assert f(q, None, s, 0, 32, 2, 7, ctypes.byref(t), None) == lib.TERN_ERR_ARG
+    s8 = lib._Tiles(None, None, None, None, P(0x14000), None)         # split planes need scale
+    assert f(q, None, None, 16, 32, 2, 7, ctypes.byref(s8), None) == lib.TERN_ERR_ARG
+    s8 = lib._Tiles(None, None, None, None, None, P(0x15008))
+    assert f(q, None, s, 16, 32, 2, 7, ctypes.byref(s8), None) == lib.TERN_ERR_ALIGN
 
 
 def test_adamw_argument_checks(lib):
