@@ -683,7 +683,7 @@ def run_ours(args):
     names = ["materialize", "fwd", "dx", "dw", "adamw"]
     step_no = [0]
 
-    def step(ev=None, Xs=None, dYs=None, tl=None):
+    def step(ev=None, Xs=None, dYs=None, tl=None, ws8=None):
         Xs = X if Xs is None else Xs
         dYs = dY if dYs is None else dYs
         tl = tiles if tl is None else tl
@@ -696,7 +696,10 @@ def run_ours(args):
         bl.tern_linear_fwd(Xs, tl, scale, Y)
         if ev is not None:
             ev[2].record(stream)
-        bl.tern_linear_bwd(Xs, dYs, tl, scale, dX, None, None, None)
+        if ws8 is None:
+            bl.tern_linear_bwd(Xs, dYs, tl, scale, dX, None, None, None)
+        else:   # dX from the fp16 + e4m3 split: dY is split into ws8 first
+            bl.tern_linear_bwd(Xs, dYs, tl, scale, dX, None, None, ws8, split8=True)
         if ev is not None:
             ev[3].record(stream)
         bl.tern_linear_bwd(Xs, dYs, tl, scale, None, gq, sgrad, wsp)
@@ -786,6 +789,30 @@ def run_ours(args):
                "kernels_ms": per_o, "fwd_tflops": 2.0 * M * K * N / (per_o["fwd"] * 1e-3) / 1e12,
                "materialize_bytes_per_weight": 1 + 0.25 + (2 if other == "bf16" else 0) + 4}
     del tiles_o
+
+    # ---- the same step with dX from the fp16 + e4m3 split (TERN_BWD_DX_SPLIT8): one
+    #      binary16 and one e4m3 pass (1.5 bf16-pass equivalents executed) after a split of dY
+    progress("step with dX from the fp16 + e4m3 split")
+    tiles_8 = bl.Tiles.empty(K, N, t=(args.t_operand == "bf16"), hi_lo=False, split8=True)
+    ws8 = torch.empty(bl.tern_linear_bwd_workspace_ex(M, K, N, bl.TERN_BWD_DX_SPLIT8) // 4, device=dev)
+    for _ in range(3):
+        step(tl=tiles_8, ws8=ws8)
+    torch.cuda.synchronize()
+    ev8 = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        step(ev8[i], tl=tiles_8, ws8=ws8)
+    torch.cuda.synchronize()
+    if bl.tern_device_status() != bl.TERN_OK:
+        raise RuntimeError("a kernel gave up on a bounded wait (dX from the fp16 + e4m3 split)")
+    per_8 = {n: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev8) for j, n in enumerate(names)}
+    ms_8 = ev8[0][0].elapsed_time(ev8[-1][5]) / args.steps
+    dx8 = {"ms_per_step": ms_8, "tflops": flops / (ms_8 * 1e-3) / 1e12, "kernels_ms": per_8,
+           "dx_tflops_credited": 2.0 * M * K * N / (per_8["dx"] * 1e-3) / 1e12,
+           "dx_executed": "2*M*K*N binary16 + 2*M*K*N e4m3 (1.5 bf16-pass equivalents), after the dY split",
+           "dx_ms_includes": "the dY split (binary16 and e4m3 copies, per-row exponents) and the GEMM",
+           "materialize_bytes_per_weight": 1 + 0.25 + (2 if args.t_operand == "bf16" else 0) + 3,
+           "error_bound": "6.3e-5*sum|term| + 4.3e-9*max_c|dY*scale|*nnz(T row), against 1e-4*sum|term|"}
+    del tiles_8, ws8
 
     # ---- end to end through the C ABI: every step's inputs X and dY copied from
     #      pinned host memory and the step's result (updated scales and their
@@ -879,6 +906,7 @@ def run_ours(args):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": dict(large_config(M, K, N, ws), t_operand=args.t_operand),
             "other_t_operand": variant,
+            "dx_split8": dx8,
             "frac_of_peak": {"spec_dense_bf16_2250": value / ws / SPEC_BF16_TFLOPS,
                              "measured_burst": value / ws / pk["bf16"],
                              "measured_sustained": value / ws / pk["bf16_sus"],

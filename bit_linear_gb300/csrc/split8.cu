@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(256) tern_split8_planes_kernel(const int8_t* _
 // The column exponents first (e_c, or kNoCol for a zero scale), then one block per row
 // of dY, eight columns (one 16-byte load) per chunk; up to kCh chunks per thread stay in
 // registers between the block's two passes (the rest are read again).
-constexpr int kCh = 8;
+constexpr int kCh = 4;
 constexpr int kNoCol = -(1 << 20);   // a zero scale: the column of W is zero
 
 __global__ void __launch_bounds__(256) tern_split8_colexp_kernel(const float* __restrict__ scale, int N,
@@ -156,13 +156,13 @@ __device__ __forceinline__ float times_pow2(uint32_t b, int e) {
     return scale_pow2(b, e);
 }
 
-__global__ void __launch_bounds__(256) tern_split8_dy_kernel(const uint16_t* __restrict__ dY,
+__global__ void __launch_bounds__(512) tern_split8_dy_kernel(const uint16_t* __restrict__ dY,
                                                               const int* __restrict__ ec, int N,
                                                               uint16_t* __restrict__ dy16, uint8_t* __restrict__ dy8,
                                                               int* __restrict__ row_exp) {
     ptx::pdl_trigger();
     ptx::pdl_wait();
-    __shared__ int red[8];
+    __shared__ int red[16];
     const int64_t row = blockIdx.x;
     const int chunks = N / 8;
     const uint4* src = reinterpret_cast<const uint4*>(dY + row * N);
@@ -266,10 +266,10 @@ int split8_dy(const uint16_t* dY, const float* scale, int64_t M, int64_t N, void
     if (int st = launch_pdl(tern_split8_colexp_kernel, dim3(static_cast<unsigned>((N + 255) / 256)), dim3(256), 0, s,
                             scale, static_cast<int>(N), ec))
         return st;
-    // threads per row: enough that each holds at most four chunks, from one warp to eight
+    // threads per row: enough that each holds at most four chunks (kCh), one warp to sixteen
     const int64_t chunks = N / 8;
     int tpr = 32;
-    while (tpr < 256 && chunks > 4 * tpr) tpr *= 2;
+    while (tpr < 512 && chunks > kCh * tpr) tpr *= 2;
     return launch_pdl(tern_split8_dy_kernel, dim3(static_cast<unsigned>(M)), dim3(tpr), 0, s, dY,
                       static_cast<const int*>(ec), static_cast<int>(N), *dy16, *dy8, *row_exp);
 }
