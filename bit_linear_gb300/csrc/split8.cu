@@ -134,105 +134,165 @@ __global__ void __launch_bounds__(256) tern_split8_planes_kernel(const int8_t* _
 
 // ---------------------------------------------------------------- the split of dY
 //
-// The column exponents first (e_c, or kNoCol for a zero scale), then one block per row
-// of dY, eight columns (one 16-byte load) per chunk; up to kCh chunks per thread stay in
-// registers between the block's two passes (the rest are read again).
-constexpr int kCh = 4;
-constexpr int kNoCol = -(1 << 20);   // a zero scale: the column of W is zero
+// The column factors 2^e_c first (0 for a zero scale) with the range of e_c, then one
+// block per row of dY, eight columns (one 16-byte load) per chunk; up to kCh chunks per
+// thread stay in registers between the block's two passes (the rest are read again).
+// A row takes the fp32 path (a multiply per value, exact while the products are fp32
+// normals) when its largest product and every column's 2^(e_c - e_m) are fp32 normals,
+// else the integer path (exponent arithmetic on the bit patterns).
+constexpr int kCh = 3;
 
-__global__ void __launch_bounds__(256) tern_split8_colexp_kernel(const float* __restrict__ scale, int N,
-                                                                  int* __restrict__ ec) {
+// 2^e as fp32 for e in [-149, 127] (subnormal below -126).
+__device__ __forceinline__ float pow2f(int e) {
+    return e >= -126 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23) : __uint_as_float(1u << (e + 149));
+}
+
+__global__ void __launch_bounds__(1024) tern_split8_colexp_kernel(const float* __restrict__ scale, int N,
+                                                                   float* __restrict__ fac, int* __restrict__ ext) {
     ptx::pdl_trigger();
     ptx::pdl_wait();
-    const int c = static_cast<int>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (c >= N) return;
-    const uint32_t sb = __float_as_uint(scale[c]);
-    ec[c] = (sb & 0x7FFFFFFFu) ? ilog2f(sb) : kNoCol;
+    __shared__ int rlo[32], rhi[32];
+    int lo = INT_MAX, hi = INT_MIN;
+    for (int c = static_cast<int>(threadIdx.x); c < N; c += static_cast<int>(blockDim.x)) {
+        const uint32_t sb = __float_as_uint(scale[c]);
+        float f = 0.0f;
+        if (sb & 0x7FFFFFFFu) {
+            const int e = ilog2f(sb);
+            f = pow2f(e);
+            lo = min(lo, e);
+            hi = max(hi, e);
+        }
+        fac[c] = f;
+    }
+    lo = __reduce_min_sync(0xffffffffu, lo);
+    hi = __reduce_max_sync(0xffffffffu, hi);
+    if ((threadIdx.x & 31) == 0) {
+        rlo[threadIdx.x >> 5] = lo;
+        rhi[threadIdx.x >> 5] = hi;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int k = 1; k < static_cast<int>(blockDim.x >> 5); ++k) {
+            lo = min(lo, rlo[k]);
+            hi = max(hi, rhi[k]);
+        }
+        ext[0] = lo == INT_MAX ? 0 : lo;   // no nonzero scale: every output is zero
+        ext[1] = hi == INT_MIN ? 0 : hi;
+    }
 }
 
-// dY[c] * 2^e as fp32 (see scale_pow2): one multiply by 2^e when 2^e is an fp32 normal.
-__device__ __forceinline__ float times_pow2(uint32_t b, int e) {
-    if (e >= -126 && e <= 127) return __uint_as_float(b) * __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
-    return scale_pow2(b, e);
+__device__ __forceinline__ float bf16_at(const uint32_t (&w)[4], int j) {
+    return __uint_as_float((j & 1) ? (w[j >> 1] & 0xFFFF0000u) : (w[j >> 1] << 16));
 }
 
-__global__ void __launch_bounds__(512) tern_split8_dy_kernel(const uint16_t* __restrict__ dY,
-                                                              const int* __restrict__ ec, int N,
+// Block-wide maximum of a non-negative int (or of non-negative fp32 bit patterns, which
+// order like their values).
+__device__ __forceinline__ int block_max(int v, int* red) {
+    v = __reduce_max_sync(0xffffffffu, v);
+    __syncthreads();   // red is reused
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    v = red[0];
+    for (int k = 1; k < static_cast<int>(blockDim.x >> 5); ++k) v = max(v, red[k]);
+    return v;
+}
+
+__global__ void __launch_bounds__(512, 3) tern_split8_dy_kernel(const uint16_t* __restrict__ dY,
+                                                              const float* __restrict__ fac,
+                                                              const int* __restrict__ ext, int N,
                                                               uint16_t* __restrict__ dy16, uint8_t* __restrict__ dy8,
                                                               int* __restrict__ row_exp) {
     ptx::pdl_trigger();
     ptx::pdl_wait();
     __shared__ int red[16];
     const int64_t row = blockIdx.x;
-    const int chunks = N / 8;
+    const int chunks = N / 8, tid = static_cast<int>(threadIdx.x), nt = static_cast<int>(blockDim.x);
     const uint4* src = reinterpret_cast<const uint4*>(dY + row * N);
-    const int4* ecv = reinterpret_cast<const int4*>(ec);
+    const float4* facv = reinterpret_cast<const float4*>(fac);
     uint4 keep[kCh];
 #pragma unroll
-    for (int i = 0; i < kCh; ++i) {
-        const int ch = static_cast<int>(threadIdx.x) + i * static_cast<int>(blockDim.x);
-        if (ch < chunks) keep[i] = __ldcs(src + ch);
-    }
-    auto chunk = [&](int i, int ch) {
-        uint4 v;
-        if (i < kCh) {
-#pragma unroll
-            for (int k = 0; k < kCh; ++k)
-                if (k == i) v = keep[k];
-        } else {
-            v = __ldcs(src + ch);
-        }
-        return v;
+    for (int i = 0; i < kCh; ++i)
+        if (tid + i * nt < chunks) keep[i] = __ldcs(src + tid + i * nt);
+    auto factors = [&](int ch, float (&f)[8]) {
+        const float4 f0 = __ldg(facv + 2 * ch), f1 = __ldg(facv + 2 * ch + 1);
+        f[0] = f0.x, f[1] = f0.y, f[2] = f0.z, f[3] = f0.w, f[4] = f1.x, f[5] = f1.y, f[6] = f1.z, f[7] = f1.w;
     };
-    // pass 1: E = max over the row of floor(log2|dY[c]|) + e_c (nonzero dY, nonzero scale)
-    int E = INT_MIN;
-    for (int i = 0;; ++i) {
-        const int ch = static_cast<int>(threadIdx.x) + i * static_cast<int>(blockDim.x);
-        if (ch >= chunks) break;
-        const uint4 v = chunk(i, ch);
-        const int4 e0 = __ldg(ecv + 2 * ch), e1 = __ldg(ecv + 2 * ch + 1);
-        const int ecs[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    // every chunk of the row once: the kCh kept ones, then the rest from global memory
+    auto for_chunks = [&](auto&& fn) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const uint32_t b = (j & 1) ? (w[j >> 1] & 0xFFFF0000u) : (w[j >> 1] << 16);   // bf16 -> fp32 bits
-            if ((b & 0x7FFFFFFFu) && ecs[j] != kNoCol) E = max(E, ilog2f(b) + ecs[j]);
-        }
-    }
-    E = __reduce_max_sync(0xffffffffu, E);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = E;
-    __syncthreads();
-    E = red[0];
-    for (int k = 1; k < static_cast<int>(blockDim.x >> 5); ++k) E = max(E, red[k]);
-    const int em = E == INT_MIN ? 0 : E - 14;
-    if (threadIdx.x == 0) row_exp[row] = em;
-    // pass 2: the two scaled copies
-    for (int i = 0;; ++i) {
-        const int ch = static_cast<int>(threadIdx.x) + i * static_cast<int>(blockDim.x);
-        if (ch >= chunks) break;
-        const uint4 v = chunk(i, ch);
-        const int4 e0 = __ldg(ecv + 2 * ch), e1 = __ldg(ecv + 2 * ch + 1);
-        const int ecs[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        for (int i = 0; i < kCh; ++i)
+            if (tid + i * nt < chunks) fn(keep[i], tid + i * nt);
+        for (int ch = tid + kCh * nt; ch < chunks; ch += nt) fn(__ldcs(src + ch), ch);
+    };
+    auto for_chunks_again = [&](auto&& fn) {   // the integer path (rare) reads the row again
+        for (int ch = tid; ch < chunks; ch += nt) fn(__ldg(src + ch), ch);
+    };
+    auto store = [&](int ch, const float (&y)[8]) {
         uint32_t o16[4], o8[4];
 #pragma unroll
         for (int j = 0; j < 8; j += 2) {
-            float y[2];
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                const uint32_t b = t ? (w[j >> 1] & 0xFFFF0000u) : (w[j >> 1] << 16);
-                y[t] = ecs[j + t] == kNoCol ? 0.0f : times_pow2(b, ecs[j + t] - em);
-            }
-            const __half2 hv = __floats2half2_rn(y[0], y[1]);   // .x (low half) = column j
+            const __half2 hv = __floats2half2_rn(y[j], y[j + 1]);   // .x (low half) = column j
             o16[j >> 1] = *reinterpret_cast<const uint32_t*>(&hv);
-            // the e4m3 copy is 2^-7 of the binary16 one (exact: y is an fp32 normal or below 2^-126)
-            o8[j >> 1] = __nv_cvt_float2_to_fp8x2(make_float2(y[0] * 0.0078125f, y[1] * 0.0078125f), __NV_SATFINITE,
-                                                 __NV_E4M3);   // low byte = column j
+            // the e4m3 copy is 2^-7 of the binary16 one (exact for fp32 normals; below 2^-126
+            // both formats give zero)
+            o8[j >> 1] = __nv_cvt_float2_to_fp8x2(make_float2(y[j] * 0.0078125f, y[j + 1] * 0.0078125f),
+                                                 __NV_SATFINITE, __NV_E4M3);   // low byte = column j
         }
         reinterpret_cast<uint4*>(dy16 + row * N)[ch] = make_uint4(o16[0], o16[1], o16[2], o16[3]);
-        reinterpret_cast<uint2*>(dy8 + row * N)[ch] =
-            make_uint2(o8[0] | (o8[1] << 16), o8[2] | (o8[3] << 16));
+        reinterpret_cast<uint2*>(dy8 + row * N)[ch] = make_uint2(o8[0] | (o8[1] << 16), o8[2] | (o8[3] << 16));
+    };
+
+    // pass 1, fp32: the row's largest |dY[c]| * 2^e_c
+    float mx = 0.0f;
+    for_chunks([&](const uint4& v, int ch) {
+        float f[8];
+        factors(ch, f);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) mx = fmaxf(mx, fabsf(bf16_at(w, j)) * f[j]);
+    });
+    const uint32_t mb = static_cast<uint32_t>(block_max(static_cast<int>(__float_as_uint(mx)), red));
+    int em = static_cast<int>(mb >> 23) - 127 - 14;
+    const bool fast = mb >= 0x00800000u && mb < 0x7F800000u && em >= -126 && em <= 126 && ext[0] - em >= -126 &&
+                      ext[1] - em <= 127;   // the same for the whole block
+    if (fast) {
+        // pass 2: y = dY[c] * (2^e_c * 2^-e_m), both factors and the product fp32 normals
+        const float sm = pow2f(-em);
+        for_chunks([&](const uint4& v, int ch) {
+            float f[8], y[8];
+            factors(ch, f);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 8; ++j) y[j] = bf16_at(w, j) * (f[j] * sm);
+            store(ch, y);
+        });
+    } else {
+        // the integer path: E = max of floor(log2|dY[c]|) + e_c over nonzero values and scales
+        int E = INT_MIN;
+        for_chunks_again([&](const uint4& v, int ch) {
+            float f[8];
+            factors(ch, f);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll 1
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t b = __float_as_uint(bf16_at(w, j));
+                if ((b & 0x7FFFFFFFu) && f[j] != 0.0f) E = max(E, ilog2f(b) + ilog2f(__float_as_uint(f[j])));
+            }
+        });
+        E = block_max(E, red);
+        em = E == INT_MIN ? 0 : E - 14;
+        for_chunks_again([&](const uint4& v, int ch) {
+            float f[8], y[8];
+            factors(ch, f);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll 1
+            for (int j = 0; j < 8; ++j)
+                y[j] = f[j] == 0.0f ? 0.0f
+                                    : scale_pow2(__float_as_uint(bf16_at(w, j)), ilog2f(__float_as_uint(f[j])) - em);
+            store(ch, y);
+        });
     }
+    if (threadIdx.x == 0) row_exp[row] = em;
 }
 
 int64_t round256(int64_t b) { return (b + 255) / 256 * 256; }
@@ -253,25 +313,29 @@ int split8_planes(const int8_t* q, const float* scale, int64_t K, int64_t N, int
 }
 
 int64_t split8_dy_bytes(int64_t M, int64_t N) {
-    return round256(M * N * 2) + round256(M * N) + round256(M * 4) + round256(N * 4);
+    return round256(M * N * 2) + round256(M * N) + round256(M * 4) + round256(N * 4) + 256;
 }
 
 int split8_dy(const uint16_t* dY, const float* scale, int64_t M, int64_t N, void* ws, uint16_t** dy16, uint8_t** dy8,
               int** row_exp, cudaStream_t s) {
     char* p = static_cast<char*>(ws);
     *dy16 = reinterpret_cast<uint16_t*>(p);
-    *dy8 = reinterpret_cast<uint8_t*>(p + round256(M * N * 2));
-    *row_exp = reinterpret_cast<int*>(p + round256(M * N * 2) + round256(M * N));
-    int* ec = reinterpret_cast<int*>(p + round256(M * N * 2) + round256(M * N) + round256(M * 4));
-    if (int st = launch_pdl(tern_split8_colexp_kernel, dim3(static_cast<unsigned>((N + 255) / 256)), dim3(256), 0, s,
-                            scale, static_cast<int>(N), ec))
+    p += round256(M * N * 2);
+    *dy8 = reinterpret_cast<uint8_t*>(p);
+    p += round256(M * N);
+    *row_exp = reinterpret_cast<int*>(p);
+    p += round256(M * 4);
+    float* fac = reinterpret_cast<float*>(p);
+    int* ext = reinterpret_cast<int*>(p + round256(N * 4));
+    if (int st = launch_pdl(tern_split8_colexp_kernel, dim3(1), dim3(1024), 0, s, scale, static_cast<int>(N), fac, ext))
         return st;
-    // threads per row: enough that each holds at most four chunks (kCh), one warp to sixteen
+    // threads per row: enough that each holds at most kCh chunks, one warp to sixteen
     const int64_t chunks = N / 8;
     int tpr = 32;
     while (tpr < 512 && chunks > kCh * tpr) tpr *= 2;
     return launch_pdl(tern_split8_dy_kernel, dim3(static_cast<unsigned>(M)), dim3(tpr), 0, s, dY,
-                      static_cast<const int*>(ec), static_cast<int>(N), *dy16, *dy8, *row_exp);
+                      static_cast<const float*>(fac), static_cast<const int*>(ext), static_cast<int>(N), *dy16, *dy8,
+                      *row_exp);
 }
 
 }  // namespace tern

@@ -55,12 +55,13 @@ def test_sizes(lib):
     # K <= 128: single-CTA tiles (128 x 256), 1 tile x 1 k-block -> one split tile at most
     assert lib.tern_linear_bwd_workspace(64, 128, 16) == 256 * (-(-(1 * 4 * 16 * 4) // 256)) + 128 * 256 * 4
     assert lib.tern_linear_bwd_workspace(0, 16, 16) == 0
-    # the fp16 + e4m3 dX planes and the split of dY (binary16, e4m3, the row and column
-    # exponents, each rounded up to 256 bytes), which the G GEMM's workspace shares
+    # the fp16 + e4m3 dX planes and the split of dY (binary16, e4m3, the row exponents, the
+    # column factors and their range, each rounded up to 256 bytes), which the G GEMM's
+    # workspace shares
     assert lib.tern_tiles_bytes(4096, 12288, lib.TERN_TILE_WHI16) == 4096 * 12288 * 2
     assert lib.tern_tiles_bytes(4096, 12288, lib.TERN_TILE_WLO8) == 4096 * 12288
     assert lib.tern_linear_bwd_workspace_ex(32768, 4096, 12288, 0) == lib.tern_linear_bwd_workspace(32768, 4096, 12288)
-    split = 32768 * 12288 * 3 + 32768 * 4 + 12288 * 4     # ... and the column exponents
+    split = 32768 * 12288 * 3 + 32768 * 4 + 12288 * 4 + 256   # ... the column factors and their range
     assert lib.tern_linear_bwd_workspace_ex(32768, 4096, 12288, lib.TERN_BWD_DX_SPLIT8) == split
     assert lib.tern_linear_bwd_workspace_ex(64, 4096, 16, lib.TERN_BWD_DX_SPLIT8) == \
         lib.tern_linear_bwd_workspace(64, 4096, 16)       # the G workspace is the larger here
@@ -119,7 +120,7 @@ def test_split8_backward_argument_checks(lib):
                                          None, ws, n, M, K, N, flags, None)
     bf = _tiles(lib)                                                   # bf16 planes, no split planes
     assert call(bf, P(0x40000), P(0x70000), need, lib.TERN_BWD_DX_SPLIT8) == lib.TERN_ERR_ARG
-    split_bytes = M * N * 2 + M * N + 256 + 512   # copies of dY, row and column exponents (256-byte units)
+    split_bytes = M * N * 2 + M * N + 256 + 512 + 256   # copies of dY, row exponents, column factors, range
     assert split_bytes <= need
     assert call(split8, P(0x40000), P(0x70000), split_bytes - 16, lib.TERN_BWD_DX_SPLIT8) == lib.TERN_ERR_WORKSPACE
     assert call(split8, P(0x40000), None, 0, lib.TERN_BWD_DX_SPLIT8) == lib.TERN_ERR_WORKSPACE
