@@ -600,7 +600,8 @@ def graph_bw(torch, fn, nbytes, reps, warm, stream, peak_gbs):
 def hbm_kernels(args):
     """The HBM-bound kernels alone at profiling sizes (each input over L2, a few GB in
     all): AdamW on 1e8 elements, packed ternarisation of 1e9 weights, the full
-    materialise, the SR4 step and the panel of the large projection's weight.
+    materialise, the SR4 step and the panel of the large projection's weight, the fp16 +
+    e4m3 dX planes and the split dX call (whose dY split is the HBM-bound part).
     Prints one line of GB/s per kernel; a case for ncu, not a bench line."""
     import torch
     torch.cuda.set_device(0)
@@ -637,6 +638,19 @@ def hbm_kernels(args):
     stats = torch.zeros(3, dtype=torch.float64, device=dev)
     out["sr4_panel"] = loop(lambda: bl.tern_sr4_panel(q, scale, counts, stats, packed_prev=tiles.packed),
                             1.25 * K * N, args.steps)
+    # the fp16 + e4m3 dX planes alone (1 B of q read, 2 + 1 B written per weight), and the
+    # split of dY at the profiling case's M = 8192 (2 B read, 3 B written per element; the
+    # call also runs the split GEMM, so this is a case for ncu's per-kernel counters)
+    t8 = bl.Tiles(K, N, whi_f16=torch.empty((K, N), dtype=torch.float16, device=dev),
+                  wlo_e4m3=torch.empty((K, N), dtype=torch.uint8, device=dev))
+    out["split8_planes"] = loop(lambda: bl.tern_materialize(q, scale, t8, 2, 7), 4.0 * K * N, args.steps)
+    Mq = 8192
+    X = torch.empty(Mq, K, device=dev).normal_().to(torch.bfloat16)
+    dY = torch.empty(Mq, N, device=dev).normal_(0, 0.01).to(torch.bfloat16)
+    dX = torch.empty(Mq, K, device=dev)
+    ws8 = torch.empty(bl.tern_linear_bwd_workspace_ex(Mq, K, N, bl.TERN_BWD_DX_SPLIT8) // 4, device=dev)
+    out["split8_dx_call"] = loop(lambda: bl.tern_linear_bwd(X, dY, t8, scale, dX, None, None, ws8, split8=True),
+                                 5.0 * Mq * N, args.steps)
     print(json.dumps({"hbm_kernels": out, "peak_hbm_gbs": pk["hbm"]}), flush=True)
     return 0
 
