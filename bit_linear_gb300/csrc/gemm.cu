@@ -155,6 +155,9 @@ struct Cfg {
     static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES + A8_BYTES + B8_BYTES;   // per CTA
     static constexpr int TX_BYTES = CG * (PK ? A_BYTES : STAGE_BYTES);   // TMA bytes on the leader's barrier
     static constexpr int P_BYTES = PK ? BK * (B_ROWS / 16) * 4 : 0;     // 2-bit codes of a stage's B (PK)
+    // raster: runs of RASTER m-tiles share an n-tile (tile_coords).  dX's B operands (W_hi
+    // and W_lo, or the split planes) are the larger panels, so its runs are longer.
+    static constexpr int RASTER = (EPI == EPI_DX ? 24 : 16) / CG;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int SMEM_BYTES = STAGES * (STAGE_BYTES + P_BYTES) + 1024 + 256;
     static_assert(CG == 1 || CG == 2, "CTA group");
@@ -509,7 +512,7 @@ __device__ __forceinline__ void gemm_body(const GRP& grp) {
             const CUtensorMap* tmB0 = &grp.mB0[p];
             const CUtensorMap* tmB1 = &grp.mB1[p];
             int mt, nt;
-            tile_coords<16 / CG>(a.tile_begin + u / a.split, a.tiles_m, a.tiles_n, mt, nt);
+            tile_coords<C::RASTER>(a.tile_begin + u / a.split, a.tiles_m, a.tiles_n, mt, nt);
             const int arow = mt * C::TILE_M + static_cast<int>(rank) * kBM;
             const int brow = nt * C::BN + static_cast<int>(rank) * C::B_ROWS;
             const int kb0 = (u % a.split) * a.kb_per, kb1 = min(a.num_kb, kb0 + a.kb_per);
@@ -744,7 +747,7 @@ __device__ __forceinline__ void gemm_body(const GRP& grp) {
                 const GemmArgs& an = grp.args[pn];
                 if (an.partial_g == nullptr && (C::EPI == EPI_FWD || an.out != nullptr)) {
                     int mtn, ntn;
-                    tile_coords<16 / CG>(an.tile_begin + (ugn - grp.unit_begin[pn]) / an.split, an.tiles_m,
+                    tile_coords<C::RASTER>(an.tile_begin + (ugn - grp.unit_begin[pn]) / an.split, an.tiles_m,
                                          an.tiles_n, mtn, ntn);
                     sp = an.scale;
                     col0 = ntn * C::BN;
@@ -767,7 +770,7 @@ __device__ __forceinline__ void gemm_body(const GRP& grp) {
             ptx::tc_fence_after();
             unit_scales(ug + units, sc_next);   // in flight while this tile drains
             int mt, nt;
-            tile_coords<16 / CG>(a.tile_begin + u / a.split, a.tiles_m, a.tiles_n, mt, nt);
+            tile_coords<C::RASTER>(a.tile_begin + u / a.split, a.tiles_m, a.tiles_n, mt, nt);
             const int row0 = mt * C::TILE_M + static_cast<int>(rank) * kBM;
             const uint32_t trow = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * C::BN;
             if (C::EPI == EPI_DW && a.partial_g != nullptr) {
