@@ -1312,23 +1312,37 @@ int launch_split_reduce(const ReduceGroup<G>& r, cudaStream_t s) {
 // they are; when the last wave would leave units idle and `tail` has room, the
 // remaining tiles are split along the token axis over the idle units and
 // finished by tern_dw_split_reduce.
-template <class C, class K>
-int run_dw(K kernel, const uint16_t* X, const uint16_t* dY, const float* scale, const uint32_t* packed, float* gq,
-           float* partial, int accumulate, float* tail, int64_t tail_bytes, int64_t M, int64_t K_, int64_t N,
-           int num_sms, cudaStream_t s) {
-    GemmGroup<1> g;
-    GemmArgs a = make_args<C>(K_, N, M);
-    a.out = gq;
-    a.scale = scale;
-    a.packed = packed;
-    a.partial = partial;
-    a.accumulate = accumulate;
-    if (int st = group_set<C>(g, 0, X, K_, M, dY, nullptr, N, M, a)) return st;
+// The split factor of the tail of a G launch: the R tiles left after whole waves of
+// `units` are split along the token axis into s slices of ceil(kb/s) k-blocks when that
+// shortens the last rounds.  Minimises rounds(R*s) * ceil(kb/s) + 0.15 * R*s, the second
+// term the reduce pass's read of each partial tile in k-block times (256 KB at the HBM
+// rate against one 64-deep k-block of a 256 x 256 tile).
+int tail_split(int R, int kb, int units, int max_units) {
+    if (R <= 0) return 1;
+    int best = 1;
+    double best_cost = kb;   // one round of whole tiles
+    for (int sp = 2; sp <= kb && R * sp <= max_units; ++sp) {
+        const int per = (kb + sp - 1) / sp;
+        const double cost = std::ceil(static_cast<double>(R) * sp / units) * per + 0.15 * R * sp;
+        if (cost < best_cost - 1e-9) {
+            best = sp;
+            best_cost = cost;
+        }
+    }
+    return best;
+}
+
+// The G launch of one problem (index 0 of g): whole waves of tiles as they are; when the
+// last wave would leave units idle and `tail` has room, its tiles are split along the
+// token axis (tail_split) and finished by tern_dw_split_reduce.
+template <class C, class K, class GRP>
+int dw_waves_and_tail(K kernel, GRP& g, float* tail, int64_t tail_bytes, int max_units, int num_sms, cudaStream_t s) {
     if (tail) {
         int units = 0;
         if (int st = persistent_units<C>(kernel, num_sms, &units)) return st;
+        const GemmArgs a = g.args[0];
         const int T = a.num_tiles, T0 = (T / units) * units, R = T - T0;
-        int split = R > 0 ? std::min(units / R, a.num_kb) : 1;
+        int split = tail_split(R, a.num_kb, units, max_units);
         if (split >= 2) {
             const int kb_per = (a.num_kb + split - 1) / split;
             split = (a.num_kb + kb_per - 1) / kb_per;   // every slice non-empty
@@ -1360,6 +1374,21 @@ int run_dw(K kernel, const uint16_t* X, const uint16_t* dY, const float* scale, 
     }
     group_close(g, 1);
     return launch<C>(kernel, g, num_sms, s);
+}
+
+template <class C, class K>
+int run_dw(K kernel, const uint16_t* X, const uint16_t* dY, const float* scale, const uint32_t* packed, float* gq,
+           float* partial, int accumulate, float* tail, int64_t tail_bytes, int64_t M, int64_t K_, int64_t N,
+           int num_sms, cudaStream_t s) {
+    GemmGroup<1> g;
+    GemmArgs a = make_args<C>(K_, N, M);
+    a.out = gq;
+    a.scale = scale;
+    a.packed = packed;
+    a.partial = partial;
+    a.accumulate = accumulate;
+    if (int st = group_set<C>(g, 0, X, K_, M, dY, nullptr, N, M, a)) return st;
+    return dw_waves_and_tail<C>(kernel, g, tail, tail_bytes, kMaxTailUnits, num_sms, s);
 }
 
 }  // namespace
@@ -1654,6 +1683,8 @@ int dw_group(K kernel, const tern_layer* L, const int* idx, int n, float* const*
     const int64_t tile_bytes = static_cast<int64_t>(C::TILE_M) * C::BN * static_cast<int64_t>(sizeof(float));
     if (split >= 2 && static_cast<int64_t>(tiles) * split * tile_bytes > tail_bytes) split = 1;
     if (split == 1) {
+        // one layer: whole waves, then its last wave's tiles split (as the single-layer call)
+        if (n == 1) return dw_waves_and_tail<C>(kernel, g, tail, tail_bytes, kMaxGroupTailUnits, num_sms, s);
         group_close(g, n);
         return launch<C>(kernel, g, num_sms, s);
     }
