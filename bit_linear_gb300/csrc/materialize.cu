@@ -50,8 +50,11 @@ __device__ __forceinline__ uint32_t lanes16(uint32_t bytemask, uint32_t sel) {
     return __byte_perm(bytemask, 0u, sel);
 }
 
+// Sixteen weights (one packed word) per thread and call, for the launches that write no
+// bf16 plane (those take encode_half).
 template <bool QC, bool PK, bool TT, bool HL>
 __device__ __forceinline__ void encode_group(const MatArgs& a, int4 raw, int64_t gi) {
+    static_assert(!TT && !HL, "the bf16 planes are written eight weights at a time (encode_half)");
     const uint32_t w[4] = {static_cast<uint32_t>(raw.x), static_cast<uint32_t>(raw.y),
                            static_cast<uint32_t>(raw.z), static_cast<uint32_t>(raw.w)};
     uint32_t pos[4], neg[4];
@@ -75,61 +78,6 @@ __device__ __forceinline__ void encode_group(const MatArgs& a, int4 raw, int64_t
         __stcs(reinterpret_cast<int4*>(a.qc + e0), c);
     }
     if constexpr (PK) __stcs(a.packed + gi, code);
-    if constexpr (!TT && !HL) return;
-    // 16-bit lane masks of weight pairs (2i, 2i+1): nz = weight != 0, ng = weight < 0
-    uint32_t nz[8], ng[8];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        nz[2 * k] = lanes16(pos[k] | neg[k], 0x1100u);
-        nz[2 * k + 1] = lanes16(pos[k] | neg[k], 0x3322u);
-        ng[2 * k] = lanes16(neg[k], 0x1100u);
-        ng[2 * k + 1] = lanes16(neg[k], 0x3322u);
-    }
-    if constexpr (TT) {
-        uint32_t p[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) p[i] = (nz[i] & 0x3F803F80u) | (ng[i] & 0x80008000u);
-        int4* dst = reinterpret_cast<int4*>(a.t + e0);
-        __stcs(dst, make_int4(p[0], p[1], p[2], p[3]));
-        __stcs(dst + 1, make_int4(p[4], p[5], p[6], p[7]));
-    }
-    if constexpr (HL) {
-        const uint32_t cg = static_cast<uint32_t>(gi % a.ngroups_row);
-        const float4* sp = reinterpret_cast<const float4*>(a.scale + static_cast<int64_t>(cg) * 16);
-        uint32_t hi2[8], lo2[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float4 s4 = __ldg(sp + i);
-            const float s[4] = {s4.x, s4.y, s4.z, s4.w};
-            uint32_t hb[4], lb[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                hb[k] = bf16_bits(s[k]);
-                lb[k] = bf16_bits(s[k] - __uint_as_float(hb[k] << 16));   // exact difference in fp32
-            }
-            hi2[2 * i] = hb[0] | (hb[1] << 16);
-            hi2[2 * i + 1] = hb[2] | (hb[3] << 16);
-            lo2[2 * i] = lb[0] | (lb[1] << 16);
-            lo2[2 * i + 1] = lb[2] | (lb[3] << 16);
-        }
-        // a zero weight is +0; a negative weight flips the sign bit of s_hi / s_lo
-        if (a.whi) {
-            uint32_t p[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) p[i] = (hi2[i] & nz[i]) ^ (ng[i] & 0x80008000u);
-            int4* dst = reinterpret_cast<int4*>(a.whi + e0);
-            __stcs(dst, make_int4(p[0], p[1], p[2], p[3]));
-            __stcs(dst + 1, make_int4(p[4], p[5], p[6], p[7]));
-        }
-        if (a.wlo) {
-            uint32_t p[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) p[i] = (lo2[i] & nz[i]) ^ (ng[i] & 0x80008000u);
-            int4* dst = reinterpret_cast<int4*>(a.wlo + e0);
-            __stcs(dst, make_int4(p[0], p[1], p[2], p[3]));
-            __stcs(dst + 1, make_int4(p[4], p[5], p[6], p[7]));
-        }
-    }
 }
 
 // Eight weights (half a packed word) per thread and call, for the launches that
