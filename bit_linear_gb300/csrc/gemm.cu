@@ -1314,16 +1314,17 @@ int launch_split_reduce(const ReduceGroup<G>& r, cudaStream_t s) {
 // finished by tern_dw_split_reduce.
 // The split factor of the tail of a G launch: the R tiles left after whole waves of
 // `units` are split along the token axis into s slices of ceil(kb/s) k-blocks when that
-// shortens the last rounds.  Minimises rounds(R*s) * ceil(kb/s) + 0.15 * R*s, the second
-// term the reduce pass's read of each partial tile in k-block times (256 KB at the HBM
-// rate against one 64-deep k-block of a 256 x 256 tile).
+// shortens the last rounds.  Minimises, in times of one 64-deep k-block of a 256 x 256
+// tile, rounds(R*s) * ceil(kb/s) + 0.32 * R*s + 20: the reduce pass costs about 0.32 per
+// partial tile and the extra launches about 20 (measured at the wide chain's G: 200
+// partial tiles reduced in 17 us).
 int tail_split(int R, int kb, int units, int max_units) {
     if (R <= 0) return 1;
     int best = 1;
     double best_cost = kb;   // one round of whole tiles
     for (int sp = 2; sp <= kb && R * sp <= max_units; ++sp) {
         const int per = (kb + sp - 1) / sp;
-        const double cost = std::ceil(static_cast<double>(R) * sp / units) * per + 0.15 * R * sp;
+        const double cost = std::ceil(static_cast<double>(R) * sp / units) * per + 0.32 * R * sp + 20.0;
         if (cost < best_cost - 1e-9) {
             best = sp;
             best_cost = cost;
