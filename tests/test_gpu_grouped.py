@@ -248,3 +248,25 @@ def test_prepared_calls_repeat_the_plain_calls(cuda_lib):
     torch.cuda.synchronize()
     for a, b in zip(w + m1 + v1, w2 + m2 + v2):
         assert torch.equal(a, b)
+
+
+def test_single_layer_group_splits_the_last_wave_like_the_single_call(cuda_lib):
+    """A grouped backward of one layer whose G tiles fill two waves and part of a third (the
+    wide chain's up projection: 192 pair tiles on 76 pairs) runs the whole waves, then the
+    last wave's tiles split along the token axis, as the single-layer call does: the same
+    gq and sgrad bits, and the oracle's values on sampled entries."""
+    from _parity import sampled_oracle_check
+    bl = cuda_lib
+    c = syn.WIDE
+    inp = syn.linear_inputs(c["M"], c["K"], c["N"], seed=3, scale_lo=c["scale_lo"], scale_hi=c["scale_hi"],
+                            zero_prob=c["zero_prob"])
+    L = Layer(inp)
+    bl.tern_materialize(L.q, L.scale, L.tiles, 2, 7)
+    bl.tern_linear_fwd(L.X, L.tiles, L.scale, L.Y)
+    bl.tern_linear_bwd_grouped(_bwd_dicts([L]), _workspace(bl, [L]))
+    assert bl.tern_device_status() == bl.TERN_OK
+    gq1, sg1 = torch.empty_like(L.gq), torch.empty_like(L.sgrad)
+    bl.tern_linear_bwd(L.X, L.dY, L.tiles, L.scale, None, gq1, sg1, L.ws)
+    torch.cuda.synchronize()
+    assert torch.equal(gq1, L.gq) and torch.equal(sg1, L.sgrad)
+    sampled_oracle_check(L, n=1024, ncols=16)
