@@ -697,7 +697,7 @@ def run_ours(args):
     names = ["materialize", "fwd", "dx", "dw", "adamw"]
     step_no = [0]
 
-    def step(ev=None, Xs=None, dYs=None, tl=None, ws8=None):
+    def step(ev=None, Xs=None, dYs=None, tl=None, ws8=None, wsd=None):
         Xs = X if Xs is None else Xs
         dYs = dY if dYs is None else dYs
         tl = tiles if tl is None else tl
@@ -710,8 +710,8 @@ def run_ours(args):
         bl.tern_linear_fwd(Xs, tl, scale, Y)
         if ev is not None:
             ev[2].record(stream)
-        if ws8 is None:
-            bl.tern_linear_bwd(Xs, dYs, tl, scale, dX, None, None, None)
+        if ws8 is None:   # dX from the 2-bit codes takes a workspace for its s_hi / s_lo table
+            bl.tern_linear_bwd(Xs, dYs, tl, scale, dX, None, None, wsd)
         else:   # dX from the fp16 + e4m3 split: dY is split into ws8 first
             bl.tern_linear_bwd(Xs, dYs, tl, scale, dX, None, None, ws8, split8=True)
         if ev is not None:
@@ -803,6 +803,28 @@ def run_ours(args):
                "kernels_ms": per_o, "fwd_tflops": 2.0 * M * K * N / (per_o["fwd"] * 1e-3) / 1e12,
                "materialize_bytes_per_weight": 1 + 0.25 + (2 if other == "bf16" else 0) + 4}
     del tiles_o
+
+    # ---- the same step with dX's W_hi / W_lo expanded from the 2-bit codes inside the GEMM
+    #      (materialise then writes no hi/lo planes: 3.25 instead of 7.25 B per weight)
+    progress("step with dX from the 2-bit codes")
+    tiles_c = bl.Tiles.empty(K, N, t=(args.t_operand == "bf16"), hi_lo=False)
+    wsc = torch.empty(max(bl.tern_linear_bwd_workspace(M, K, N) // 4, N), device=dev)
+    for _ in range(3):
+        step(tl=tiles_c, wsd=wsc)
+    torch.cuda.synchronize()
+    evc = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        step(evc[i], tl=tiles_c, wsd=wsc)
+    torch.cuda.synchronize()
+    if bl.tern_device_status() != bl.TERN_OK:
+        raise RuntimeError("a kernel gave up on a bounded wait (dX from the 2-bit codes)")
+    per_c = {n: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evc) for j, n in enumerate(names)}
+    ms_c = evc[0][0].elapsed_time(evc[-1][5]) / args.steps
+    dxc = {"ms_per_step": ms_c, "tflops": flops / (ms_c * 1e-3) / 1e12, "kernels_ms": per_c,
+           "dx_tflops_credited": 2.0 * M * K * N / (per_c["dx"] * 1e-3) / 1e12,
+           "dx_ms_includes": "the s_hi / s_lo table (N columns) and the GEMM",
+           "materialize_bytes_per_weight": 1 + 0.25 + (2 if args.t_operand == "bf16" else 0)}
+    del tiles_c, wsc
 
     # ---- the same step with dX from the fp16 + e4m3 split (TERN_BWD_DX_SPLIT8): one
     #      binary16 and one e4m3 pass (1.5 bf16-pass equivalents executed) after a split of dY
@@ -921,6 +943,7 @@ def run_ours(args):
             "config": dict(large_config(M, K, N, ws), t_operand=args.t_operand),
             "other_t_operand": variant,
             "dx_split8": dx8,
+            "dx_from_codes": dxc,
             "frac_of_peak": {"spec_dense_bf16_2250": value / ws / SPEC_BF16_TFLOPS,
                              "measured_burst": value / ws / pk["bf16"],
                              "measured_sustained": value / ws / pk["bf16_sus"],

@@ -30,6 +30,9 @@ int gemm_status_read(int clear);
 int split8_planes(const int8_t* q, const float* scale, int64_t K, int64_t N, int theta, uint16_t* wh16,
                   uint8_t* wl8, int num_sms, cudaStream_t s);
 int64_t split8_dy_bytes(int64_t M, int64_t N);
+// s_hi / s_lo of every column as two bf16 arrays (hilo[0..N), hilo[N..2N)), for the dX
+// GEMM that expands W_hi / W_lo from the 2-bit codes (materialize.cu).
+int scale_hilo(const float* scale, int64_t N, uint16_t* hilo, cudaStream_t s);
 int split8_dy(const uint16_t* dY, const float* scale, int64_t M, int64_t N, void* ws, uint16_t** dy16, uint8_t** dy8,
               int** row_exp, cudaStream_t s);
 

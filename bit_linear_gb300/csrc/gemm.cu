@@ -165,7 +165,8 @@ struct Cfg {
     static_assert(BN % 64 == 0 && BN <= 256 && B_ROWS % 64 == 0, "BN");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of two");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
-    static_assert(!PK || (EPI == EPI_FWD && B_MN && NB == 1 && BK == 64), "packed operand: the forward's T");
+    static_assert(!PK || (EPI == EPI_FWD && B_MN && NB == 1 && BK == 64) || (EPI == EPI_DX && !B_MN && NB == 2 && BK == 64),
+                  "packed operand: the forward's T or dX's W_hi / W_lo");
     static_assert(!F8 || (EPI == EPI_DX && !A_MN && !B_MN && NB == 1 && BK == 64 && !PK), "fp16 + e4m3 split: dX");
 };
 
@@ -180,6 +181,9 @@ using Dw2 = Cfg<2, 256, 64, true, true, 1, EPI_DW, 7>;
 // The forward with T read as 2-bit codes.
 using FwdP1 = Cfg<1, 256, 64, false, true, 1, EPI_FWD, 4, true>;
 using FwdP2 = Cfg<2, 256, 64, false, true, 1, EPI_FWD, 6, true>;
+// dX with W_hi and W_lo expanded from the 2-bit codes and a per-column s_hi / s_lo table.
+using DxP1 = Cfg<1, 256, 64, false, false, 2, EPI_DX, 2, true>;
+using DxP2 = Cfg<2, 256, 64, false, false, 2, EPI_DX, 4, true>;
 // dX from the fp16 + e4m3 split.
 using Dx8_1 = Cfg<1, 256, 64, false, false, 1, EPI_DX, 3, false, true>;
 using Dx8_2 = Cfg<2, 256, 64, false, false, 1, EPI_DX, 4, false, true>;
@@ -360,7 +364,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const uint32_t
     const bool row_ok = row < a.Mg;
     const bool hi_ok = c0 + 16 < a.Ng;   // N is a multiple of 16: the chunk's second half may lie past it
     float v[32];
-    if constexpr (C::PK) {
+    if constexpr (C::PK && C::EPI == EPI_FWD) {
         // the converters store columns i and i+8 of each 16-column group as the bf16 pair at
         // positions 2i, 2i+1: accumulator column 2i holds column i, 2i+1 holds i+8
 #pragma unroll
@@ -535,7 +539,10 @@ __device__ __forceinline__ void gemm_body(const GRP& grp) {
                 if constexpr (C::PK) {   // this CTA's B rows as 2-bit codes, for its converters
                     const uint32_t pfull = PFULL0 + 8u * stage;
                     ptx::mbar_arrive_expect_tx(pfull, C::P_BYTES);
-                    ptx::tma_load_2d(pring0 + stage * C::P_BYTES, tmB0, brow / 16, k0, pfull);
+                    if constexpr (C::EPI == EPI_DX)   // K-major: rows of W, 16 contraction codes per word
+                        ptx::tma_load_2d(pring0 + stage * C::P_BYTES, tmB0, k0 / 16, brow, pfull);
+                    else
+                        ptx::tma_load_2d(pring0 + stage * C::P_BYTES, tmB0, brow / 16, k0, pfull);
                 }
                 if constexpr (C::A_MN) {
 #pragma unroll
@@ -689,6 +696,52 @@ __device__ __forceinline__ void gemm_body(const GRP& grp) {
                     ok = false;
                     break;
                 }
+                if constexpr (C::EPI == EPI_DX) {
+                    // K-major W_hi / W_lo: this thread's rows of W (ct, ct + 128, ...), each 64
+                    // contraction indices as four words of 16 codes; a 16-byte unit holds eight
+                    // consecutive indices c as bf16 pairs t*s_hi[c], t*s_lo[c] (the sign bit flipped
+                    // for t = -1, +0 for t = 0: the bits tern_materialize writes)
+                    const uint16_t* shi = reinterpret_cast<const uint16_t*>(a.packed);   // s_hi [Kg], s_lo after
+                    const uint16_t* slo = shi + a.Kg;
+                    const int c0 = kb * C::BK;
+                    const uint32_t sB = base + stage * C::STAGE_BYTES + C::A_BYTES;
+#pragma unroll
+                    for (int rr = 0; rr < C::B_ROWS / 128; ++rr) {
+                        const int r = ct + 128 * rr;
+                        uint32_t w[4];
+                        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                                     : "r"(pring0 + stage * C::P_BYTES + static_cast<uint32_t>(r) * 16u)
+                                     : "memory");
+                        const uint32_t rowoff = static_cast<uint32_t>(r >> 3) * 1024u + static_cast<uint32_t>(r & 7) * 128u;
+#pragma unroll
+                        for (int un = 0; un < 8; ++un) {
+                            uint4 h4 = make_uint4(0u, 0u, 0u, 0u), l4 = h4;
+                            if (c0 + 8 * un < a.Kg) {   // Kg % 16 == 0: the unit is wholly inside or outside
+                                h4 = __ldg(reinterpret_cast<const uint4*>(shi + c0 + 8 * un));
+                                l4 = __ldg(reinterpret_cast<const uint4*>(slo + c0 + 8 * un));
+                            }
+                            const uint32_t hp[4] = {h4.x, h4.y, h4.z, h4.w}, lp[4] = {l4.x, l4.y, l4.z, l4.w};
+                            const uint32_t w16 = w[un >> 1] >> (16 * (un & 1));
+                            uint32_t qh[4], ql[4];
+#pragma unroll
+                            for (int pr = 0; pr < 4; ++pr) {
+                                const uint32_t x = (w16 >> (4 * pr)) & 0xFu;   // codes of c and c + 1
+                                const uint32_t nz = ((x & 1u) | ((x & 4u) << 14)) * 0xFFFFu;
+                                const uint32_t ng = ((x & 2u) << 14) | ((x & 8u) << 28);
+                                qh[pr] = (hp[pr] & nz) ^ ng;
+                                ql[pr] = (lp[pr] & nz) ^ ng;
+                            }
+                            const uint32_t at = rowoff + (static_cast<uint32_t>(un ^ (r & 7)) << 4);
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sB + at), "r"(qh[0]),
+                                         "r"(qh[1]), "r"(qh[2]), "r"(qh[3])
+                                         : "memory");
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sB + C::B_BYTES + at),
+                                         "r"(ql[0]), "r"(ql[1]), "r"(ql[2]), "r"(ql[3])
+                                         : "memory");
+                        }
+                    }
+                } else {
                 const uint32_t src = pring0 + stage * C::P_BYTES + static_cast<uint32_t>(kr) * (C::B_ROWS / 16) * 4u +
                                      static_cast<uint32_t>(half) * WPT * 4u;
                 const uint32_t sB = base + stage * C::STAGE_BYTES + C::A_BYTES;
@@ -716,6 +769,7 @@ __device__ __forceinline__ void gemm_body(const GRP& grp) {
                                      "r"(q[4]), "r"(q[5]), "r"(q[6]), "r"(q[7])
                                      : "memory");
                     }
+                }
                 }
                 ptx::fence_proxy_async_smem();   // generic-proxy writes, read next by the tensor core
                 __syncwarp();
@@ -862,6 +916,13 @@ __global__ void __launch_bounds__(320, 1) tern_dx_gemm(const __grid_constant__ G
 template <int CG, int G>
 __global__ void __launch_bounds__(320, 1) tern_dw_gemm(const __grid_constant__ GemmGroup<G> grp) {
     gemm_body<std::conditional_t<CG == 2, Dw2, Dw1>>(grp);
+}
+
+// dX with W_hi / W_lo expanded from the 2-bit codes inside the GEMM (converter warps, as
+// the forward's tern_fwdp_gemm) and a per-column s_hi / s_lo table.
+template <int CG, int G>
+__global__ void __launch_bounds__(448, 1) tern_dxp_gemm(const __grid_constant__ GemmGroup<G> grp) {
+    gemm_body<std::conditional_t<CG == 2, DxP2, DxP1>>(grp);
 }
 
 // dX from the fp16 + e4m3 split (split8.cu): a binary16 pass and an e4m3 pass into one
@@ -1213,7 +1274,12 @@ template <class C, int G>
 int group_set(GemmGroup<G>& g, int p, const void* A, int64_t a_inner, int64_t a_outer, const void* B0,
               const void* B1, int64_t b_inner, int64_t b_outer, const GemmArgs& a) {
     if (int st = map_operand<C>(&g.mA[p], A, a_inner, a_outer, C::A_MN, kBM)) return st;
-    if constexpr (C::PK) {   // B as 2-bit codes [Kg][Ng/16] words, copied per stage for the converters
+    if constexpr (C::PK && C::EPI == EPI_DX) {   // W as 2-bit codes [Ng][Kg/16] words (K-major rows)
+        if (int st = encode_2d(&g.mB0[p], MapKey{a.bpacked, a.Kg / 16, a.Ng, C::BK / 16, C::B_ROWS,
+                                                 static_cast<int>(CU_TENSOR_MAP_SWIZZLE_NONE),
+                                                 static_cast<int>(CU_TENSOR_MAP_DATA_TYPE_UINT32)}))
+            return st;
+    } else if constexpr (C::PK) {   // B as 2-bit codes [Kg][Ng/16] words, copied per stage for the converters
         if (int st = encode_2d(&g.mB0[p], MapKey{a.bpacked, a.Ng / 16, a.Kg, C::B_ROWS / 16, C::BK,
                                                  static_cast<int>(CU_TENSOR_MAP_SWIZZLE_NONE),
                                                  static_cast<int>(CU_TENSOR_MAP_DATA_TYPE_UINT32)}))
@@ -1258,6 +1324,20 @@ int run_dx(K kernel, const uint16_t* dY, const uint16_t* whi, const uint16_t* wl
     GemmArgs a = make_args<C>(M, K_, N);
     a.out = dX;
     if (int st = group_set<C>(g, 0, dY, N, M, whi, wlo, N, K_, a)) return st;
+    group_close(g, 1);
+    return launch<C>(kernel, g, num_sms, s);
+}
+
+// dX from the 2-bit codes [K][N/16] and the s_hi / s_lo table (hilo: N bf16 s_hi, then N s_lo).
+template <class C, class K>
+int run_dxp(K kernel, const uint16_t* dY, const uint32_t* codes, const uint16_t* hilo, float* dX, int64_t M,
+            int64_t K_, int64_t N, int num_sms, cudaStream_t s) {
+    GemmGroup<1> g;
+    GemmArgs a = make_args<C>(M, K_, N);
+    a.out = dX;
+    a.bpacked = codes;
+    a.packed = reinterpret_cast<const uint32_t*>(hilo);
+    if (int st = group_set<C>(g, 0, dY, N, M, nullptr, nullptr, N, K_, a)) return st;
     group_close(g, 1);
     return launch<C>(kernel, g, num_sms, s);
 }
@@ -1465,7 +1545,9 @@ extern "C" int tern_linear_bwd_ex(const uint16_t* X, const uint16_t* dY, const t
     const int accumulate = (flags & TERN_BWD_ACCUMULATE) ? 1 : 0;
     if (!X || !dY || !W || !scale) return TERN_ERR_ARG;
     const bool split8 = dX != nullptr && (flags & TERN_BWD_DX_SPLIT8) != 0;
-    if (dX && !split8 && (!W->whi_bf16 || !W->wlo_bf16)) return TERN_ERR_ARG;
+    // without the hi/lo planes, dX expands them from the 2-bit codes inside the GEMM
+    const bool codes = dX != nullptr && !split8 && !W->whi_bf16 && !W->wlo_bf16 && W->packed;
+    if (dX && !split8 && !codes && (!W->whi_bf16 || !W->wlo_bf16)) return TERN_ERR_ARG;
     if (split8 && (!W->whi_f16 || !W->wlo_e4m3)) return TERN_ERR_ARG;
     if (sgrad && !W->packed) return TERN_ERR_ARG;
     if (!dX && !gq && !sgrad) return TERN_ERR_ARG;
@@ -1474,12 +1556,17 @@ extern "C" int tern_linear_bwd_ex(const uint16_t* X, const uint16_t* dY, const t
     if (!aligned16(X) || !aligned16(dY) || !aligned16(scale)) return TERN_ERR_ALIGN;
     if (sgrad && (!aligned16(sgrad) || !aligned16(W->packed) || !aligned16(workspace))) return TERN_ERR_ALIGN;
     if (gq && !aligned16(gq)) return TERN_ERR_ALIGN;
-    if (dX && !split8 && (!aligned16(dX) || !aligned16(W->whi_bf16) || !aligned16(W->wlo_bf16))) return TERN_ERR_ALIGN;
+    if (dX && !split8 && !codes && (!aligned16(dX) || !aligned16(W->whi_bf16) || !aligned16(W->wlo_bf16)))
+        return TERN_ERR_ALIGN;
+    // the codes' rows are copied by TMA: N / 16 words a row, a 16-byte multiple
+    if (codes && (!aligned16(dX) || !aligned16(W->packed) || N % 64 || (workspace && !aligned16(workspace))))
+        return TERN_ERR_ALIGN;
     if (split8 && (!aligned16(dX) || !aligned16(W->whi_f16) || !aligned16(W->wlo_e4m3) ||
                    (workspace && !aligned16(workspace))))
         return TERN_ERR_ALIGN;
     if (sgrad && (!workspace || ws_bytes < tern_linear_bwd_workspace_min(M, K, N))) return TERN_ERR_WORKSPACE;
     if (split8 && (!workspace || static_cast<int64_t>(ws_bytes) < split8_dy_bytes(M, N))) return TERN_ERR_WORKSPACE;
+    if (codes && (!workspace || static_cast<int64_t>(ws_bytes) < 4 * N)) return TERN_ERR_WORKSPACE;
     int num_sms = 0;
     if (int st = check_device(&num_sms)) return st;
     if (int st = gemm_setup(num_sms)) return st;
@@ -1496,6 +1583,14 @@ extern "C" int tern_linear_bwd_ex(const uint16_t* X, const uint16_t* dY, const t
                                                     M, K, N, num_sms, s)
                                    : run_dx8<Dx8_1>(tern_dx8_gemm<1, 1>, dy16, dy8, rexp, W->whi_f16, W->wlo_e4m3, dX,
                                                     M, K, N, num_sms, s);
+        if (st) return st;
+    } else if (codes) {
+        // the s_hi / s_lo table into the workspace, read only by this dX GEMM (the G GEMM
+        // below reuses the bytes after it on the same stream)
+        uint16_t* hilo = static_cast<uint16_t*>(workspace);
+        if (int st = scale_hilo(scale, N, hilo, s)) return st;
+        const int st = use_pair(M) ? run_dxp<DxP2>(tern_dxp_gemm<2, 1>, dY, W->packed, hilo, dX, M, K, N, num_sms, s)
+                                   : run_dxp<DxP1>(tern_dxp_gemm<1, 1>, dY, W->packed, hilo, dX, M, K, N, num_sms, s);
         if (st) return st;
     } else if (dX) {
         const int st = use_pair(M)
@@ -1894,6 +1989,8 @@ int gemm_setup(int num_sms) {
         gemm(persistent_units<FwdP1>(tern_fwdp_gemm<1, kGroup>, num_sms, &u));
         gemm(persistent_units<FwdP2>(tern_fwdp_gemm<2, kGroup>, num_sms, &u));
         gemm(persistent_units<Dx8_1>(tern_dx8_gemm<1, 1>, num_sms, &u));
+        gemm(persistent_units<DxP1>(tern_dxp_gemm<1, 1>, num_sms, &u));
+        gemm(persistent_units<DxP2>(tern_dxp_gemm<2, 1>, num_sms, &u));
         gemm(persistent_units<Dx8_2>(tern_dx8_gemm<2, 1>, num_sms, &u));
         cudaFuncAttributes fa;
         auto load = [&](cudaError_t e) {

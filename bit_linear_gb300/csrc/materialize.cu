@@ -220,6 +220,21 @@ __global__ void __launch_bounds__(256) tern_materialize_group_kernel(const __gri
                                      static_cast<int64_t>(nb) * blockDim.x);
 }
 
+// s_hi[c] = bf16(scale[c]) and s_lo[c] = bf16(scale[c] - s_hi[c]) as two bf16 arrays
+// (hilo[c], hilo[N + c]): the values the hi/lo planes carry, for the dX GEMM that expands
+// them from the 2-bit codes.
+__global__ void __launch_bounds__(256) tern_scale_hilo_kernel(const float* __restrict__ scale, int N,
+                                                               uint16_t* __restrict__ hilo) {
+    ptx::pdl_trigger();
+    ptx::pdl_wait();
+    const int c = static_cast<int>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (c >= N) return;
+    const float sv = scale[c];
+    const uint32_t hb = bf16_bits(sv);
+    hilo[c] = static_cast<uint16_t>(hb);
+    hilo[N + c] = static_cast<uint16_t>(bf16_bits(sv - __uint_as_float(hb << 16)));   // exact difference in fp32
+}
+
 namespace {
 
 template <bool QC, bool PK, bool TT, bool HL>
@@ -414,6 +429,13 @@ extern "C" int tern_materialize(const int8_t* q, int8_t* q_clamped, const float*
     if (s8) return split8_planes(q, scale, K, N, theta, out->whi_f16, out->wlo_e4m3, num_sms, s);
     return TERN_OK;
 }
+
+namespace tern {
+int scale_hilo(const float* scale, int64_t N, uint16_t* hilo, cudaStream_t s) {
+    return launch_pdl(tern_scale_hilo_kernel, dim3(static_cast<unsigned>((N + 255) / 256)), dim3(256), 0, s, scale,
+                      static_cast<int>(N), hilo);
+}
+}  // namespace tern
 
 extern "C" size_t tern_tiles_bytes(int64_t K, int64_t N, int which) {
     if (K < 1 || N < 16 || N % 16) return 0;

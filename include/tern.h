@@ -149,7 +149,11 @@ size_t tern_linear_bwd_workspace(int64_t M, int64_t K, int64_t N);
  * Backward (page "train_gpu.cu": the backward GEMMs are the off-page fm_backward;
  * tg_gq and tg_scale_grad give gq and sgrad from grad = X^T * dY).
  *   dX[m][r]  = sum_c dY[m][c] * scale[c] * T[r][c]   fp32 [M][K]  (NULL to skip)
- *               computed as dY*W_hi^T + dY*W_lo^T (reads W->whi_bf16, W->wlo_bf16)
+ *               computed as dY*W_hi^T + dY*W_lo^T (reads W->whi_bf16, W->wlo_bf16; with both
+ *               NULL it reads W->packed and expands W_hi / W_lo from the codes and a
+ *               per-column s_hi / s_lo table inside the GEMM: the same bits, so the same dX,
+ *               at the cost of converter work in the GEMM; then N % 64 == 0 (else
+ *               TERN_ERR_ALIGN) and a workspace of at least 4*N bytes are needed)
  *   gq[r][c]  = G[r][c] * scale[c], G = X^T * dY      fp32 [K][N]  (NULL to skip)
  *   sgrad[c]  = sum_r G[r][c] * T[r][c]               fp32 [N]    (NULL to skip;
  *               reads W->packed)

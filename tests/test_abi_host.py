@@ -99,9 +99,18 @@ def test_backward_argument_checks(lib):
     need = lib.tern_linear_bwd_workspace_min(64, 128, 128)
     assert f(*args(P(0x40000), P(0x70000), need - 4)) == lib.TERN_ERR_WORKSPACE
     assert f(*args(P(0x40000), None, need)) == lib.TERN_ERR_WORKSPACE
-    nohl = lib._Tiles(P(0x10000), P(0x11000), None, None)           # dX asked without W_hi/W_lo
-    assert f(P(0x20000), P(0x21000), ctypes.byref(nohl), P(0x30000), P(0x40000), P(0x50000), P(0x60000),
+    nohl = lib._Tiles(None, P(0x11000), None, None)                 # dX asked without W_hi/W_lo or codes
+    assert f(P(0x20000), P(0x21000), ctypes.byref(nohl), P(0x30000), P(0x40000), P(0x50000), None,
              P(0x70000), need, 64, 128, 128, None) == lib.TERN_ERR_ARG
+    onehl = lib._Tiles(P(0x10000), None, P(0x12000), None)         # one of the two planes only
+    assert f(P(0x20000), P(0x21000), ctypes.byref(onehl), P(0x30000), P(0x40000), None, None,
+             P(0x70000), need, 64, 128, 128, None) == lib.TERN_ERR_ARG
+    # the codes alone: dX expands W_hi / W_lo in the GEMM; N a multiple of 64 and a workspace
+    codes = lib._Tiles(P(0x10000), None, None, None)
+    assert f(P(0x20000), P(0x21000), ctypes.byref(codes), P(0x30000), P(0x40000), None, None,
+             P(0x70000), need, 64, 128, 48, None) == lib.TERN_ERR_ALIGN
+    assert f(P(0x20000), P(0x21000), ctypes.byref(codes), P(0x30000), P(0x40000), None, None,
+             None, 0, 64, 128, 128, None) == lib.TERN_ERR_WORKSPACE
     assert f(P(0x20000), P(0x21000), ctypes.byref(t), P(0x30000), P(0x40004), P(0x50000), P(0x60000),
              P(0x70000), need, 64, 128, 128, None) == lib.TERN_ERR_ALIGN
     assert f(P(0x20000), P(0x21000), ctypes.byref(t), P(0x30000), None, None, None,
@@ -128,7 +137,8 @@ def test_split8_backward_argument_checks(lib):
     bad = lib._Tiles(P(0x10000), None, None, None, P(0x14000), P(0x15001))
     assert call(bad, P(0x40000), P(0x70000), need, lib.TERN_BWD_DX_SPLIT8) == lib.TERN_ERR_ALIGN
     assert call(split8, P(0x40000), P(0x70000), need, 4) == lib.TERN_ERR_ARG          # unknown flag
-    assert call(split8, P(0x40000), P(0x70000), need, 0) == lib.TERN_ERR_ARG          # bf16 planes needed
+    only8 = lib._Tiles(None, None, None, None, P(0x14000), P(0x15000))
+    assert call(only8, P(0x40000), P(0x70000), need, 0) == lib.TERN_ERR_ARG   # without the flag: planes or codes
 
 
 def test_materialize_argument_checks(lib):
