@@ -250,6 +250,8 @@ int tern_linear_fwd_grouped(const tern_layer* layers, int count, void* stream);
  * single-layer call's; gq and sgrad equal it up to the order of fp32 sums.
  * dX_bf16 (with or without dX) receives dX rounded to bf16: the dY of the layer
  * before in a chain.
+ * A layer that asks for dX needs the hi/lo planes here (the expansion from the codes
+ * and the fp16 + e4m3 split are single-layer options of tern_linear_bwd_ex).
  * flags: 0 or TERN_BWD_ACCUMULATE (every layer).  Errors as tern_linear_bwd_ex;
  * a NULL workspace is TERN_ERR_WORKSPACE.
  */
